@@ -1,0 +1,439 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: a value the
+pages print, a hand-worked example of the pages' rules, a closed form, an
+invariant, exact arithmetic, or an independent library routine (numpy,
+torch CPU).  None of these tests touches the GPU or the product library.
+"""
+
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+F32, BF16, F16 = oracle.F32, oracle.BF16, oracle.F16
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------
+# A1 shard map
+
+
+def test_shard_map_worked_example():
+    g = _golden("shard_worked_example.json")
+    m = oracle.ShardMap([dict(numel=1024, dtype=BF16)], g["dp"], None)
+    (buf,) = m.buffers
+    assert len(buf.buckets) == 1 and buf.buckets[0].numel == g["bucket_numel"]
+    assert m.shard_numel(0) == g["elements_per_rank"]
+    for r, (a, b) in enumerate(g["world_ranges"]):
+        assert m.bucket_world_range(0, 0, r).as_tuple() == (a, b)
+        (view,) = m.rank_views(0, 0, r).values()
+        assert view["param"].as_tuple() == (a, b)
+        assert view["gbuf_local"].as_tuple() == (0, 256)
+
+
+def test_bucketing_hand_worked_cases():
+    for case in _golden("bucketing_hand.json")["cases"]:
+        nb = case.get("new_bucket", [False] * len(case["numels"]))
+        params = [dict(numel=n, dtype=BF16, new_bucket=f) for n, f in zip(case["numels"], nb)]
+        m = oracle.ShardMap(params, case["dp"], case["bucket_size"], False, case["busbw"])
+        (buf,) = m.buffers
+        got = [buf.index[i][:2] for i in range(len(params))]
+        assert [list(x) for x in got] == case["param_ranges"], case["why"]
+        assert [[b.offset, b.numel, b.numel_unpadded] for b in buf.buckets] == case["buckets"], case["why"]
+
+
+def _random_params(rng, n):
+    return [dict(numel=rng.randint(1, 300), dtype=rng.choice([BF16, F16, F32]),
+                 new_bucket=rng.random() < 0.1) for _ in range(n)]
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_shard_map_brute_force_invariants(seed):
+    rng = random.Random(seed)
+    params = _random_params(rng, rng.randint(1, 12))
+    dp = rng.randint(1, 8)
+    bucket_size = rng.choice([None, rng.randint(1, 2000)])
+    busbw = rng.random() < 0.2
+    m = oracle.ShardMap(params, dp, bucket_size, rng.random() < 0.5, busbw)
+    divisor = math.lcm(dp, 128, 2**16) if busbw else math.lcm(dp, 128)
+    seen_params = set()
+    for bi, buf in enumerate(m.buffers):
+        assert buf.numel % dp == 0 and buf.numel_unpadded <= buf.numel
+        # buckets tile the buffer contiguously, each a multiple of the divisor
+        pos = 0
+        for bk in buf.buckets:
+            assert bk.offset == pos and bk.numel % divisor == 0 and bk.numel_unpadded <= bk.numel
+            pos += bk.numel
+        assert pos == buf.numel
+        # params: 64-aligned starts, inside their bucket's unpadded part, no overlap,
+        # laid out in reverse model order
+        owner = np.full(buf.numel, -1)
+        starts = []
+        for pid in buf.params:
+            s, e, b = buf.index[pid]
+            bk = buf.buckets[b]
+            assert s % 64 == 0 and bk.offset <= s and e <= bk.offset + bk.numel_unpadded
+            assert (owner[s:e] == -1).all()
+            owner[s:e] = pid
+            starts.append(s)
+            seen_params.add(pid)
+        assert starts == sorted(starts, reverse=True)
+        # every buffer element has exactly one owning rank: (w - offset) // (numel/dp)
+        rank_of = np.full(buf.numel, -1)
+        for b, bk in enumerate(buf.buckets):
+            for r in range(dp):
+                rg = m.bucket_world_range(bi, b, r)
+                assert rg.size == bk.numel // dp
+                assert (rank_of[rg.start:rg.end] == -1).all()
+                rank_of[rg.start:rg.end] = r
+            w = np.arange(bk.offset, bk.offset + bk.numel)
+            assert (rank_of[w] == (w - bk.offset) // (bk.numel // dp)).all()
+        assert (rank_of >= 0).all()
+        # per param: the ranks' param views tile [0, numel) exactly once and the
+        # four views agree with each other
+        cover = {pid: np.zeros(params[pid]["numel"], dtype=int) for pid in buf.params}
+        for r in range(dp):
+            base = 0
+            for b, bk in enumerate(buf.buckets):
+                rg = m.bucket_world_range(bi, b, r)
+                for pid, v in m.rank_views(bi, b, r).items():
+                    s, e, _ = buf.index[pid]
+                    gw, gwb, gl, pr = (v["gbuf_world"], v["gbuf_world_in_bucket"],
+                                       v["gbuf_local"], v["param"])
+                    assert gw.size == gwb.size == gl.size == pr.size > 0
+                    assert gw.start - s == pr.start
+                    assert gwb.start == gw.start - bk.offset
+                    assert gl.start == gw.start - rg.start
+                    assert v["shard_offset"] == base + gl.start
+                    assert (rank_of[gw.start:gw.end] == r).all()
+                    cover[pid][pr.start:pr.end] += 1
+                base += bk.numel // dp
+        for pid, c in cover.items():
+            assert (c == 1).all()
+    assert seen_params == set(range(len(params)))
+
+
+def test_buffers_grouped_by_dtype_pair():
+    params = [dict(numel=10, dtype=BF16), dict(numel=10, dtype=F32), dict(numel=10, dtype=BF16)]
+    m = oracle.ShardMap(params, 2, None, grad_reduce_in_fp32=False)
+    assert [(b.param_dtype, b.grad_dtype, b.params) for b in m.buffers] == \
+        [(BF16, BF16, [0, 2]), (F32, F32, [1])]
+    m = oracle.ShardMap(params, 2, None, grad_reduce_in_fp32=True)
+    assert [(b.param_dtype, b.grad_dtype) for b in m.buffers] == [(BF16, F32), (F32, F32)]
+
+
+# --------------------------------------------------------------------------
+# 16-bit casts: round-to-nearest-even, against numpy / torch
+
+
+def test_rne_casts_match_libraries():
+    rng = np.random.RandomState(0)
+    x = np.concatenate([
+        (rng.standard_normal(100000) * 0.02).astype(np.float32),
+        (rng.standard_normal(20000) * 3e-5).astype(np.float32),
+        rng.uniform(-7e4, 7e4, 20000).astype(np.float32),
+        np.array([0.0, -0.0, 65504, 65519.996, 65520, 1e-8, 2**-24, 2**-25, 3 * 2**-26,
+                  6.1e-5, 2**-14, np.inf, -np.inf, 1e38, -3.4e38], np.float32)])
+    bf = oracle.round_bf16(x)
+    assert (bf == torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)).all()
+    with np.errstate(over="ignore"):
+        f16 = x.astype(np.float16).view(np.uint16)
+    assert (oracle.round_f16(x) == f16).all()
+    # ties to even: 1 + 2^-8 sits halfway between two bf16 values
+    assert oracle.round_bf16([1 + 2**-8])[0] == 0x3F80
+    assert oracle.round_bf16([1 + 3 * 2**-8])[0] == 0x3F82
+
+
+# --------------------------------------------------------------------------
+# A2 reduce-scatter semantics and A3 prepare
+
+
+def _exact_replicas(rng, n_rep, n, dtype=np.float32):
+    # small integers times 2^-12: every partial sum is exact in fp32, in any order
+    return [(rng.randint(-2000, 2000, n) * 2.0**-12).astype(dtype) for _ in range(n_rep)]
+
+
+@pytest.mark.parametrize("n_rep", [1, 2, 4, 8, 16])
+def test_reduce_exact_sum_and_prescale_equals_average(n_rep):
+    rng = np.random.RandomState(n_rep)
+    reps = _exact_replicas(rng, n_rep, 777)
+    exact = np.sum(np.stack(reps).astype(np.float64), axis=0) / n_rep
+    out, bad = oracle.reduce_prepare(reps, F32, 0, 777, 1.0)
+    assert bad == 0 and (out.astype(np.float64) == exact).all()
+    avg, _ = oracle.reduce_prepare(reps, F32, 0, 777, 1.0, average=True)
+    assert (avg == out).all()
+
+
+def test_reduce_hierarchical_matches_flat_on_exact_values():
+    rng = np.random.RandomState(7)
+    reps = _exact_replicas(rng, 16, 513)
+    flat, _ = oracle.reduce_prepare(reps, F32, 0, 513, 1.0)
+    for n_inst in (1, 2, 4):
+        h, _ = oracle.reduce_prepare(reps, F32, 0, 513, 1.0, n_inst=n_inst)
+        assert (h == flat).all()
+        ha, _ = oracle.reduce_prepare(reps, F32, 0, 513, 1.0, n_inst=n_inst, average=True)
+        assert (ha == flat).all()
+
+
+def test_reduce_rounds_once_to_grad_dtype():
+    rng = np.random.RandomState(3)
+    reps32 = [(rng.standard_normal(999) * 1e-3).astype(np.float32) for _ in range(8)]
+    for gdt, tdt in ((BF16, torch.bfloat16), (F16, torch.float16)):
+        reps = [torch.from_numpy(r).to(tdt) for r in reps32]
+        bits = [r.view(torch.int16).numpy().view(np.uint16) for r in reps]
+        out, _ = oracle.reduce_prepare(bits, gdt, 0, 999, 1.0)
+        # reference: widen exactly, fp32 sum in replica order (each term /8, exact),
+        # then one torch cast to the grad dtype
+        acc = reps[0].float() * 0.125
+        for r in reps[1:]:
+            acc = acc + r.float() * 0.125
+        want = acc.to(tdt).float().numpy()
+        assert (out == want).all()
+
+
+def test_prepare_unscale_and_inf_detection():
+    reps = [np.full(64, 65536.0 * 3, np.float32) for _ in range(4)]
+    out, bad = oracle.reduce_prepare(reps, F32, 0, 64, 1.0 / 65536)
+    assert bad == 0 and (out == 3.0).all()
+    for pos in (0, 31, 63):
+        for v in (np.inf, -np.inf, np.nan):
+            rr = [r.copy() for r in reps]
+            rr[2][pos] = v
+            _, bad = oracle.reduce_prepare(rr, F32, 0, 64, 1.0)
+            assert bad == 1
+
+
+def test_reduce_sign_of_zero():
+    reps = [np.full(8, -0.0, np.float32) for _ in range(4)]
+    out, _ = oracle.reduce_prepare(reps, F32, 0, 8, 1.0)
+    assert (np.signbit(out)).all()  # -0 + -0 = -0 in IEEE arithmetic
+
+
+# --------------------------------------------------------------------------
+# full step: norm, clip, AdamW, skip
+
+
+def _setup(params, dp, bucket_size=None, seed=0, layout="full", ranks=None, n_inst=1,
+           grad_fp32=True, grad_sigma=1e-3, warm=False):
+    m = oracle.ShardMap(params, dp, bucket_size, grad_fp32)
+    ranks = list(range(dp)) if ranks is None else ranks
+    n_rep = dp * n_inst
+    grads, state, pbufs = [], [], []
+    for bi, buf in enumerate(m.buffers):
+        S = m.shard_numel(bi)
+        kind = {F32: synth.OUT_F32, BF16: synth.OUT_BF16, F16: synth.OUT_F16}[buf.grad_dtype]
+        n = buf.numel if layout == "full" else S
+        grads.append([synth.normal(n, synth.key(seed, synth.STREAM_GRAD, 1, k), 0, grad_sigma, kind)
+                      for k in range(n_rep)])
+        pkind = {F32: synth.OUT_F32, BF16: synth.OUT_BF16, F16: synth.OUT_F16}[buf.param_dtype]
+        pk = synth.key(seed, synth.STREAM_PARAM, 0, 0)
+        pbufs.append(synth.normal(buf.numel, pk, 0, 0.02, pkind))
+        st = {"exp_avg": np.zeros(len(ranks) * S, np.float32),
+              "exp_avg_sq": np.zeros(len(ranks) * S, np.float32)}
+        if warm:
+            st["exp_avg"] = synth.normal(len(ranks) * S, synth.key(seed, synth.STREAM_EXP_AVG, 0, 0), 0, 1e-4)
+            st["exp_avg_sq"] = synth.uniform(len(ranks) * S, synth.key(seed, synth.STREAM_EXP_AVG_SQ, 0, 0), 0, 1e-6)
+        if buf.param_dtype != F32:
+            full = synth.normal(buf.numel, pk, 0, 0.02,
+                                synth.OUT_F32_OF_BF16 if buf.param_dtype == BF16 else synth.OUT_F32_OF_F16)
+            master = np.zeros(len(ranks) * S, np.float32)
+            for slot, r in enumerate(ranks):
+                for b in range(len(buf.buckets)):
+                    rg = m.bucket_world_range(bi, b, r)
+                    base = slot * S + m.bucket_shard_base(bi, b)
+                    master[base:base + rg.size] = full[rg.start:rg.end]
+            st["master"] = master
+        state.append(st)
+    return m, ranks, grads, state, pbufs
+
+
+def test_norm_closed_form():
+    # every main grad equal to c: norm = |c| * sqrt(n); chosen so sqrt is exact
+    n = 4**6
+    params = [dict(numel=n, dtype=BF16)]
+    m = oracle.ShardMap(params, 4, None, True)
+    c = 2.0**-7
+    grads = [[np.full(n, c, np.float32) for _ in range(4)]]  # avg of 4 equal replicas = c
+    st = [{"exp_avg": np.zeros(n, np.float32), "exp_avg_sq": np.zeros(n, np.float32),
+           "master": np.zeros(n, np.float32)}]
+    res = oracle.step(m, [0, 1, 2, 3], grads, st, [np.zeros(n, np.uint16)], W.HP, 1, max_norm=0.0)
+    assert res["norm"] == c * 2**6
+
+
+def test_norm_matches_library_vector_norm():
+    m, ranks, grads, st, pb = _setup(W.toy_mlp(blocks=1, d_in=96, d_hidden=80), 4, 5000)
+    res = oracle.step(m, ranks, grads, st, pb, W.HP, 1, max_norm=0.0)
+    allm = np.concatenate(res["main"]).astype(np.float64)
+    want = torch.linalg.vector_norm(torch.from_numpy(allm)).item()
+    assert abs(res["norm"] - want) <= 1e-12 * want
+
+
+def test_step_dp1_matches_torch_adamw_and_clip():
+    """DP=1 is a plain mixed-precision AdamW step: compare with torch's own
+    clip_grad_norm_ and AdamW(foreach=False) on CPU fp32 over several steps."""
+    params = [dict(numel=3000, dtype=F32), dict(numel=1001, dtype=F32)]
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    m = oracle.ShardMap(params, 1, None, True)
+    (buf,) = m.buffers
+    p0 = synth.normal(buf.numel, synth.key(5, synth.STREAM_PARAM, 0, 0), 0, 0.02)
+    tparams = [torch.nn.Parameter(torch.from_numpy(p0[s:e].copy()))
+               for s, e, _ in (buf.index[i] for i in range(2))]
+    opt = torch.optim.AdamW(tparams, lr=hp["lr"], betas=(hp["beta1"], hp["beta2"]),
+                            eps=hp["eps"], weight_decay=hp["weight_decay"], foreach=False)
+    pbuf = p0.copy()
+    st = [{"exp_avg": np.zeros(buf.numel, np.float32), "exp_avg_sq": np.zeros(buf.numel, np.float32)}]
+    for t in range(1, 6):
+        before = pbuf.copy()
+        g = synth.normal(buf.numel, synth.key(5, synth.STREAM_GRAD, t, 0), 0, 0.05)
+        max_norm = 1.0 if t % 2 else 1e9  # clipped and unclipped branches
+        res = oracle.step(m, [0], [[g]], st, [pbuf], hp, t, max_norm=max_norm)
+        for i, tp in enumerate(tparams):
+            s, e, _ = buf.index[i]
+            tp.grad = torch.from_numpy(g[s:e].copy())
+        tn = torch.nn.utils.clip_grad_norm_(tparams, max_norm)
+        assert abs(res["norm"] - tn.item()) <= 1e-6 * tn.item()
+        assert res["clip"] == (t % 2 == 1)
+        opt.step()
+        for i, tp in enumerate(tparams):
+            s, e, _ = buf.index[i]
+            # differences carried from earlier steps are absolute, so bound them
+            # by ulps of the tensor's scale rather than of each (possibly
+            # cancelled, tiny) element
+            got, want = pbuf[s:e], tp.detach().numpy()
+            tol = 4 * float(np.spacing(np.float32(np.abs(want).max())))
+            assert np.abs(got.astype(np.float64) - want).max() <= tol, t
+            if t == 1:  # no history yet: element-wise, in ulps of the operands
+                assert oracle.master_close(got, want, before[s:e], hp["lr"]).all()
+            # torch updates m with lerp (m + w*(g - m)), which rounds differently
+            # from beta1*m + (1-beta1)*g; the gap stays at rounding level
+            ea = opt.state[tp]["exp_avg"].numpy()
+            assert np.abs(st[0]["exp_avg"][s:e] - ea).max() <= 1e-5 * np.abs(ea).max(), t
+            va = opt.state[tp]["exp_avg_sq"].numpy()
+            assert oracle.float_ulp_diff(st[0]["exp_avg_sq"][s:e], va).max() <= 4, t
+
+
+def test_step1_closed_form_and_zero_grads():
+    """From m = v = 0 the first update is lr * g / (|g| + eps) after the decay
+    p * (1 - lr*wd); elements with g = 0 only decay."""
+    n = 4096
+    params = [dict(numel=n, dtype=BF16)]
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    m = oracle.ShardMap(params, 1, None, True)
+    g = synth.normal(n, synth.key(9, synth.STREAM_GRAD, 1, 0), 0, 1e-2)
+    g[::7] = 0.0
+    p0 = synth.normal(n, synth.key(9, synth.STREAM_PARAM, 0, 0), 0, 0.02, synth.OUT_F32_OF_BF16)
+    st = [{"master": p0.copy(), "exp_avg": np.zeros(n, np.float32), "exp_avg_sq": np.zeros(n, np.float32)}]
+    pb = np.zeros(n, np.uint16)
+    oracle.step(m, [0], [[g]], st, [pb], hp, 1, max_norm=0.0)
+    p0d, gd = p0.astype(np.float64), g.astype(np.float64)
+    want = p0d * (1 - hp["lr"] * hp["weight_decay"]) - hp["lr"] * gd / (np.abs(gd) + hp["eps"])
+    got = st[0]["master"].astype(np.float64)
+    assert np.abs(got - want).max() <= 4 * np.spacing(np.float32(0.1))
+    z = g == 0
+    decay = np.float32(1 - hp["lr"] * hp["weight_decay"])
+    assert (st[0]["master"][z] == p0[z] * decay).all()
+    assert (st[0]["exp_avg"][z] == 0).all() and (st[0]["exp_avg_sq"][z] == 0).all()
+    # the write-back is the RNE cast of the new master (pinned against torch above)
+    assert (pb == oracle.round_bf16(st[0]["master"])).all()
+
+
+@pytest.mark.parametrize("dp", [2, 4, 8])
+def test_sharding_invariance(dp):
+    """The union of all ranks' shards equals the DP=1 step, up to the norm's
+    summation order (coef within 1e-6): the shard map only decides who
+    updates an element, not how."""
+    params = W.llama(1, 64, 172, 77)
+    res = {}
+    for d in (1, dp):
+        m, ranks, _, st, pb = _setup(params, d, 3000, seed=21)
+        grads = []
+        for bi, buf in enumerate(m.buffers):
+            g = synth.normal(buf.numel, synth.key(21, synth.STREAM_GRAD, 1, 0), 0, 1e-2)
+            # replica 0 carries d*g, the others 0: the prescaled sum is exactly g
+            grads.append([g * np.float32(d)] + [np.zeros_like(g) for _ in range(d - 1)])
+        out = oracle.step(m, ranks, grads, st, pb, W.HP, 1)
+        per_param = {}
+        for bi, buf in enumerate(m.buffers):
+            S = m.shard_numel(bi)
+            for slot, r in enumerate(ranks):
+                for pid, b, v in m.rank_pieces(bi, r):
+                    arr = per_param.setdefault(pid, np.zeros(params[pid]["numel"], np.float32))
+                    lo = slot * S + v["shard_offset"]
+                    if "master" in st[bi]:
+                        piece = st[bi]["master"][lo:lo + v["param"].size]
+                    else:
+                        piece = pb[bi][v["gbuf_world"].start:v["gbuf_world"].end]
+                    arr[v["param"].start:v["param"].end] = piece
+        res[d] = (per_param, out["coef"])
+    (a, ca), (b, cb) = res[1], res[dp]
+    assert ca < 1 and abs(ca - cb) <= 1e-6 * ca
+    for pid in a:
+        assert oracle.float_ulp_diff(a[pid], b[pid]).max() <= 4
+
+
+def test_skip_leaves_state_untouched():
+    m, ranks, grads, st, pb = _setup(W.gpt2(layers=1, d=64, ffn=256, vocab=97, n_pos=33), 4, 9000,
+                                     warm=True)
+    before = [{k: v.copy() for k, v in s.items()} for s in st]
+    pbefore = [p.copy() for p in pb]
+    for bi in range(len(m.buffers)):
+        g = grads[bi][1]
+        g[len(g) // 2] = np.inf
+        res = oracle.step(m, ranks, grads, st, pb, W.HP, 1)
+        assert res["found_inf"] and math.isnan(res["norm"])
+        for s0, s1 in zip(before, st):
+            for k in s0:
+                assert s0[k].tobytes() == s1[k].tobytes()
+        for p0, p1 in zip(pbefore, pb):
+            assert p0.tobytes() == p1.tobytes()
+        g[len(g) // 2] = 0.0
+    res = oracle.step(m, ranks, grads, st, pb, W.HP, 1, remote_found_inf=True)
+    assert res["found_inf"]
+
+
+def test_stream_sumsq_equals_array_path():
+    n_rep = 8
+    keys = [synth.key(3, synth.STREAM_GRAD, 1, k) for k in range(n_rep)]
+    for gdt, kind in ((F32, synth.OUT_F32), (BF16, synth.OUT_BF16), (F16, synth.OUT_F16)):
+        reps = [synth.normal(5000, k, 1234, 1e-3, kind) for k in keys]
+        main, bad = oracle.reduce_prepare(reps, gdt, 0, 5000, 0.5)
+        s_arr = float(np.sum(main.astype(np.float64) ** 2))
+        s, b = oracle.stream_sumsq(keys, gdt, synth.factor(1e-3), 1234, 5000, 0.5)
+        assert bad == b == 0 and abs(s - s_arr) <= 1e-12 * s_arr
+
+
+# --------------------------------------------------------------------------
+# the seeded generator itself
+
+
+def test_generator_matches_published_splitmix64():
+    g = _golden("splitmix64_seed1234567.json")
+    L = synth.host()
+    assert [int(L.synth_bits_at(g["seed"], i)) for i in range(5)] == [int(x) for x in g["outputs"]]
+
+
+def test_generator_truncations_are_exact_16_bit_values():
+    k = synth.key(1, synth.STREAM_PARAM, 0, 0)
+    v = synth.normal(50000, k, 0, 0.02, synth.OUT_F32_OF_BF16)
+    b = synth.normal(50000, k, 0, 0.02, synth.OUT_BF16)
+    assert (v.view(np.uint32) >> 16 == b).all()
+    v16 = synth.normal(50000, k, 0, 0.02, synth.OUT_F32_OF_F16)
+    b16 = synth.normal(50000, k, 0, 0.02, synth.OUT_F16)
+    assert (b16.view(np.float16).astype(np.float32) == v16).all()
+    x = synth.normal(50000, k, 0, 0.02)
+    assert (np.abs(v16) <= np.abs(x)).all() and (np.abs(v) <= np.abs(x)).all()
+    assert abs(float(x.std()) - 0.02) < 5e-4
