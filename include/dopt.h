@@ -1,0 +1,342 @@
+/*
+ * dopt.h -- C ABI of the sharded mixed-precision Adam step on one GPU.
+ *
+ * The operation is the data-parallel hot path of a Megatron-style
+ * DistributedOptimizer (ZeRO-1) step over a contiguous param-and-grad buffer,
+ * as described by the "Megatron-LM distrib_optimizer.py close reading" page
+ * (xiaolong-dev.me, megatron-docs/optimizer/distrib_optimizer), the "ZeRO
+ * memory ledger and Megatron DistributedOptimizer" page (llm-infra-atlas,
+ * parallel/01_dp/02_zero_and_distributed_optimizer) and the "Megatron-LM
+ * distributed package" page (2kiu.com).  Citations below name the page and
+ * its section.
+ *
+ * Conventions (every entry point):
+ *  - Return value: DOPT_OK (0) or a negative dopt_status.  Nothing aborts and
+ *    no C++ exception crosses this boundary.  dopt_last_error() returns a
+ *    thread-local message describing the last failure.
+ *  - Device memory: every device pointer is allocated and owned by the
+ *    caller, must be 16-byte aligned and stays owned by the caller.  The
+ *    library allocates no device memory.  The only library-owned object is
+ *    the opaque shard map (host memory), freed by dopt_shard_map_free().
+ *  - Streams: a dopt_stream is a cudaStream_t passed as a plain pointer
+ *    (NULL = the legacy default stream).  Device entry points only enqueue
+ *    work on it and return; dopt_step() alone waits for its stream, to hand
+ *    back found_inf and the grad norm.
+ *  - Element counts are int64; dtypes are dopt_dtype codes.
+ *  - Rank selection: rank in [0, DP) steps that rank's shard; DOPT_ALL_RANKS
+ *    emulates every rank of the instance on this GPU, their shard arrays laid
+ *    out rank-major (rank r's slot begins at r * shard_numel).
+ *  - Flat shard layout: a rank's shard of a buffer is the concatenation, in
+ *    bucket order, of its slice of every bucket (dopt_bucket_info.shard_base
+ *    is where bucket b's slice starts).  main_grad, master, exp_avg and
+ *    exp_avg_sq use this layout.  Only elements of parameters are read or
+ *    written; padding positions of these arrays are never touched.
+ */
+#ifndef DOPT_H
+#define DOPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* dopt_stream; /* a cudaStream_t */
+
+typedef enum { DOPT_F32 = 0, DOPT_BF16 = 1, DOPT_F16 = 2 } dopt_dtype;
+
+typedef enum {
+  DOPT_OK = 0,
+  DOPT_E_INVALID = -1, /* bad argument (null, out of range, inconsistent)   */
+  DOPT_E_ALIGN = -2,   /* a device pointer is not 16-byte aligned            */
+  DOPT_E_SIZE = -3,    /* workspace too small, or a size exceeds a limit     */
+  DOPT_E_CUDA = -4,    /* a CUDA runtime call or kernel launch failed        */
+  DOPT_E_NOMEM = -5    /* host allocation failed                             */
+} dopt_status;
+
+/* Shard group of a buffer (distrib_optimizer page, "five groups"; ledger
+ * page, section 3): bf16/fp16 params get an fp32 master copy of their shard
+ * (shard_fp32_from_float16); fp32 params are stepped in place in the param
+ * buffer (shard_fp32). */
+typedef enum { DOPT_GROUP_FP32_FROM_FLOAT16 = 0, DOPT_GROUP_FP32 = 1 } dopt_group;
+
+/* Layout of the emulated replica gradient buffers. */
+typedef enum {
+  DOPT_LAYOUT_FULL_BUFFER = 0, /* each replica is a whole grad buffer (numel)   */
+  DOPT_LAYOUT_SHARD_ONLY = 1   /* each replica holds only the selected rank's
+                                  flat shard (shard_numel); one rank only      */
+} dopt_layout;
+
+#define DOPT_ALL_RANKS (-1)
+#define DOPT_MAX_REPLICAS 64
+
+/* Range: [start, end) -- distrib_optimizer page, "Range class". */
+typedef struct {
+  int64_t start, end;
+} dopt_range;
+
+/* One model parameter, in model (registration) order. */
+typedef struct {
+  int64_t numel;      /* >= 0                                                */
+  int32_t dtype;      /* dopt_dtype of the param                             */
+  int32_t new_bucket; /* nonzero: this param must start a bucket of its own
+                         (the page's _does_param_require_new_bucket)         */
+  double wd_mult;     /* weight-decay multiplier of this param (1.0 usual)   */
+} dopt_param_desc;
+
+typedef struct {
+  int32_t param_dtype, grad_dtype, group, n_buckets;
+  int32_t n_params, reserved;
+  int64_t numel;          /* padded buffer size, a multiple of DP            */
+  int64_t numel_unpadded; /* sum of the buckets' unpadded sizes              */
+  int64_t shard_numel;    /* numel / DP: one rank's flat shard               */
+} dopt_buffer_info;
+
+typedef struct {
+  int64_t offset;         /* bucket start in the buffer                      */
+  int64_t numel;          /* padded size, a multiple of lcm(DP,128)          */
+  int64_t numel_unpadded;
+  int64_t shard_numel;    /* numel / DP                                      */
+  int64_t shard_base;     /* start of this bucket's slice in a flat shard    */
+} dopt_bucket_info;
+
+/* The four views of one param piece owned by one rank (distrib_optimizer
+ * page, "Range class: four views", _build_model_gbuf_param_range_map), plus
+ * where the piece sits in the rank's flat shard. */
+typedef struct {
+  int32_t param, buffer, bucket, rank;
+  dopt_range gbuf_world;           /* in the whole buffer                    */
+  dopt_range gbuf_world_in_bucket; /* relative to the bucket's offset        */
+  dopt_range gbuf_local;           /* relative to the rank's bucket slice    */
+  dopt_range param_range;          /* inside the param's own flat tensor     */
+  int64_t shard_offset;            /* = bucket shard_base + gbuf_local.start */
+} dopt_param_shard;
+
+/* AdamW hyper-parameters, given like torch's Python floats (double).  step
+ * is the step number t used for bias correction when the step is applied
+ * (the count of applied steps so far plus one). */
+typedef struct {
+  double lr, beta1, beta2, eps, weight_decay;
+  int64_t step;
+} dopt_adamw_hparams;
+
+typedef struct dopt_shard_map dopt_shard_map; /* opaque, library-owned */
+
+/* ---------------------------------------------------------------------------
+ * Shard map (host only; no GPU needed).
+ */
+
+/*
+ * Builds the buffers, buckets and per-rank shards of a param list.
+ * distrib_optimizer page: "Buffer layout", "Bucket partition: reverse walk +
+ * size trigger", "Two levels of padding", "Final memory size assertions",
+ * "Bucket-level equal split"; distributed-package page, section 2.2 (2)-(3)
+ * (default bucket size, one buffer per (param dtype, grad dtype)).
+ *
+ *  params, n_params : model params in registration order (n_params >= 1).
+ *  dp_size          : data-parallel ranks sharing one optimizer instance.
+ *  bucket_size      : 0 = the default max(40000000, 1000000 * dp_size);
+ *                     < 0 = no size trigger (one bucket per buffer unless a
+ *                     param asks for a new one); > 0 = elements.
+ *  grad_reduce_in_fp32 : nonzero: every grad buffer is fp32; else the grad
+ *                     dtype is the param dtype.
+ *  pad_for_high_busbw  : nonzero: bucket ends are padded to
+ *                     lcm(DP, 128, 2^16) instead of lcm(DP, 128).
+ *  out              : receives the map; free it with dopt_shard_map_free.
+ * Errors: DOPT_E_INVALID (null, n_params < 1, dp_size < 1, negative numel,
+ * unknown dtype), DOPT_E_NOMEM.
+ */
+int dopt_build_shard_map(const dopt_param_desc* params, int32_t n_params, int32_t dp_size,
+                         int64_t bucket_size, int32_t grad_reduce_in_fp32,
+                         int32_t pad_for_high_busbw, dopt_shard_map** out);
+void dopt_shard_map_free(dopt_shard_map* map);
+
+int32_t dopt_num_buffers(const dopt_shard_map* map); /* < 0 on null map */
+int32_t dopt_dp_size(const dopt_shard_map* map);
+int dopt_buffer_info_get(const dopt_shard_map* map, int32_t buffer, dopt_buffer_info* out);
+int dopt_bucket_info_get(const dopt_shard_map* map, int32_t buffer, int32_t bucket,
+                         dopt_bucket_info* out);
+/* param_index_map[param] = (start, end, bucket) inside its buffer. */
+int dopt_param_index(const dopt_shard_map* map, int32_t param, int32_t* buffer,
+                     int64_t* start, int64_t* end, int32_t* bucket);
+/*
+ * The pieces of params that rank `rank` owns in `buffer`, in flat-shard
+ * order.  Writes at most `cap` entries to `out` (out may be NULL when cap is
+ * 0) and the total count to *count.
+ */
+int dopt_rank_shards(const dopt_shard_map* map, int32_t buffer, int32_t rank,
+                     dopt_param_shard* out, int32_t cap, int32_t* count);
+
+/* ---------------------------------------------------------------------------
+ * Device entry points.  `rank` is a rank or DOPT_ALL_RANKS; the workspace
+ * must be at least dopt_workspace_bytes(map, rank) bytes of device memory
+ * and is scratch owned by the caller (no initialisation needed).  A
+ * workspace may serve only one step at a time.
+ */
+size_t dopt_workspace_bytes(const dopt_shard_map* map, int32_t rank);
+
+/*
+ * Emulated reduce-scatter (step A2): for every element of the selected
+ * shard(s) of `buffer`, main_grad = fp32(round_grad_dtype(reduced sum)).
+ * distrib_optimizer page section 7.1 (start_grad_sync: reduce-scatter of
+ * each bucket's grad_data, output = this rank's shard); distributed-package
+ * page section 2.2 (4) (average_in_collective: prescale 1/dp_size and SUM,
+ * or AVG); ledger page section 5 (n_instances > 1: reduce-scatter inside
+ * each instance, all-reduce of the shards between instances).
+ *
+ *  replicas     : host array of n_replicas device pointers, replica k being
+ *                 rank k's grad buffer in the buffer's grad dtype; replica k
+ *                 belongs to instance k / DP.  n_replicas = DP * n_instances.
+ *  layout       : dopt_layout; DOPT_LAYOUT_SHARD_ONLY needs rank >= 0.
+ *  main_grad    : fp32 output, n_ranks * shard_numel (flat-shard layout).
+ * The replicas are summed in replica order, starting from the first term,
+ * each pre-scaled by 1/(DP*n_instances) (or summed and then averaged), and
+ * the sum is rounded once to the grad dtype (again after the inter-instance
+ * sum when n_instances > 1).
+ */
+int dopt_grad_reduce_shard(const dopt_shard_map* map, int32_t buffer, int32_t rank,
+                           const void* const* replicas, int32_t n_replicas,
+                           int32_t n_instances, int32_t layout, int32_t average_in_collective,
+                           float* main_grad, void* workspace, size_t workspace_bytes,
+                           dopt_stream stream);
+
+/*
+ * prepare_grads (step A3): main_grad *= inv_loss_scale in place, and records
+ * per-CTA partials (fp64 sum of squares, non-finite flag) of this buffer in
+ * the workspace for dopt_grad_norm.  distrib_optimizer page, the
+ * MixedPrecisionOptimizer step skeleton (copy to fp32 main grads, unscale,
+ * inf/NaN check).  Call it for every buffer before dopt_grad_norm.
+ */
+int dopt_prepare_grads(const dopt_shard_map* map, int32_t buffer, int32_t rank,
+                       float inv_loss_scale, float* main_grad, void* workspace,
+                       size_t workspace_bytes, dopt_stream stream);
+
+/*
+ * Global grad norm and clip coefficient (step A4): sums the partials of every
+ * buffer in a fixed order (deterministic), adds remote_sumsq / ORs
+ * remote_found_inf (the contribution of ranks not emulated here), and
+ * writes device scalars:
+ *   *d_norm      = sqrt(sumsq) as fp32, NaN when found_inf;
+ *   *d_clip_coef = max_norm / (norm + 1e-6) when max_norm > 0 and that is
+ *                  < 1, else 1 (computed in fp64, rounded once to fp32);
+ *   *d_found_inf = 1 if any main grad or the remote flag is non-finite.
+ * Any of the three pointers may be NULL.  distrib_optimizer page,
+ * MegatronOptimizer utilities (clip_grad_norm, get_grad_norm) and
+ * get_grad_stats_parallel_group (the norm spans the whole instance).
+ */
+int dopt_grad_norm(const dopt_shard_map* map, int32_t rank, void* workspace,
+                   size_t workspace_bytes, double remote_sumsq, int32_t remote_found_inf,
+                   double max_norm, float* d_norm, float* d_clip_coef, int32_t* d_found_inf,
+                   dopt_stream stream);
+
+/*
+ * AdamW on the fp32 shard and the write-back into the param buffer (steps A5
+ * and A6).  Per element, with g = main_grad * (*d_clip_coef):
+ *   p = p * (1 - lr*wd*wd_mult);  m = b1*m + (1-b1)*g;
+ *   v = b2*v + ((1-b2)*g)*g;      p = p - lr/(1-b1^t) * m/(sqrt(v)/sqrt(1-b2^t) + eps)
+ * then param_buffer[gbuf_world] = RNE cast of p (bf16/fp16 buffers).  For an
+ * fp32 buffer the master IS the param buffer (updated in place at the
+ * gbuf_world offsets) and `master` must be NULL.  If *d_found_inf is nonzero
+ * nothing is written (the step is skipped on the device).
+ * distrib_optimizer page: "Why a distributed optimizer" (fp32 master, m, v),
+ * the optimizer-type assertion (torch AdamW), step_with_ready_grads, and the
+ * _copy_main_params_to_model_params listing (fp32 -> bf16 copy into
+ * param_data at gbuf_world_in_bucket).
+ *  master, exp_avg, exp_avg_sq : fp32, n_ranks * shard_numel, flat layout.
+ *  param_buffer : the whole param buffer (numel) in the param dtype.
+ */
+int dopt_adam_step(const dopt_shard_map* map, int32_t buffer, int32_t rank,
+                   const float* main_grad, float* master, float* exp_avg, float* exp_avg_sq,
+                   void* param_buffer, const dopt_adamw_hparams* hp, const float* d_clip_coef,
+                   const int32_t* d_found_inf, dopt_stream stream);
+
+/* Everything one fused step needs; per-buffer arrays are host arrays indexed
+ * by buffer (length dopt_num_buffers). */
+typedef struct {
+  const dopt_shard_map* map;
+  int32_t rank;                   /* a rank or DOPT_ALL_RANKS                  */
+  int32_t n_instances;            /* >= 1; replicas = DP * n_instances         */
+  int32_t layout;                 /* dopt_layout of the replica grads          */
+  int32_t average_in_collective;
+  const void* const* const* replica_grads; /* [buffer][replica] device ptrs    */
+  float* const* main_grad;        /* [buffer] fp32 temporary                   */
+  float* const* master;           /* [buffer]; NULL for fp32 buffers           */
+  float* const* exp_avg;          /* [buffer]                                  */
+  float* const* exp_avg_sq;       /* [buffer]                                  */
+  void* const* param_buffer;      /* [buffer] whole param buffer               */
+  float inv_loss_scale;           /* 1 / loss scale (1 for bf16)               */
+  int32_t remote_found_inf;
+  double max_norm;                /* <= 0 disables clipping                    */
+  double remote_sumsq;
+  dopt_adamw_hparams hp;          /* hp.step = t of this step if applied       */
+  void* workspace;
+  size_t workspace_bytes;
+  dopt_stream stream;
+} dopt_step_args;
+
+/*
+ * One fused optimizer step (steps A2..A6): for every buffer, reduce the
+ * replicas, unscale, check inf/NaN and accumulate the sum of squares in one
+ * pass; then the global norm, clip coefficient and skip decision on the
+ * device; then AdamW and the write-back, skipped on the device when
+ * found_inf.  Waits for the stream, then returns *found_inf_out (0/1) and
+ * *grad_norm_out (NaN when skipped).  The caller advances its step count
+ * only when *found_inf_out is 0.  MixedPrecisionOptimizer.step skeleton of
+ * the distrib_optimizer page: prepare_grads -> (return on inf) ->
+ * clip_grad_norm -> step_with_ready_grads.
+ */
+int dopt_step(const dopt_step_args* args, int32_t* found_inf_out, float* grad_norm_out);
+
+/*
+ * The same step without waiting: the results stay on the device, in
+ * d_found_inf / d_norm (either may be NULL).  The caller decides when to
+ * read them.
+ */
+int dopt_step_async(const dopt_step_args* args, int32_t* d_found_inf, float* d_norm);
+
+/* ---------------------------------------------------------------------------
+ * Host arithmetic of the pages (no GPU).
+ */
+
+/*
+ * Per-card memory ledger with Adam and 16-bit params/grads, in bytes: ZeRO
+ * ledger page, section 2 table (DDP 16P, ZeRO-1 4P + 12P/N, ZeRO-2 2P +
+ * 14P/N, ZeRO-3 16P/N).  stage: 0 = DDP, 1..3 = ZeRO stage.  A sharded part
+ * holds ceil(P/N) elements per card.  parts_out (may be NULL) receives 5
+ * values: param, grad, master, exp_avg, exp_avg_sq bytes.  Returns the total,
+ * or a negative dopt_status.
+ */
+int64_t dopt_memory_ledger(int64_t P, int32_t N, int32_t stage, int64_t* parts_out);
+
+/*
+ * Bytes one rank sends in a ring collective over N ranks on a buffer of P
+ * elements of elem_bytes each, P padded up to a multiple of N: reduce-scatter
+ * and all-gather (N-1) * (P/N) * b, all-reduce twice that.  ZeRO ledger page,
+ * section 4 (reduce-scatter + all-gather = 2P = one all-reduce);
+ * distrib_optimizer page section 8.2.  kind: 0 = RS, 1 = AG, 2 = AR.
+ */
+int64_t dopt_comm_bytes(int64_t P, int32_t N, int32_t elem_bytes, int32_t kind);
+
+/* Dynamic loss scaler for fp16 (host state).  The pages give only the
+ * initial scale (2^16, the DeepSpeed config of the ipipp.com page); the
+ * policy is: on found_inf, count a hysteresis strike and, once `hysteresis`
+ * strikes are used up, multiply by backoff; after growth_interval clean
+ * steps in a row, multiply by growth and restore the hysteresis budget. */
+typedef struct {
+  double scale, growth_factor, backoff_factor, min_scale;
+  int32_t growth_interval, hysteresis;
+  int32_t growth_tracker, hysteresis_tracker;
+} dopt_loss_scaler;
+
+int dopt_loss_scaler_init(dopt_loss_scaler* s, double initial_scale, double growth_factor,
+                          double backoff_factor, int32_t growth_interval, int32_t hysteresis,
+                          double min_scale);
+int dopt_loss_scaler_update(dopt_loss_scaler* s, int32_t found_inf);
+
+const char* dopt_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DOPT_H */

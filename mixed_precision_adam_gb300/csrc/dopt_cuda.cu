@@ -1,0 +1,941 @@
+// dopt_cuda.cu -- device kernels and device entry points of the sharded
+// mixed-precision Adam step, for sm_103a.
+//
+// The step is three HBM-bound passes over the selected shard(s):
+//   K1 reduce_prepare : reads the N replica grads of every element, sums
+//                       them (emulated reduce-scatter), rounds to the grad
+//                       dtype, unscales, writes the fp32 main grad and keeps
+//                       per-CTA partials of the sum of squares and of the
+//                       non-finite flag.
+//   K2 finalize       : one CTA sums the partials in a fixed order and decides
+//                       norm, clip coefficient and skip on the device.
+//   K3 adamw          : reads main grad, master, m, v once, writes master, m,
+//                       v and the 16-bit param at its buffer offset once.
+// No tensor cores: nothing here is a contraction.  The work is described to
+// the kernels by a table of runs (contiguous in both the flat shard and the
+// buffer) passed by value as a __grid_constant__ kernel parameter, so a step
+// needs no host-to-device copy and no library-owned device memory.  Each run
+// is cut into tiles of kTile elements; CTAs take tiles round-robin.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "dopt_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;              // threads per CTA
+constexpr int kVec = 4;                    // contiguous elements per thread access
+constexpr int kUnroll = 2;                 // accesses per thread per tile
+constexpr int kTile = kThreads * kVec * kUnroll;  // elements per tile
+constexpr int kMaxSeg = 960;               // runs per launch (kernel-parameter table)
+constexpr int kMaxGrid = 2048;             // partial slots per launch region
+constexpr int kBatch = 8;                  // replicas loaded together
+constexpr size_t kScalarBytes = 256;
+
+constexpr int32_t kSegAligned = 1;  // local and world starts are multiples of 8
+
+struct Seg {
+  int64_t local;  // first element in the flat shard arrays (rank slot included)
+  int64_t world;  // first element in the buffer
+  int32_t len;    // elements
+  int32_t tile0;  // first tile of this run in the launch
+  float decay;    // (float)(1 - lr*wd*wd_mult); K3 only
+  int32_t flags;
+};
+static_assert(sizeof(Seg) == 32, "Seg layout");
+
+struct SegTable {
+  int32_t n_seg;
+  int32_t n_tiles;
+  Seg seg[kMaxSeg];
+};
+
+struct Partial {
+  double sumsq;
+  int32_t nonfinite;
+  int32_t pad;
+};
+static_assert(sizeof(Partial) == 16, "Partial layout");
+
+// Device scalars of one step, at the start of the workspace.
+struct Scalars {
+  double sumsq;
+  float norm;
+  float coef;
+  int32_t found_inf;
+  int32_t clip;
+};
+
+struct K1Params {
+  const void* rep[DOPT_MAX_REPLICAS];
+  float* main_grad;
+  Partial* partials;  // this launch's region of kMaxGrid slots (STATS only)
+  int32_t n_rep, n_inst;
+  float pre;        // (float)(1 / n_rep): prescale of average_in_collective = 0
+  float inv_dpi;    // (float)(1 / (n_rep / n_inst))
+  float inv_ninst;  // (float)(1 / n_inst)
+  float inv_scale;  // 1 / loss scale
+  int32_t average;
+  int32_t pad;
+  SegTable tab;
+};
+
+struct K3Params {
+  const float* main_grad;
+  float* master;      // flat shard, or NULL when the param buffer is the master
+  float* exp_avg;
+  float* exp_avg_sq;
+  void* param;        // the whole param buffer
+  const float* coef;  // device scalar
+  const int32_t* found_inf;
+  float b1, b2, omb1, omb2, eps, step_size, bc2_sqrt;
+  int32_t pad;
+  SegTable tab;
+};
+
+static_assert(sizeof(K1Params) <= 32764 && sizeof(K3Params) <= 32764, "kernel parameter limit");
+
+// ---------------------------------------------------------------- helpers --
+
+template <typename T>
+struct GradT;
+template <>
+struct GradT<float> {
+  static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
+    return __ldcs(static_cast<const float*>(p) + i);
+  }
+  static __device__ __forceinline__ void widen4(const void* p, int64_t i, float* x) {
+    float4 v = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+  static __device__ __forceinline__ float round_to(float s) { return s; }
+};
+template <>
+struct GradT<__nv_bfloat16> {
+  static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
+    unsigned short b = __ldcs(static_cast<const unsigned short*>(p) + i);
+    return __uint_as_float((unsigned)b << 16);
+  }
+  static __device__ __forceinline__ void widen4(const void* p, int64_t i, float* x) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  }
+  static __device__ __forceinline__ float round_to(float s) {
+    return __bfloat162float(__float2bfloat16_rn(s));
+  }
+};
+template <>
+struct GradT<__half> {
+  static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
+    unsigned short b = __ldcs(static_cast<const unsigned short*>(p) + i);
+    return __half2float(__ushort_as_half(b));
+  }
+  static __device__ __forceinline__ void widen4(const void* p, int64_t i, float* x) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+    x[0] = __half2float(__ushort_as_half((unsigned short)(v.x & 0xFFFFu)));
+    x[1] = __half2float(__ushort_as_half((unsigned short)(v.x >> 16)));
+    x[2] = __half2float(__ushort_as_half((unsigned short)(v.y & 0xFFFFu)));
+    x[3] = __half2float(__ushort_as_half((unsigned short)(v.y >> 16)));
+  }
+  static __device__ __forceinline__ float round_to(float s) {
+    return __half2float(__float2half_rn(s));
+  }
+};
+
+__device__ __forceinline__ bool is_nonfinite(float x) {
+  return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
+}
+
+// Advances the run cursor of a CTA to the run holding tile t (tiles visited
+// in increasing order, so the cursor only moves forward).
+__device__ __forceinline__ int seek(const SegTable& tab, int si, int t) {
+  while (si + 1 < tab.n_seg && tab.seg[si + 1].tile0 <= t) ++si;
+  return si;
+}
+
+// Reduction of one element over the replicas, in replica order, starting
+// from the first term; rounded to the grad dtype after each instance's sum
+// and again after the inter-instance sum.
+struct ReduceState {
+  float s, total;
+};
+
+// Where replica k sits in the reduction: its index inside its instance,
+// whether it opens / closes the instance's sum and whether its instance is
+// the first one.  The same for every element, so computed once per replica.
+struct ReplicaPos {
+  bool opens, closes, first_inst;
+};
+
+__device__ __forceinline__ ReplicaPos replica_pos(int k, int dpi) {
+  const int q = k % dpi;
+  return ReplicaPos{q == 0, q == dpi - 1, k < dpi};
+}
+
+template <typename GT>
+__device__ __forceinline__ void reduce_term(ReduceState& st, float x, ReplicaPos rp,
+                                            const K1Params& p) {
+  float term = p.average ? x : __fmul_rn(x, p.pre);
+  st.s = rp.opens ? term : __fadd_rn(st.s, term);
+  if (rp.closes) {
+    float s = p.average ? __fmul_rn(st.s, p.inv_dpi) : st.s;
+    s = GradT<GT>::round_to(s);
+    st.total = rp.first_inst ? s : __fadd_rn(st.total, s);
+  }
+}
+
+template <typename GT>
+__device__ __forceinline__ float reduce_finish(const ReduceState& st, const K1Params& p) {
+  float total = st.total;
+  if (p.n_inst > 1) {
+    if (p.average) total = __fmul_rn(total, p.inv_ninst);
+    total = GradT<GT>::round_to(total);
+  }
+  return __fmul_rn(total, p.inv_scale);
+}
+
+// Sum of squares of a thread's main grads, accurate to about fp64 while
+// computing in fp32: each square is split exactly into p + pe (FMA) and added
+// with the error-free TwoSum, the errors gathered in c (the Dot2 scheme of
+// Ogita, Rump & Oishi, "Accurate sum and dot product", SIAM J. Sci. Comput.
+// 2005).  Squares of |x| >= 2^62 would overflow fp32 and go to an fp64
+// accumulator instead; the fp32 pair is moved to fp64 before it could
+// overflow.
+struct SumSq {
+  float s = 0.f, c = 0.f;
+  double d = 0.0;
+  __device__ __forceinline__ void add(float x) {
+    if (fabsf(x) >= 0x1p62f) {
+      d += (double)x * (double)x;
+      return;
+    }
+    float p = __fmul_rn(x, x);
+    float pe = fmaf(x, x, -p);
+    float t = __fadd_rn(s, p);
+    float bp = __fsub_rn(t, s);
+    float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(e, pe));
+  }
+  __device__ __forceinline__ void maybe_flush() {
+    if (fabsf(s) > 0x1p100f) {
+      d += (double)s + (double)c;
+      s = c = 0.f;
+    }
+  }
+  __device__ __forceinline__ double value() const { return d + ((double)s + (double)c); }
+};
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------------- K1 --
+
+template <typename GT, bool FULL, bool STATS>
+__global__ void __launch_bounds__(kThreads) k1_reduce_prepare(const __grid_constant__ K1Params p) {
+  const int dpi = p.n_rep / p.n_inst;
+  SumSq acc;
+  int bad = 0;
+  int si = 0;
+  for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
+    si = seek(p.tab, si, t);
+    const Seg& sg = p.tab.seg[si];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTile;
+    const int n = (int)min((int64_t)kTile, (int64_t)sg.len - off);
+    const int64_t l0 = sg.local + off;
+    const int64_t r0 = FULL ? sg.world + off : l0;
+    const bool aligned = (sg.flags & kSegAligned) != 0;
+
+    ReduceState st[kUnroll][kVec];
+    bool vec_ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) vec_ok[u] = aligned && ((u * kThreads + threadIdx.x) * kVec + kVec <= n);
+
+    // vector path: kBatch replicas x kUnroll accesses of kVec elements in flight
+    for (int k0 = 0; k0 < p.n_rep; k0 += kBatch) {
+      float x[kBatch][kUnroll][kVec];
+#pragma unroll
+      for (int kk = 0; kk < kBatch; ++kk) {
+        if (k0 + kk < p.n_rep) {
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int e = (u * kThreads + threadIdx.x) * kVec;
+            if (vec_ok[u]) GradT<GT>::widen4(p.rep[k0 + kk], r0 + e, x[kk][u]);
+          }
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kBatch; ++kk) {
+        if (k0 + kk < p.n_rep) {
+          const ReplicaPos rp = replica_pos(k0 + kk, dpi);
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            if (vec_ok[u]) {
+#pragma unroll
+              for (int j = 0; j < kVec; ++j) reduce_term<GT>(st[u][j], x[kk][u][j], rp, p);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (vec_ok[u]) {
+        float m[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) m[j] = reduce_finish<GT>(st[u][j], p);
+        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        if (STATS) {
+#pragma unroll
+          for (int j = 0; j < kVec; ++j) {
+            bad |= is_nonfinite(m[j]);
+            acc.add(m[j]);
+          }
+        }
+      } else if (e < n) {
+        // scalar path: the ragged end of a run, or a run whose starts are
+        // not 8-element aligned
+        const int cnt = min(kVec, n - e);
+        for (int j = 0; j < cnt; ++j) {
+          ReduceState s1;
+          s1.s = 0.f;
+          s1.total = 0.f;
+          for (int k = 0; k < p.n_rep; ++k)
+            reduce_term<GT>(s1, GradT<GT>::widen1(p.rep[k], r0 + e + j), replica_pos(k, dpi), p);
+          float m = reduce_finish<GT>(s1, p);
+          p.main_grad[l0 + e + j] = m;
+          if (STATS) {
+            bad |= is_nonfinite(m);
+            acc.add(m);
+          }
+        }
+      }
+    }
+    if (STATS) acc.maybe_flush();
+  }
+
+  if (STATS) {
+    __shared__ double s_sum[kThreads / 32];
+    __shared__ int s_bad[kThreads / 32];
+    double v = warp_sum(acc.value());
+    int b = __any_sync(0xFFFFFFFFu, bad);
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (lane == 0) {
+      s_sum[w] = v;
+      s_bad[w] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double tot = 0.0;
+      int any = 0;
+      for (int i = 0; i < kThreads / 32; ++i) {
+        tot += s_sum[i];
+        any |= s_bad[i];
+      }
+      p.partials[blockIdx.x] = Partial{tot, any, 0};
+      // slots this launch does not use are zeroed, so the finalize pass can
+      // always sum whole regions
+      for (int i = gridDim.x + blockIdx.x; i < kMaxGrid; i += gridDim.x)
+        p.partials[i] = Partial{0.0, 0, 0};
+    }
+  }
+}
+
+// ------------------------------------------------------------------- K2 --
+
+__global__ void __launch_bounds__(kThreads)
+k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
+            int remote_found_inf, double max_norm, Scalars* __restrict__ sc,
+            float* d_norm, float* d_coef, int32_t* d_found) {
+  __shared__ double s_sum[kThreads];
+  __shared__ int s_bad[kThreads];
+  double v = 0.0;
+  int b = 0;
+  for (int i = threadIdx.x; i < n_slots; i += kThreads) {
+    v += parts[i].sumsq;
+    b |= parts[i].nonfinite;
+  }
+  s_sum[threadIdx.x] = v;
+  s_bad[threadIdx.x] = b;
+  __syncthreads();
+  for (int w = kThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
+      s_bad[threadIdx.x] |= s_bad[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double sumsq = s_sum[0] + remote_sumsq;
+    const int found = (s_bad[0] || remote_found_inf) ? 1 : 0;
+    const double norm = sqrt(sumsq);
+    double coef = 1.0;
+    int clip = 0;
+    if (max_norm > 0.0) {
+      coef = max_norm / (norm + 1.0e-6);
+      clip = coef < 1.0;
+    }
+    const float coef_f = clip ? (float)coef : 1.0f;
+    const float norm_f = found ? __int_as_float(0x7FC00000) : (float)norm;
+    sc->sumsq = sumsq;
+    sc->norm = norm_f;
+    sc->coef = coef_f;
+    sc->found_inf = found;
+    sc->clip = clip;
+    if (d_norm) *d_norm = norm_f;
+    if (d_coef) *d_coef = coef_f;
+    if (d_found) *d_found = found;
+  }
+}
+
+// ------------------------------------------------------------------- K3 --
+
+template <typename PT>
+struct ParamT;
+template <>
+struct ParamT<__nv_bfloat16> {
+  static constexpr bool kInPlace = false;
+  static __device__ __forceinline__ void store4(void* p, int64_t i, const float* x) {
+    unsigned short h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __bfloat16_as_ushort(__float2bfloat16_rn(x[j]));
+    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i),
+           make_uint2((unsigned)h[0] | ((unsigned)h[1] << 16), (unsigned)h[2] | ((unsigned)h[3] << 16)));
+  }
+  static __device__ __forceinline__ void store1(void* p, int64_t i, float x) {
+    static_cast<unsigned short*>(p)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  }
+};
+template <>
+struct ParamT<__half> {
+  static constexpr bool kInPlace = false;
+  static __device__ __forceinline__ void store4(void* p, int64_t i, const float* x) {
+    unsigned short h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__float2half_rn(x[j]));
+    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i),
+           make_uint2((unsigned)h[0] | ((unsigned)h[1] << 16), (unsigned)h[2] | ((unsigned)h[3] << 16)));
+  }
+  static __device__ __forceinline__ void store1(void* p, int64_t i, float x) {
+    static_cast<unsigned short*>(p)[i] = __half_as_ushort(__float2half_rn(x));
+  }
+};
+template <>
+struct ParamT<float> {
+  static constexpr bool kInPlace = true;  // the fp32 param buffer is the master
+  static __device__ __forceinline__ void store4(void*, int64_t, const float*) {}
+  static __device__ __forceinline__ void store1(void*, int64_t, float) {}
+};
+
+// One element of AdamW, in the order of the reference arithmetic.
+__device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, float& w, float& m,
+                                       float& v) {
+  float pp = __fmul_rn(w, decay);
+  float mm = __fadd_rn(__fmul_rn(p.b1, m), __fmul_rn(p.omb1, g));
+  float vv = __fadd_rn(__fmul_rn(p.b2, v), __fmul_rn(__fmul_rn(p.omb2, g), g));
+  float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(vv), p.bc2_sqrt), p.eps);
+  pp = __fsub_rn(pp, __fmul_rn(p.step_size, __fdiv_rn(mm, denom)));
+  w = pp;
+  m = mm;
+  v = vv;
+}
+
+template <typename PT>
+__global__ void __launch_bounds__(kThreads) k3_adamw(const __grid_constant__ K3Params p) {
+  if (*p.found_inf) return;  // skipped step: nothing is written
+  const float c = *p.coef;
+  float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
+  int si = 0;
+  for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
+    si = seek(p.tab, si, t);
+    const Seg& sg = p.tab.seg[si];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTile;
+    const int n = (int)min((int64_t)kTile, (int64_t)sg.len - off);
+    const int64_t l0 = sg.local + off, w0 = sg.world + off;
+    const int64_t m0 = ParamT<PT>::kInPlace ? w0 : l0;  // master index
+    const bool aligned = (sg.flags & kSegAligned) != 0;
+    const float decay = sg.decay;
+
+    float g[kUnroll][kVec], w[kUnroll][kVec], m[kUnroll][kVec], v[kUnroll][kVec];
+    bool vec_ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      vec_ok[u] = aligned && e + kVec <= n;
+      if (vec_ok[u]) {
+        float4 a = __ldcs(reinterpret_cast<const float4*>(p.main_grad + l0 + e));
+        float4 b = __ldcs(reinterpret_cast<const float4*>(wbase + m0 + e));
+        float4 cc = __ldcs(reinterpret_cast<const float4*>(p.exp_avg + l0 + e));
+        float4 d = __ldcs(reinterpret_cast<const float4*>(p.exp_avg_sq + l0 + e));
+        g[u][0] = a.x; g[u][1] = a.y; g[u][2] = a.z; g[u][3] = a.w;
+        w[u][0] = b.x; w[u][1] = b.y; w[u][2] = b.z; w[u][3] = b.w;
+        m[u][0] = cc.x; m[u][1] = cc.y; m[u][2] = cc.z; m[u][3] = cc.w;
+        v[u][0] = d.x; v[u][1] = d.y; v[u][2] = d.z; v[u][3] = d.w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (vec_ok[u]) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[u][j], c), decay, p, w[u][j], m[u][j], v[u][j]);
+        __stcs(reinterpret_cast<float4*>(wbase + m0 + e), make_float4(w[u][0], w[u][1], w[u][2], w[u][3]));
+        __stcs(reinterpret_cast<float4*>(p.exp_avg + l0 + e), make_float4(m[u][0], m[u][1], m[u][2], m[u][3]));
+        __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + l0 + e), make_float4(v[u][0], v[u][1], v[u][2], v[u][3]));
+        ParamT<PT>::store4(p.param, w0 + e, w[u]);
+      } else if (e < n) {
+        const int cnt = min(kVec, n - e);
+        for (int j = 0; j < cnt; ++j) {
+          float ww = wbase[m0 + e + j], mm = p.exp_avg[l0 + e + j], vv = p.exp_avg_sq[l0 + e + j];
+          adamw1(__fmul_rn(p.main_grad[l0 + e + j], c), decay, p, ww, mm, vv);
+          wbase[m0 + e + j] = ww;
+          p.exp_avg[l0 + e + j] = mm;
+          p.exp_avg_sq[l0 + e + j] = vv;
+          ParamT<PT>::store1(p.param, w0 + e + j, ww);
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ host side --
+
+thread_local std::vector<char> t_param_scratch;  // kernel-parameter staging
+
+// The run table of one launch: runs [first, first + count) of a rank
+// selection, with per-run decay for K3.
+struct Chunk {
+  int first, count, n_tiles;
+};
+
+std::vector<Chunk> chunks_of(const std::vector<dopt::Run>& runs) {
+  std::vector<Chunk> out;
+  int i = 0;
+  do {
+    Chunk c{i, 0, 0};
+    while (i < (int)runs.size() && c.count < kMaxSeg) {
+      c.n_tiles += (int)((runs[i].len + kTile - 1) / kTile);
+      ++c.count;
+      ++i;
+    }
+    out.push_back(c);
+  } while (i < (int)runs.size());
+  return out;  // at least one (possibly empty) chunk
+}
+
+void fill_table(SegTable& tab, const std::vector<dopt::Run>& runs, const Chunk& c, double lr,
+                double wd) {
+  tab.n_seg = c.count;
+  int tile = 0;
+  for (int k = 0; k < c.count; ++k) {
+    const dopt::Run& r = runs[c.first + k];
+    Seg& s = tab.seg[k];
+    s.local = r.local;
+    s.world = r.world;
+    s.len = (int32_t)r.len;
+    s.tile0 = tile;
+    s.decay = (float)(1.0 - lr * wd * r.wd_mult);
+    s.flags = ((r.local % 8) == 0 && (r.world % 8) == 0) ? kSegAligned : 0;
+    tile += (int)((r.len + kTile - 1) / kTile);
+  }
+  tab.n_tiles = tile;
+}
+
+struct DeviceInfo {
+  int device = -1, sms = 0;
+};
+
+int device_sms(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  static thread_local DeviceInfo cache;
+  if (cache.device != dev) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+      return dopt::fail(DOPT_E_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    cache.device = dev;
+    cache.sms = n;
+  }
+  *sms = cache.sms;
+  return DOPT_OK;
+}
+
+template <typename K>
+int grid_for(K kernel, int n_tiles, int* grid) {
+  int sms = 0;
+  int st = device_sms(&sms);
+  if (st) return st;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+  if (e != cudaSuccess)
+    return dopt::fail(DOPT_E_CUDA, std::string("occupancy query: ") + cudaGetErrorString(e));
+  int g = std::max(1, per_sm) * sms;
+  g = std::min(g, kMaxGrid);
+  g = std::min(g, std::max(1, n_tiles));
+  *grid = g;
+  return DOPT_OK;
+}
+
+int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  return DOPT_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_map_buffer_rank(const dopt_shard_map* m, int32_t buffer, int32_t rank, const char* fn) {
+  if (!m) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL map");
+  if (buffer < 0 || buffer >= (int32_t)m->buffers.size())
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": buffer out of range");
+  if (rank != DOPT_ALL_RANKS && (rank < 0 || rank >= m->dp))
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": rank out of range");
+  return DOPT_OK;
+}
+
+// Workspace layout: [Scalars | pad to 256] then, per buffer, per launch chunk
+// of its run table, a region of kMaxGrid Partial slots.
+int regions_before(dopt_shard_map* m, int32_t buffer, int32_t rank) {
+  int n = 0;
+  for (int32_t b = 0; b < buffer; ++b) n += (int)chunks_of(dopt::runs_for(m, b, rank)).size();
+  return n;
+}
+
+int total_regions(dopt_shard_map* m, int32_t rank) {
+  return regions_before(m, (int32_t)m->buffers.size(), rank);
+}
+
+size_t workspace_bytes(dopt_shard_map* m, int32_t rank) {
+  return kScalarBytes + (size_t)total_regions(m, rank) * kMaxGrid * sizeof(Partial);
+}
+
+int check_workspace(dopt_shard_map* m, int32_t rank, void* ws, size_t bytes, const char* fn) {
+  if (!ws) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL workspace");
+  if (!aligned16(ws)) return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": workspace not 16-byte aligned");
+  size_t need = workspace_bytes(m, rank);
+  if (bytes < need)
+    return dopt::fail(DOPT_E_SIZE, std::string(fn) + ": workspace needs " + std::to_string(need) +
+                                       " bytes, got " + std::to_string(bytes));
+  return DOPT_OK;
+}
+
+Partial* region_ptr(void* ws, int region) {
+  return reinterpret_cast<Partial*>(static_cast<char*>(ws) + kScalarBytes) + (size_t)region * kMaxGrid;
+}
+Scalars* scalars_ptr(void* ws) { return static_cast<Scalars*>(ws); }
+
+K1Params& k1_scratch() {
+  t_param_scratch.resize(std::max(sizeof(K1Params), sizeof(K3Params)));
+  return *reinterpret_cast<K1Params*>(t_param_scratch.data());
+}
+K3Params& k3_scratch() {
+  t_param_scratch.resize(std::max(sizeof(K1Params), sizeof(K3Params)));
+  return *reinterpret_cast<K3Params*>(t_param_scratch.data());
+}
+
+template <typename GT, bool FULL, bool STATS>
+int launch_k1_t(K1Params& kp, int n_tiles, cudaStream_t s) {
+  auto kern = k1_reduce_prepare<GT, FULL, STATS>;
+  int grid = 0;
+  int st = grid_for(kern, n_tiles, &grid);
+  if (st) return st;
+  kern<<<grid, kThreads, 0, s>>>(kp);
+  return check_launch("k1_reduce_prepare launch");
+}
+
+template <bool FULL, bool STATS>
+int launch_k1_dt(int32_t gdt, K1Params& kp, int n_tiles, cudaStream_t s) {
+  switch (gdt) {
+    case DOPT_F32: return launch_k1_t<float, FULL, STATS>(kp, n_tiles, s);
+    case DOPT_BF16: return launch_k1_t<__nv_bfloat16, FULL, STATS>(kp, n_tiles, s);
+    case DOPT_F16: return launch_k1_t<__half, FULL, STATS>(kp, n_tiles, s);
+  }
+  return dopt::fail(DOPT_E_INVALID, "unknown grad dtype");
+}
+
+// Launches K1 over every chunk of (buffer, rank).  stats: write partials to
+// the buffer's regions of the workspace.
+int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* replicas,
+           int32_t n_rep, int32_t n_inst, int32_t full_layout, int32_t average, float inv_scale,
+           int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s) {
+  const std::vector<dopt::Run>& runs = dopt::runs_for(m, buffer, rank);
+  std::vector<Chunk> chunks = chunks_of(runs);
+  int region = stats ? regions_before(m, buffer, rank) : 0;
+  for (const Chunk& c : chunks) {
+    K1Params& kp = k1_scratch();
+    for (int k = 0; k < n_rep; ++k) kp.rep[k] = replicas[k];
+    for (int k = n_rep; k < DOPT_MAX_REPLICAS; ++k) kp.rep[k] = nullptr;
+    kp.main_grad = main_grad;
+    kp.partials = stats ? region_ptr(ws, region++) : nullptr;
+    kp.n_rep = n_rep;
+    kp.n_inst = n_inst;
+    kp.pre = (float)(1.0 / (double)n_rep);
+    kp.inv_dpi = (float)(1.0 / (double)(n_rep / n_inst));
+    kp.inv_ninst = (float)(1.0 / (double)n_inst);
+    kp.inv_scale = inv_scale;
+    kp.average = average ? 1 : 0;
+    kp.pad = 0;
+    fill_table(kp.tab, runs, c, 0.0, 0.0);
+    int st;
+    if (stats)
+      st = full_layout ? launch_k1_dt<true, true>(gdt, kp, c.n_tiles, s)
+                       : launch_k1_dt<false, true>(gdt, kp, c.n_tiles, s);
+    else
+      st = full_layout ? launch_k1_dt<true, false>(gdt, kp, c.n_tiles, s)
+                       : launch_k1_dt<false, false>(gdt, kp, c.n_tiles, s);
+    if (st) return st;
+  }
+  return DOPT_OK;
+}
+
+int run_k2(dopt_shard_map* m, int32_t rank, void* ws, double remote_sumsq, int32_t remote_found,
+           double max_norm, float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
+  int n_slots = total_regions(m, rank) * kMaxGrid;
+  k2_finalize<<<1, kThreads, 0, s>>>(region_ptr(ws, 0), n_slots, remote_sumsq, remote_found ? 1 : 0,
+                                     max_norm, scalars_ptr(ws), d_norm, d_coef, d_found);
+  return check_launch("k2_finalize launch");
+}
+
+int check_hparams(const dopt_adamw_hparams* hp, const char* fn) {
+  if (!hp) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL hparams");
+  bool ok = hp->step >= 1 && std::isfinite(hp->lr) && hp->lr >= 0 && hp->beta1 >= 0 &&
+            hp->beta1 < 1 && hp->beta2 >= 0 && hp->beta2 < 1 && std::isfinite(hp->eps) &&
+            hp->eps > 0 && std::isfinite(hp->weight_decay);
+  if (!ok) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": bad AdamW hyper-parameters");
+  return DOPT_OK;
+}
+
+// beta^t by binary powering in double.
+double pow_int(double b, int64_t t) {
+  double r = 1.0, x = b;
+  while (t > 0) {
+    if (t & 1) r *= x;
+    x *= x;
+    t >>= 1;
+  }
+  return r;
+}
+
+template <typename PT>
+int launch_k3_t(K3Params& kp, int n_tiles, cudaStream_t s) {
+  auto kern = k3_adamw<PT>;
+  int grid = 0;
+  int st = grid_for(kern, n_tiles, &grid);
+  if (st) return st;
+  kern<<<grid, kThreads, 0, s>>>(kp);
+  return check_launch("k3_adamw launch");
+}
+
+int run_k3(dopt_shard_map* m, int32_t buffer, int32_t rank, const float* main_grad, float* master,
+           float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
+           const float* d_coef, const int32_t* d_found, cudaStream_t s) {
+  const std::vector<dopt::Run>& runs = dopt::runs_for(m, buffer, rank);
+  std::vector<Chunk> chunks = chunks_of(runs);
+  const int32_t pdt = m->buffers[buffer].param_dtype;
+  for (const Chunk& c : chunks) {
+    K3Params& kp = k3_scratch();
+    kp.main_grad = main_grad;
+    kp.master = master;
+    kp.exp_avg = exp_avg;
+    kp.exp_avg_sq = exp_avg_sq;
+    kp.param = param;
+    kp.coef = d_coef;
+    kp.found_inf = d_found;
+    kp.b1 = (float)hp->beta1;
+    kp.b2 = (float)hp->beta2;
+    kp.omb1 = (float)(1.0 - hp->beta1);
+    kp.omb2 = (float)(1.0 - hp->beta2);
+    kp.eps = (float)hp->eps;
+    kp.step_size = (float)(hp->lr / (1.0 - pow_int(hp->beta1, hp->step)));
+    kp.bc2_sqrt = (float)std::sqrt(1.0 - pow_int(hp->beta2, hp->step));
+    kp.pad = 0;
+    fill_table(kp.tab, runs, c, hp->lr, hp->weight_decay);
+    int st;
+    switch (pdt) {
+      case DOPT_BF16: st = launch_k3_t<__nv_bfloat16>(kp, c.n_tiles, s); break;
+      case DOPT_F16: st = launch_k3_t<__half>(kp, c.n_tiles, s); break;
+      default: st = launch_k3_t<float>(kp, c.n_tiles, s); break;
+    }
+    if (st) return st;
+  }
+  return DOPT_OK;
+}
+
+int check_state_ptrs(const dopt_shard_map* m, int32_t buffer, const float* master,
+                     const float* exp_avg, const float* exp_avg_sq, const void* param,
+                     const char* fn) {
+  const bool fp32 = m->buffers[buffer].param_dtype == DOPT_F32;
+  if (!exp_avg || !exp_avg_sq || !param || (!fp32 && !master))
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL state or param pointer");
+  if (fp32 && master)
+    return dopt::fail(DOPT_E_INVALID,
+                      std::string(fn) + ": master must be NULL for an fp32 buffer (the param buffer is the master)");
+  if (!aligned16(exp_avg) || !aligned16(exp_avg_sq) || !aligned16(param) || (master && !aligned16(master)))
+    return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": state or param pointer not 16-byte aligned");
+  return DOPT_OK;
+}
+
+int check_replicas(const dopt_shard_map* m, int32_t rank, const void* const* replicas,
+                   int32_t n_rep, int32_t n_inst, int32_t layout, const char* fn) {
+  if (n_inst < 1 || n_rep != m->dp * n_inst || n_rep > DOPT_MAX_REPLICAS)
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": n_replicas must be DP * n_instances (at most " +
+                                          std::to_string(DOPT_MAX_REPLICAS) + ")");
+  if (layout != DOPT_LAYOUT_FULL_BUFFER && layout != DOPT_LAYOUT_SHARD_ONLY)
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": unknown layout");
+  if (layout == DOPT_LAYOUT_SHARD_ONLY && rank == DOPT_ALL_RANKS)
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": SHARD_ONLY layout needs a single rank");
+  if (!replicas) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL replica array");
+  for (int k = 0; k < n_rep; ++k) {
+    if (!replicas[k]) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL replica pointer");
+    if (!aligned16(replicas[k]))
+      return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": replica pointer not 16-byte aligned");
+  }
+  return DOPT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dopt_workspace_bytes(const dopt_shard_map* map, int32_t rank) {
+  if (!map || (rank != DOPT_ALL_RANKS && (rank < 0 || rank >= map->dp))) {
+    dopt::fail(DOPT_E_INVALID, "dopt_workspace_bytes: bad map or rank");
+    return 0;
+  }
+  return workspace_bytes(const_cast<dopt_shard_map*>(map), rank);
+}
+
+int dopt_grad_reduce_shard(const dopt_shard_map* map, int32_t buffer, int32_t rank,
+                           const void* const* replicas, int32_t n_replicas, int32_t n_instances,
+                           int32_t layout, int32_t average_in_collective, float* main_grad,
+                           void* workspace, size_t workspace_bytes_, dopt_stream stream) {
+  const char* fn = "dopt_grad_reduce_shard";
+  int st = check_map_buffer_rank(map, buffer, rank, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(map);
+  if ((st = check_replicas(m, rank, replicas, n_replicas, n_instances, layout, fn))) return st;
+  if (!main_grad) return dopt::fail(DOPT_E_INVALID, "dopt_grad_reduce_shard: NULL main_grad");
+  if (!aligned16(main_grad)) return dopt::fail(DOPT_E_ALIGN, "dopt_grad_reduce_shard: main_grad not aligned");
+  (void)workspace;
+  (void)workspace_bytes_;
+  return run_k1(m, buffer, rank, replicas, n_replicas, n_instances,
+                layout == DOPT_LAYOUT_FULL_BUFFER, average_in_collective, 1.0f,
+                m->buffers[buffer].grad_dtype, main_grad, false, nullptr, (cudaStream_t)stream);
+}
+
+int dopt_prepare_grads(const dopt_shard_map* map, int32_t buffer, int32_t rank,
+                       float inv_loss_scale, float* main_grad, void* workspace,
+                       size_t workspace_bytes_, dopt_stream stream) {
+  const char* fn = "dopt_prepare_grads";
+  int st = check_map_buffer_rank(map, buffer, rank, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(map);
+  if ((st = check_workspace(m, rank, workspace, workspace_bytes_, fn))) return st;
+  if (!main_grad) return dopt::fail(DOPT_E_INVALID, "dopt_prepare_grads: NULL main_grad");
+  if (!aligned16(main_grad)) return dopt::fail(DOPT_E_ALIGN, "dopt_prepare_grads: main_grad not aligned");
+  if (!std::isfinite(inv_loss_scale)) return dopt::fail(DOPT_E_INVALID, "dopt_prepare_grads: bad inv_loss_scale");
+  // the main grad itself is the single input, read at its own (flat) index
+  const void* one[1] = {main_grad};
+  return run_k1(m, buffer, rank, one, 1, 1, 0, 0, inv_loss_scale, DOPT_F32, main_grad, true,
+                workspace, (cudaStream_t)stream);
+}
+
+int dopt_grad_norm(const dopt_shard_map* map, int32_t rank, void* workspace, size_t workspace_bytes_,
+                   double remote_sumsq, int32_t remote_found_inf, double max_norm, float* d_norm,
+                   float* d_clip_coef, int32_t* d_found_inf, dopt_stream stream) {
+  const char* fn = "dopt_grad_norm";
+  int st = check_map_buffer_rank(map, 0, rank, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(map);
+  if ((st = check_workspace(m, rank, workspace, workspace_bytes_, fn))) return st;
+  if (!(remote_sumsq >= 0) || std::isnan(max_norm))
+    return dopt::fail(DOPT_E_INVALID, "dopt_grad_norm: bad remote_sumsq or max_norm");
+  return run_k2(m, rank, workspace, remote_sumsq, remote_found_inf, max_norm, d_norm, d_clip_coef,
+                d_found_inf, (cudaStream_t)stream);
+}
+
+int dopt_adam_step(const dopt_shard_map* map, int32_t buffer, int32_t rank, const float* main_grad,
+                   float* master, float* exp_avg, float* exp_avg_sq, void* param_buffer,
+                   const dopt_adamw_hparams* hp, const float* d_clip_coef,
+                   const int32_t* d_found_inf, dopt_stream stream) {
+  const char* fn = "dopt_adam_step";
+  int st = check_map_buffer_rank(map, buffer, rank, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(map);
+  if ((st = check_hparams(hp, fn))) return st;
+  if ((st = check_state_ptrs(m, buffer, master, exp_avg, exp_avg_sq, param_buffer, fn))) return st;
+  if (!main_grad || !d_clip_coef || !d_found_inf)
+    return dopt::fail(DOPT_E_INVALID, "dopt_adam_step: NULL main_grad, clip coef or found_inf");
+  if (!aligned16(main_grad)) return dopt::fail(DOPT_E_ALIGN, "dopt_adam_step: main_grad not aligned");
+  return run_k3(m, buffer, rank, main_grad, master, exp_avg, exp_avg_sq, param_buffer, hp, d_clip_coef,
+                d_found_inf, (cudaStream_t)stream);
+}
+
+int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm) {
+  const char* fn = "dopt_step";
+  if (!a) return dopt::fail(DOPT_E_INVALID, "dopt_step: NULL args");
+  int st = check_map_buffer_rank(a->map, 0, a->rank, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  const int32_t nb = (int32_t)m->buffers.size();
+  const int32_t n_rep = m->dp * a->n_instances;
+  if ((st = check_workspace(m, a->rank, a->workspace, a->workspace_bytes, fn))) return st;
+  if ((st = check_hparams(&a->hp, fn))) return st;
+  if (!a->replica_grads || !a->main_grad || !a->master || !a->exp_avg || !a->exp_avg_sq || !a->param_buffer)
+    return dopt::fail(DOPT_E_INVALID, "dopt_step: NULL per-buffer array");
+  if (!std::isfinite(a->inv_loss_scale) || !(a->remote_sumsq >= 0) || std::isnan(a->max_norm))
+    return dopt::fail(DOPT_E_INVALID, "dopt_step: bad inv_loss_scale, remote_sumsq or max_norm");
+  for (int32_t b = 0; b < nb; ++b) {
+    if ((st = check_replicas(m, a->rank, a->replica_grads[b], n_rep, a->n_instances, a->layout, fn))) return st;
+    if ((st = check_state_ptrs(m, b, a->master[b], a->exp_avg[b], a->exp_avg_sq[b], a->param_buffer[b], fn)))
+      return st;
+    if (!a->main_grad[b]) return dopt::fail(DOPT_E_INVALID, "dopt_step: NULL main_grad");
+    if (!aligned16(a->main_grad[b])) return dopt::fail(DOPT_E_ALIGN, "dopt_step: main_grad not aligned");
+  }
+  cudaStream_t s = (cudaStream_t)a->stream;
+  for (int32_t b = 0; b < nb; ++b) {
+    st = run_k1(m, b, a->rank, a->replica_grads[b], n_rep, a->n_instances,
+                a->layout == DOPT_LAYOUT_FULL_BUFFER, a->average_in_collective, a->inv_loss_scale,
+                m->buffers[b].grad_dtype, a->main_grad[b], true, a->workspace, s);
+    if (st) return st;
+  }
+  Scalars* sc = scalars_ptr(a->workspace);
+  if ((st = run_k2(m, a->rank, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm, d_norm,
+                   nullptr, d_found_inf, s)))
+    return st;
+  for (int32_t b = 0; b < nb; ++b) {
+    st = run_k3(m, b, a->rank, a->main_grad[b], a->master[b], a->exp_avg[b], a->exp_avg_sq[b],
+                a->param_buffer[b], &a->hp, &sc->coef, &sc->found_inf, s);
+    if (st) return st;
+  }
+  return DOPT_OK;
+}
+
+int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {
+  int st = dopt_step_async(a, nullptr, nullptr);
+  if (st) return st;
+  Scalars host{};
+  cudaStream_t s = (cudaStream_t)a->stream;
+  cudaError_t e = cudaMemcpyAsync(&host, a->workspace, sizeof(Scalars), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
+  if (found_inf_out) *found_inf_out = host.found_inf;
+  if (grad_norm_out) *grad_norm_out = host.norm;
+  return DOPT_OK;
+}
+
+}  // extern "C"

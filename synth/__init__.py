@@ -65,6 +65,8 @@ def host():
         L.synth_fill_uniform_f32.restype = None
         L.synth_bits_at.argtypes = [U64, U64]
         L.synth_bits_at.restype = U64
+        L.synth_gather_normal.argtypes = [P, I32, P, I64, U64, F]
+        L.synth_gather_normal.restype = None
         _host = L
     return _host
 
@@ -101,6 +103,17 @@ def normal(n, key_, index0=0, sigma=1.0, kind=OUT_F32):
     out = np.empty(n, dtype=dt)
     if n:
         host().synth_fill_normal(out.ctypes.data, kind, n, key_, index0, factor(sigma))
+    return out
+
+
+def normal_at(indices, key_, sigma=1.0, kind=OUT_F32):
+    """Values of stream `key_` at the given element indices."""
+    idx = np.ascontiguousarray(indices, dtype=np.uint64)
+    dt = np.uint16 if kind in (OUT_BF16, OUT_F16) else np.float32
+    out = np.empty(len(idx), dtype=dt)
+    if len(idx):
+        host().synth_gather_normal(out.ctypes.data, kind, idx.ctypes.data, len(idx), key_,
+                                   factor(sigma))
     return out
 
 

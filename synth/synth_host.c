@@ -34,3 +34,10 @@ void synth_fill_uniform_f32(float* dst, int64_t n, uint64_t key, uint64_t index0
 
 /* Per-element bits, exposed so tests can check the definition itself. */
 uint64_t synth_bits_at(uint64_t key, uint64_t index) { return synth_bits(key, index); }
+
+/* Values of one stream at arbitrary indices (for sampled checks). */
+void synth_gather_normal(void* dst, int32_t kind, const uint64_t* indices, int64_t n,
+                         uint64_t key, float factor) {
+  for (int64_t i = 0; i < n; ++i) synth_fill_normal((char*)dst + i * (kind == SYNTH_OUT_BF16 || kind == SYNTH_OUT_F16 ? 2 : 4),
+                                                    kind, 1, key, indices[i], factor);
+}

@@ -1,0 +1,311 @@
+"""Builds one workload's seeded inputs for both sides -- the CPU oracle (numpy
+arrays) and the CUDA library (torch device tensors) -- runs optimizer steps
+on each, and compares the results element by element.
+
+Tolerances (from the benchmark spec of this path): shard map and
+found_inf bit-exact; fp32 master, m and v within 4 ulp or 1e-6 relative;
+16-bit params within 1 ulp of their type; grad norm within 1e-5 relative.
+The main grad (the reduced, unscaled fp32 gradient) follows the same fixed
+summation order on both sides and must be bit-exact.
+"""
+
+import numpy as np
+
+import oracle
+import synth
+
+F32, BF16, F16 = 0, 1, 2
+KIND = {F32: synth.OUT_F32, BF16: synth.OUT_BF16, F16: synth.OUT_F16}
+VALUE_KIND = {BF16: synth.OUT_F32_OF_BF16, F16: synth.OUT_F32_OF_F16}
+INF_BITS = {F32: np.float32(np.inf), BF16: np.uint16(0x7F80), F16: np.uint16(0x7C00)}
+
+
+def dopt():
+    import mixed_precision_adam_gb300 as m
+    return m
+
+
+class HostCase:
+    """Seeded inputs of a workload for the selected ranks, as numpy arrays."""
+
+    def __init__(self, cfg):
+        D = dopt()
+        self.cfg = cfg
+        dp, bs = cfg["dp"], cfg["bucket_size"]
+        self.om = oracle.ShardMap(cfg["params"], dp, bs, cfg["grad_reduce_in_fp32"],
+                                  cfg["pad_for_high_busbw"])
+        self.pm = D.dopt_build_shard_map(cfg["params"], dp, -1 if bs is None else bs,
+                                         cfg["grad_reduce_in_fp32"], cfg["pad_for_high_busbw"])
+        self.all_ranks = cfg["ranks"] == "all"
+        self.ranks = list(range(dp)) if self.all_ranks else list(cfg["ranks"])
+        self.rank_arg = D.ALL_RANKS if self.all_ranks else self.ranks[0]
+        self.n_rep = dp * cfg["n_inst"]
+        self.seed = cfg["seed"]
+        self.params, self.state = [], []
+        pkey = synth.key(self.seed, synth.STREAM_PARAM, 0, 0)
+        for bi, buf in enumerate(self.om.buffers):
+            S = self.om.shard_numel(bi)
+            n_local = len(self.ranks) * S
+            self.params.append(synth.normal(buf.numel, pkey, 0, cfg["param_sigma"],
+                                            KIND[buf.param_dtype]))
+            st = {"exp_avg": np.zeros(n_local, np.float32),
+                  "exp_avg_sq": np.zeros(n_local, np.float32)}
+            if cfg.get("warm_state"):
+                st["exp_avg"] = self.to_local(bi, synth.normal(
+                    buf.numel, synth.key(self.seed, synth.STREAM_EXP_AVG, 0, 0), 0, 1e-4))
+                st["exp_avg_sq"] = self.to_local(bi, synth.uniform(
+                    buf.numel, synth.key(self.seed, synth.STREAM_EXP_AVG_SQ, 0, 0), 0, 1e-7))
+            if buf.param_dtype != F32:
+                full = synth.normal(buf.numel, pkey, 0, cfg["param_sigma"],
+                                    VALUE_KIND[buf.param_dtype])
+                st["master"] = self.to_local(bi, full)
+            self.state.append(st)
+        self.t_applied = 0
+
+    def to_local(self, bi, world):
+        """Gathers a buffer-indexed array into the flat shard layout of the ranks."""
+        S = self.om.shard_numel(bi)
+        out = np.zeros(len(self.ranks) * S, dtype=world.dtype)
+        for slot, r in enumerate(self.ranks):
+            for b in range(len(self.om.buffers[bi].buckets)):
+                rg = self.om.bucket_world_range(bi, b, r)
+                base = slot * S + self.om.bucket_shard_base(bi, b)
+                out[base:base + rg.size] = world[rg.start:rg.end]
+        return out
+
+    def piece_mask(self, bi):
+        """True at the flat-shard positions that hold param elements."""
+        S = self.om.shard_numel(bi)
+        mask = np.zeros(len(self.ranks) * S, dtype=bool)
+        for slot, r in enumerate(self.ranks):
+            for _, _, v in self.om.rank_pieces(bi, r):
+                lo = slot * S + v["shard_offset"]
+                mask[lo:lo + v["gbuf_local"].size] = True
+        return mask
+
+    def inf_position(self):
+        """(buffer 0, world index) of the injected non-finite grad: the first
+        param element at or after numel_unpadded * frac."""
+        spec = self.cfg["inf_at"]
+        buf = self.om.buffers[0]
+        target = int(buf.numel_unpadded * spec["buffer_frac"])
+        best = None
+        for pid in buf.params:
+            s, e, _ = buf.index[pid]
+            if e > target and e > s:
+                w = max(s, target)
+                if best is None or w < best:
+                    best = w
+        return best
+
+    def grads(self, t):
+        """Replica grads of step t per buffer (layout per the config)."""
+        cfg = self.cfg
+        out = []
+        for bi, buf in enumerate(self.om.buffers):
+            reps = []
+            for k in range(self.n_rep):
+                key = synth.key(self.seed, synth.STREAM_GRAD, t, k)
+                if cfg["layout"] == "full":
+                    reps.append(synth.normal(buf.numel, key, 0, cfg["grad_sigma"], KIND[buf.grad_dtype]))
+                else:
+                    full = synth.normal(buf.numel, key, 0, cfg["grad_sigma"], KIND[buf.grad_dtype])
+                    reps.append(self.to_local(bi, full))
+            out.append(reps)
+        spec = cfg.get("inf_at")
+        if spec and spec["step"] == t:
+            w = self.inf_position()
+            rep = out[0][spec["replica"]]
+            if cfg["layout"] == "full":
+                rep[w] = INF_BITS[self.om.buffers[0].grad_dtype]
+            else:
+                marker = np.zeros(self.om.buffers[0].numel, dtype=bool)
+                marker[w] = True
+                loc = np.nonzero(self.to_local(0, marker))[0]
+                if len(loc):
+                    rep[loc[0]] = INF_BITS[self.om.buffers[0].grad_dtype]
+        return out
+
+    def oracle_step(self, grads, t):
+        cfg = self.cfg
+        return oracle.step(self.om, self.ranks, grads, self.state, self.params, cfg["hp"], t,
+                           inv_scale=float(np.float32(1.0 / cfg["loss_scale"])),
+                           max_norm=cfg["max_norm"], layout=cfg["layout"], n_inst=cfg["n_inst"],
+                           average=cfg["average"], remote_sumsq=cfg.get("remote_sumsq", 0.0),
+                           remote_found_inf=cfg.get("remote_found_inf", False))
+
+
+class DeviceCase:
+    """The same inputs on the GPU, stepped through the library's C ABI."""
+
+    def __init__(self, hc):
+        import torch
+        D = dopt()
+        self.hc = hc
+        self.torch = torch
+        dev = torch.device("cuda")
+        self.params = [self._up(p) for p in hc.params]
+        self.master = [self._up(st["master"]) if "master" in st else None for st in hc.state]
+        self.exp_avg = [self._up(st["exp_avg"]) for st in hc.state]
+        self.exp_avg_sq = [self._up(st["exp_avg_sq"]) for st in hc.state]
+        self.main = [torch.zeros(len(st["exp_avg"]), dtype=torch.float32, device=dev)
+                     for st in hc.state]
+        self.ws_bytes = D.dopt_workspace_bytes(hc.pm, hc.rank_arg)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+
+    def _up(self, a):
+        t = self.torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a.copy())
+        return t.cuda()
+
+    def step_args(self, reps, t, stream=None):
+        D = dopt()
+        cfg = self.hc.cfg
+        return D.StepArgs(self.hc.pm, self.hc.rank_arg, reps, self.main, self.master, self.exp_avg,
+                          self.exp_avg_sq, self.params, cfg["hp"], t, self.ws, self.ws_bytes,
+                          n_instances=cfg["n_inst"],
+                          layout=D.LAYOUT_FULL_BUFFER if cfg["layout"] == "full" else D.LAYOUT_SHARD_ONLY,
+                          average_in_collective=cfg["average"],
+                          inv_loss_scale=float(np.float32(1.0 / cfg["loss_scale"])),
+                          max_norm=cfg["max_norm"], remote_sumsq=cfg.get("remote_sumsq", 0.0),
+                          remote_found_inf=cfg.get("remote_found_inf", False),
+                          stream=stream if stream is not None else self.torch.cuda.current_stream())
+
+    def step(self, grads, t):
+        reps = [[self._up(r) for r in g] for g in grads]
+        args = self.step_args(reps, t)
+        found, norm = dopt().dopt_step(args)
+        return found, norm
+
+    def step_separate(self, grads, t):
+        """The same step through the separate entry points (A2, A3, A4, A5+A6)."""
+        D = dopt()
+        torch = self.torch
+        cfg = self.hc.cfg
+        reps = [[self._up(r) for r in g] for g in grads]
+        s = torch.cuda.current_stream()
+        layout = D.LAYOUT_FULL_BUFFER if cfg["layout"] == "full" else D.LAYOUT_SHARD_ONLY
+        for bi in range(len(self.main)):
+            D.dopt_grad_reduce_shard(self.hc.pm, bi, self.hc.rank_arg, reps[bi], cfg["n_inst"], layout,
+                                     cfg["average"], self.main[bi], self.ws, self.ws_bytes, s)
+            D.dopt_prepare_grads(self.hc.pm, bi, self.hc.rank_arg,
+                                 float(np.float32(1.0 / cfg["loss_scale"])), self.main[bi], self.ws,
+                                 self.ws_bytes, s)
+        d_norm = torch.zeros(1, dtype=torch.float32, device="cuda")
+        d_coef = torch.zeros(1, dtype=torch.float32, device="cuda")
+        d_found = torch.zeros(1, dtype=torch.int32, device="cuda")
+        D.dopt_grad_norm(self.hc.pm, self.hc.rank_arg, self.ws, self.ws_bytes,
+                         cfg.get("remote_sumsq", 0.0), cfg.get("remote_found_inf", False),
+                         cfg["max_norm"], d_norm, d_coef, d_found, s)
+        for bi in range(len(self.main)):
+            D.dopt_adam_step(self.hc.pm, bi, self.hc.rank_arg, self.main[bi], self.master[bi],
+                             self.exp_avg[bi], self.exp_avg_sq[bi], self.params[bi], cfg["hp"], t,
+                             d_coef, d_found, s)
+        torch.cuda.synchronize()
+        return bool(d_found.item()), float(d_norm.item())
+
+    def download(self):
+        def dn(t):
+            if t is None:
+                return None
+            a = t.cpu().numpy()
+            return a.view(np.uint16) if a.dtype == np.int16 else a
+        return ([dn(p) for p in self.params], [dn(m) for m in self.master],
+                [dn(m) for m in self.exp_avg], [dn(v) for v in self.exp_avg_sq],
+                [dn(m) for m in self.main])
+
+
+def ulp16(a, b):
+    """Distance in ulps between 16-bit float bit patterns (bf16 or fp16)."""
+    def key(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(key(a) - key(b))
+
+
+def state_close(got, want, before):
+    """fp32 state tolerance: 4 ulp, or 1e-6 relative to the operand scale."""
+    got = np.asarray(got, np.float32)
+    want = np.asarray(want, np.float32)
+    scale = np.maximum(np.maximum(np.abs(before), np.abs(want)), np.float32(1e-30))
+    return (oracle.float_ulp_diff(got, want) <= 4) | (
+        np.abs(got.astype(np.float64) - want.astype(np.float64)) <= 1e-6 * scale)
+
+
+def compare_step(hc, dc, ores, found, norm, before, report):
+    """Compares the device state after a step with the oracle's.  `before`
+    holds the oracle's state before the step.  Appends findings to report
+    and returns True when every check passes."""
+    ok = True
+    if bool(found) != bool(ores["found_inf"]):
+        report.append(f"found_inf device={found} oracle={ores['found_inf']}")
+        return False
+    if not found:
+        rel = abs(norm - ores["norm"]) / max(ores["norm"], 1e-30)
+        if not rel <= 1e-5:
+            report.append(f"grad_norm device={norm} oracle={ores['norm']} rel={rel:.3g}")
+            ok = False
+    params, master, exp_avg, exp_avg_sq, mains = dc.download()
+    for bi, buf in enumerate(hc.om.buffers):
+        mask = hc.piece_mask(bi)
+        st = hc.state[bi]
+        om_ = ores["main"][bi]
+        if not np.array_equal(mains[bi][mask].view(np.uint32), om_[mask].view(np.uint32)):
+            bad = np.nonzero(mains[bi][mask].view(np.uint32) != om_[mask].view(np.uint32))[0]
+            report.append(f"buffer {bi}: main grad differs at {len(bad)} elements")
+            ok = False
+        checks = [("exp_avg", exp_avg[bi], st["exp_avg"], before[bi]["exp_avg"]),
+                  ("exp_avg_sq", exp_avg_sq[bi], st["exp_avg_sq"], before[bi]["exp_avg_sq"])]
+        if "master" in st:
+            checks.append(("master", master[bi], st["master"], before[bi]["master"]))
+        for name, g, w, b in checks:
+            good = state_close(g[mask], w[mask], b[mask])
+            if not good.all():
+                report.append(f"buffer {bi}: {name} off at {int((~good).sum())} elements, "
+                              f"max ulp {int(oracle.float_ulp_diff(g[mask], w[mask]).max())}")
+                ok = False
+        p_dev, p_or = params[bi], hc.params[bi]
+        if buf.param_dtype == F32:
+            pm = np.zeros(buf.numel, bool)
+            for r in hc.ranks:
+                for _, _, v in hc.om.rank_pieces(bi, r):
+                    pm[v["gbuf_world"].start:v["gbuf_world"].end] = True
+            good = state_close(p_dev[pm], p_or[pm], before[bi]["param"][pm])
+            if not good.all():
+                report.append(f"buffer {bi}: fp32 param off at {int((~good).sum())} elements")
+                ok = False
+            if not np.array_equal(p_dev[~pm].view(np.uint32), p_or[~pm].view(np.uint32)):
+                report.append(f"buffer {bi}: fp32 param changed outside the shards")
+                ok = False
+        else:
+            d = ulp16(p_dev, p_or)
+            if d.max() > 1:
+                report.append(f"buffer {bi}: 16-bit param off by {int(d.max())} ulp at "
+                              f"{int((d > 1).sum())} elements")
+                ok = False
+    return ok
+
+
+def snapshot(hc):
+    return [dict({k: v.copy() for k, v in st.items()}, param=p.copy())
+            for st, p in zip(hc.state, hc.params)]
+
+
+def run_parity(cfg, steps=None, separate=False):
+    """Steps a workload on both sides and returns (all ok, report lines)."""
+    hc = HostCase(cfg)
+    dc = DeviceCase(hc)
+    report = []
+    ok = True
+    for t_step in range(1, (steps or cfg["steps"]) + 1):
+        grads = hc.grads(t_step)
+        t = hc.t_applied + 1
+        before = snapshot(hc)
+        ores = hc.oracle_step(grads, t)
+        found, norm = dc.step_separate(grads, t) if separate else dc.step(grads, t)
+        good = compare_step(hc, dc, ores, found, norm, before, report)
+        report.append(f"step {t_step} (t={t}): found_inf={found} norm={norm:.9g} "
+                      f"oracle={ores['norm']:.9g} coef={ores['coef']:.9g} ok={good}")
+        ok &= good
+        if not ores["found_inf"]:
+            hc.t_applied += 1
+    return ok, report

@@ -1,0 +1,145 @@
+"""Parity of the CUDA path with the CPU oracle, element by element, through
+the library's C ABI.  Sizes span many tiles and ragged run ends; the edge
+cases cover padding, unaligned runs, every dtype pair, hierarchical DP,
+skipped steps and the unclipped branch."""
+
+import copy
+
+import numpy as np
+import pytest
+
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import gpu_harness as H  # noqa: E402
+
+
+def _check(cfg, steps=None, separate=False):
+    ok, report = H.run_parity(cfg, steps, separate)
+    assert ok, "\n".join(report)
+
+
+@pytest.mark.parametrize("name", ["toy_mlp_dp4", "gpt2_small_dp8", "llama_1p3b_fp16_dp8",
+                                  "llama_7b_dp8_rank0", "llama_7b_dp16_2x8_1m"])
+def test_workload_mini(name):
+    _check(W.mini(name))
+
+
+def test_separate_entry_points_match_oracle():
+    _check(W.mini("gpt2_small_dp8"), separate=True)
+
+
+def _tiny(params, dp, **kw):
+    cfg = W._cfg(name="tiny", params=params, dp=dp, steps=3, seed=kw.pop("seed", 7))
+    cfg.update(kw)
+    return cfg
+
+
+RAGGED = [dict(numel=n, dtype=d) for n, d in
+          [(1, 1), (63, 1), (65, 1), (1000, 0), (127, 1), (4099, 1), (3, 0), (20001, 1), (129, 2)]]
+
+
+@pytest.mark.parametrize("dp", [1, 3, 8])
+@pytest.mark.parametrize("grad_fp32", [True, False])
+def test_ragged_params_all_dtypes(dp, grad_fp32):
+    _check(_tiny(RAGGED, dp, bucket_size=5000, grad_reduce_in_fp32=grad_fp32,
+                 grad_sigma=1e-2, max_norm=0.5))
+
+
+def test_unaligned_runs_large_dp():
+    # DP=32: lcm(32,128)=128, so a 128-element bucket gives 4-element slices
+    # that start off the 8-element vector grid
+    params = [dict(numel=n, dtype=1) for n in (100, 37, 300, 5, 77)]
+    _check(_tiny(params, 32, bucket_size=64))
+
+
+def test_busbw_padding_and_new_bucket():
+    params = [dict(numel=n, dtype=1, new_bucket=(i % 3 == 1)) for i, n in
+              enumerate([700, 5000, 33, 12000, 999, 64, 65])]
+    _check(_tiny(params, 4, bucket_size=3000, pad_for_high_busbw=True))
+
+
+def test_weight_decay_multipliers():
+    params = [dict(numel=n, dtype=1, wd_mult=w) for n, w in
+              [(5000, 1.0), (5000, 0.0), (333, 0.5), (4096, 0.0), (70, 1.0)]]
+    _check(_tiny(params, 2, bucket_size=None, warm_state=True))
+
+
+def test_many_runs_chunked_launches():
+    # more runs than one kernel-parameter table holds: alternate wd_mult so
+    # neighbouring params never merge into one run
+    params = [dict(numel=64 + (i % 5), dtype=1, wd_mult=float(i % 2)) for i in range(2500)]
+    _check(_tiny(params, 1, bucket_size=None, steps=2))
+
+
+def test_average_in_collective_and_hierarchy():
+    params = W.llama(1, 128, 344, 257)
+    _check(_tiny(params, 4, bucket_size=20000, average=True, steps=2))
+    _check(_tiny(params, 4, bucket_size=20000, n_inst=2, steps=2))
+    _check(_tiny(params, 4, bucket_size=20000, n_inst=3, average=True, steps=2,
+                 layout="shard", ranks=[2]))
+
+
+def test_shard_layout_every_rank():
+    params = W.llama(1, 96, 256, 131)
+    for r in range(4):
+        _check(_tiny(params, 4, bucket_size=9000, layout="shard", ranks=[r], steps=2))
+
+
+@pytest.mark.parametrize("max_norm", [0.0, -1.0, 1e9])
+def test_unclipped_branch(max_norm):
+    _check(_tiny(RAGGED, 2, bucket_size=5000, max_norm=max_norm))
+
+
+def test_remote_terms():
+    _check(_tiny(RAGGED, 2, bucket_size=5000, remote_sumsq=3.0, steps=2))
+    _check(_tiny(RAGGED, 2, bucket_size=5000, remote_found_inf=True, steps=1))
+
+
+@pytest.mark.parametrize("where", ["first", "last", "fp32_group", "nan"])
+def test_nonfinite_skips_step_untouched(where):
+    cfg = _tiny(RAGGED, 4, bucket_size=5000, warm_state=True, steps=1)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    grads = hc.grads(1)
+    bi = 1 if where == "fp32_group" else 0
+    pieces = hc.om.rank_pieces(bi, 3 if where == "last" else 0)
+    w = pieces[-1][2]["gbuf_world"].end - 1 if where == "last" else pieces[0][2]["gbuf_world"].start
+    val = np.nan if where == "nan" else np.inf
+    rep = grads[bi][2]
+    if rep.dtype == np.uint16:
+        rep[w] = 0x7FC0 if where == "nan" else 0x7F80
+    else:
+        rep[w] = val
+    before = dc.download()
+    found, norm = dc.step(grads, 1)
+    after = dc.download()
+    assert found and np.isnan(norm)
+    for b_list, a_list in zip(before[:4], after[:4]):  # params, master, m, v
+        for b, a in zip(b_list, a_list):
+            if b is not None:
+                assert b.tobytes() == a.tobytes()
+
+
+def test_zero_element_rank():
+    # a 10-element param with DP=8: ranks 1..7 own only padding of the
+    # 128-element bucket
+    params = [dict(numel=10, dtype=1), dict(numel=300, dtype=0)]
+    _check(_tiny(params, 8, bucket_size=None, steps=2))
+    _check(_tiny(params, 8, bucket_size=None, steps=2, layout="shard", ranks=[5]))
+
+
+def test_repeat_is_deterministic():
+    cfg = W.mini("llama_7b_dp8_rank0")
+    outs = []
+    for _ in range(2):
+        hc = H.HostCase(cfg)
+        dc = H.DeviceCase(hc)
+        norms = [dc.step(hc.grads(t), t)[1] for t in (1, 2)]
+        outs.append((norms, [a.tobytes() for a in dc.download()[1] if a is not None]))
+    assert outs[0] == outs[1]
