@@ -273,6 +273,11 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   dopt_stream stream;
+  /* Optional tracing: NULL, or 4 cudaEvent_t handles (as plain pointers)
+   * recorded on `stream` before the reduce/prepare pass, after it, after
+   * the norm finalize and after the AdamW pass, so a caller can time each
+   * stage of the step with cudaEventElapsedTime. */
+  void* const* stage_events;
 } dopt_step_args;
 
 /*
@@ -333,6 +338,10 @@ int dopt_loss_scaler_init(dopt_loss_scaler* s, double initial_scale, double grow
                           double backoff_factor, int32_t growth_interval, int32_t hysteresis,
                           double min_scale);
 int dopt_loss_scaler_update(dopt_loss_scaler* s, int32_t found_inf);
+
+/* Number of kernels this library has launched in this process (all
+ * devices, all threads); a caller can difference it around a region. */
+uint64_t dopt_kernel_launches(void);
 
 const char* dopt_last_error(void);
 

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "lib", "libdopt.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
-                      "`python -m mixed_precision_adam_gb300.build` (or __graft_entry__.build())")
+                      "`python mixed_precision_adam_gb300/build.py` (or __graft_entry__.build())")
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -70,7 +70,8 @@ class dopt_step_args(ctypes.Structure):
                 ("param_buffer", ctypes.POINTER(_P)),
                 ("inv_loss_scale", _F), ("remote_found_inf", _I32),
                 ("max_norm", _D), ("remote_sumsq", _D), ("hp", dopt_adamw_hparams),
-                ("workspace", _P), ("workspace_bytes", _SZ), ("stream", _P)]
+                ("workspace", _P), ("workspace_bytes", _SZ), ("stream", _P),
+                ("stage_events", ctypes.POINTER(_P))]
 
 
 class dopt_loss_scaler(ctypes.Structure):
@@ -121,6 +122,7 @@ _c = {
                                     ctypes.POINTER(dopt_loss_scaler), _D, _D, _D, _I32, _I32, _D),
     "dopt_loss_scaler_update": _proto("dopt_loss_scaler_update", ctypes.c_int,
                                       ctypes.POINTER(dopt_loss_scaler), _I32),
+    "dopt_kernel_launches": _proto("dopt_kernel_launches", ctypes.c_uint64),
     "dopt_last_error": _proto("dopt_last_error", ctypes.c_char_p),
 }
 
@@ -313,6 +315,15 @@ class StepArgs:
         c.workspace_bytes = workspace_bytes
         c.stream = _stream(stream)
 
+    def set_stage_events(self, events):
+        """events: None, or 4 CUDA events (objects with cuda_event, or ints)."""
+        if events is None:
+            self._events = None
+            self.c.stage_events = None
+            return
+        self._events = (_P * 4)(*[getattr(e, "cuda_event", e) for e in events])
+        self.c.stage_events = ctypes.cast(self._events, ctypes.POINTER(_P))
+
     def set_step(self, step, lr=None):
         self.c.hp.step = int(step)
         if lr is not None:
@@ -328,6 +339,10 @@ def dopt_step(args):
 
 def dopt_step_async(args, d_found_inf=None, d_norm=None):
     _check(_c["dopt_step_async"](ctypes.byref(args.c), _ptr(d_found_inf), _ptr(d_norm)))
+
+
+def dopt_kernel_launches():
+    return int(_c["dopt_kernel_launches"]())
 
 
 def dopt_memory_ledger(P, N, stage):

@@ -2,7 +2,8 @@
 
 Two translation units (host shard map in C++, kernels and device entry
 points in CUDA) are compiled in parallel and linked into one shared library
-with the CUDA runtime linked statically.  Run as a module or call build().
+with the CUDA runtime linked statically.  Run this file as a script
+(python mixed_precision_adam_gb300/build.py) or call build().
 """
 
 import os

@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -513,6 +514,7 @@ __global__ void __launch_bounds__(kThreads) k3_adamw(const __grid_constant__ K3P
 // ------------------------------------------------------------ host side --
 
 thread_local std::vector<char> t_param_scratch;  // kernel-parameter staging
+std::atomic<uint64_t> g_launches{0};             // kernels launched by this library
 
 // The run table of one launch: runs [first, first + count) of a rank
 // selection, with per-run decay for K3.
@@ -591,6 +593,7 @@ int grid_for(K kernel, int n_tiles, int* grid) {
 }
 
 int check_launch(const char* what) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
   return DOPT_OK;
@@ -807,9 +810,18 @@ int check_replicas(const dopt_shard_map* m, int32_t rank, const void* const* rep
   return DOPT_OK;
 }
 
+int record_stage(const dopt_step_args* a, int i, cudaStream_t s) {
+  if (!a->stage_events || !a->stage_events[i]) return DOPT_OK;
+  cudaError_t e = cudaEventRecord((cudaEvent_t)a->stage_events[i], s);
+  if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("stage event: ") + cudaGetErrorString(e));
+  return DOPT_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+uint64_t dopt_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 size_t dopt_workspace_bytes(const dopt_shard_map* map, int32_t rank) {
   if (!map || (rank != DOPT_ALL_RANKS && (rank < 0 || rank >= map->dp))) {
@@ -907,22 +919,25 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
     if (!aligned16(a->main_grad[b])) return dopt::fail(DOPT_E_ALIGN, "dopt_step: main_grad not aligned");
   }
   cudaStream_t s = (cudaStream_t)a->stream;
+  if ((st = record_stage(a, 0, s))) return st;
   for (int32_t b = 0; b < nb; ++b) {
     st = run_k1(m, b, a->rank, a->replica_grads[b], n_rep, a->n_instances,
                 a->layout == DOPT_LAYOUT_FULL_BUFFER, a->average_in_collective, a->inv_loss_scale,
                 m->buffers[b].grad_dtype, a->main_grad[b], true, a->workspace, s);
     if (st) return st;
   }
+  if ((st = record_stage(a, 1, s))) return st;
   Scalars* sc = scalars_ptr(a->workspace);
   if ((st = run_k2(m, a->rank, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm, d_norm,
                    nullptr, d_found_inf, s)))
     return st;
+  if ((st = record_stage(a, 2, s))) return st;
   for (int32_t b = 0; b < nb; ++b) {
     st = run_k3(m, b, a->rank, a->main_grad[b], a->master[b], a->exp_avg[b], a->exp_avg_sq[b],
                 a->param_buffer[b], &a->hp, &sc->coef, &sc->found_inf, s);
     if (st) return st;
   }
-  return DOPT_OK;
+  return record_stage(a, 3, s);
 }
 
 int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {
