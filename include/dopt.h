@@ -300,6 +300,43 @@ int dopt_step(const dopt_step_args* args, int32_t* found_inf_out, float* grad_no
  */
 int dopt_step_async(const dopt_step_args* args, int32_t* d_found_inf, float* d_norm);
 
+/*
+ * dopt_step_noalloc -- the fused step of dopt_step for callers that cannot
+ * allocate device memory.  No page describes this entry point; it exists for
+ * the library's users, not for the method.
+ *
+ * Some callers have no way to obtain a workspace buffer: a host program whose
+ * device memory is owned by another allocator (a framework's caching
+ * allocator, or a pool that reserved the GPU at start-up) and that exposes no
+ * raw allocation; a latency-bound loop that forbids device allocation after
+ * start-up because cudaMalloc may synchronize the device and stall other
+ * streams; a plugin interface that hands an operation only its inputs and
+ * outputs.  This entry point needs no workspace: its scratch (step scalars
+ * and per-CTA partial sums) is a static device array of
+ * DOPT_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ *  - args: as for dopt_step, except that args->workspace and
+ *    args->workspace_bytes are ignored.  The caller still passes every input
+ *    and output (replica grads, main grad, master, m, v, param buffers).
+ *  - The first call on a device looks up the device address of the scratch
+ *    array (with that device current); make that first call before any
+ *    stream capture.  Later calls on the device reuse the address.
+ *  - Returns DOPT_E_SIZE when the map and rank selection need more scratch
+ *    than the array holds (dopt_workspace_bytes(map, rank) >
+ *    DOPT_NOALLOC_SCRATCH_BYTES): no work is enqueued then.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Every call uses the same array, which keeps the last call's contents;
+ *    nothing in it needs to start at zero (each step writes every slot it
+ *    reads).  Calls that overlap on the GPU -- on two streams, or from two
+ *    threads without ordering -- race on the array and give wrong results:
+ *    order them.
+ * Waits for args->stream and returns found_inf and the grad norm like
+ * dopt_step.
+ */
+#define DOPT_NOALLOC_SCRATCH_BYTES (1u << 20)
+int dopt_step_noalloc(const dopt_step_args* args, int32_t* found_inf_out, float* grad_norm_out);
+
 /* ---------------------------------------------------------------------------
  * Host arithmetic of the pages (no GPU).
  */

@@ -115,6 +115,8 @@ _c = {
                         ctypes.POINTER(_I32), ctypes.POINTER(_F)),
     "dopt_step_async": _proto("dopt_step_async", ctypes.c_int, ctypes.POINTER(dopt_step_args),
                               _P, _P),
+    "dopt_step_noalloc": _proto("dopt_step_noalloc", ctypes.c_int, ctypes.POINTER(dopt_step_args),
+                                ctypes.POINTER(_I32), ctypes.POINTER(_F)),
     "dopt_memory_ledger": _proto("dopt_memory_ledger", _I64, _I64, _I32, _I32,
                                  ctypes.POINTER(_I64)),
     "dopt_comm_bytes": _proto("dopt_comm_bytes", _I64, _I64, _I32, _I32, _I32),
@@ -334,6 +336,17 @@ def dopt_step(args):
     """Runs one fused step; returns (found_inf: bool, grad_norm: float)."""
     f, n = _I32(), _F()
     _check(_c["dopt_step"](ctypes.byref(args.c), ctypes.byref(f), ctypes.byref(n)))
+    return bool(f.value), n.value
+
+
+NOALLOC_SCRATCH_BYTES = 1 << 20
+
+
+def dopt_step_noalloc(args):
+    """The fused step with the library's static scratch instead of a
+    workspace (args' workspace is ignored); returns (found_inf, grad_norm)."""
+    f, n = _I32(), _F()
+    _check(_c["dopt_step_noalloc"](ctypes.byref(args.c), ctypes.byref(f), ctypes.byref(n)))
     return bool(f.value), n.value
 
 

@@ -24,10 +24,17 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
 #include "dopt_internal.h"
+
+// Scratch of dopt_step_noalloc: the step scalars and partial-sum regions
+// that dopt_step keeps in the caller's workspace.  Host code must not use
+// this name as an address (it is a host-side stand-in): the device address
+// comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DOPT_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
@@ -938,6 +945,48 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
     if (st) return st;
   }
   return record_stage(a, 3, s);
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device, looked up on
+// the first call per device.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("dopt_step_noalloc: cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return dopt::fail(DOPT_E_INVALID, "dopt_step_noalloc: device index out of range");
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return dopt::fail(DOPT_E_CUDA, std::string("dopt_step_noalloc: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return DOPT_OK;
+}
+}  // namespace
+
+int dopt_step_noalloc(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {
+  if (!a) return dopt::fail(DOPT_E_INVALID, "dopt_step_noalloc: NULL args");
+  int st = check_map_buffer_rank(a->map, 0, a->rank, "dopt_step_noalloc");
+  if (st) return st;
+  size_t need = workspace_bytes(const_cast<dopt_shard_map*>(a->map), a->rank);
+  if (need > DOPT_NOALLOC_SCRATCH_BYTES)
+    return dopt::fail(DOPT_E_SIZE, "dopt_step_noalloc: this map and rank selection need " + std::to_string(need) +
+                                       " bytes of scratch; the static scratch holds " +
+                                       std::to_string((size_t)DOPT_NOALLOC_SCRATCH_BYTES) + " (use dopt_step with a workspace)");
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch))) return st;
+  dopt_step_args with_scratch = *a;
+  with_scratch.workspace = scratch;
+  with_scratch.workspace_bytes = DOPT_NOALLOC_SCRATCH_BYTES;
+  return dopt_step(&with_scratch, found_inf_out, grad_norm_out);
 }
 
 int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {
