@@ -15,7 +15,7 @@
 // the kernels by a table of runs (contiguous in both the flat shard and the
 // buffer) passed by value as a __grid_constant__ kernel parameter, so a step
 // needs no host-to-device copy and no library-owned device memory.  Each run
-// is cut into tiles of kTile elements; CTAs take tiles round-robin.
+// is cut into tiles (kTile1 / kTile3 elements); CTAs take tiles round-robin.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -38,10 +38,25 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[DOPT_NOALLOC_SC
 
 namespace {
 
+#ifndef DOPT_K1_UNROLL
+#define DOPT_K1_UNROLL 2
+#endif
+#ifndef DOPT_K3_UNROLL
+#define DOPT_K3_UNROLL 4
+#endif
+#ifndef DOPT_K1_MIN_BLOCKS
+#define DOPT_K1_MIN_BLOCKS 1
+#endif
+#ifndef DOPT_K3_MIN_BLOCKS
+#define DOPT_K3_MIN_BLOCKS 2
+#endif
+
 constexpr int kThreads = 256;              // threads per CTA
 constexpr int kVec = 4;                    // contiguous elements per thread access
-constexpr int kUnroll = 2;                 // accesses per thread per tile
-constexpr int kTile = kThreads * kVec * kUnroll;  // elements per tile
+constexpr int kUnroll1 = DOPT_K1_UNROLL;   // K1 accesses per thread per tile
+constexpr int kUnroll3 = DOPT_K3_UNROLL;   // K3 accesses per thread per tile
+constexpr int kTile1 = kThreads * kVec * kUnroll1;  // K1 elements per tile
+constexpr int kTile3 = kThreads * kVec * kUnroll3;  // K3 elements per tile
 constexpr int kMaxSeg = 960;               // runs per launch (kernel-parameter table)
 constexpr int kMaxGrid = 2048;             // partial slots per launch region
 constexpr int kBatch = 8;                  // replicas loaded together
@@ -158,10 +173,6 @@ struct GradT<__half> {
   }
 };
 
-__device__ __forceinline__ bool is_nonfinite(float x) {
-  return (__float_as_uint(x) & 0x7F800000u) == 0x7F800000u;
-}
-
 // Advances the run cursor of a CTA to the run holding tile t (tiles visited
 // in increasing order, so the cursor only moves forward).
 __device__ __forceinline__ int seek(const SegTable& tab, int si, int t) {
@@ -215,16 +226,24 @@ __device__ __forceinline__ float reduce_finish(const ReduceState& st, const K1Pa
 // with the error-free TwoSum, the errors gathered in c (the Dot2 scheme of
 // Ogita, Rump & Oishi, "Accurate sum and dot product", SIAM J. Sci. Comput.
 // 2005).  Squares of |x| >= 2^62 would overflow fp32 and go to an fp64
-// accumulator instead; the fp32 pair is moved to fp64 before it could
-// overflow.
+// accumulator instead, and the fp32 pair moves to fp64 before it could
+// overflow; both rare paths are out-of-line calls, so no fp64 instruction
+// is issued per element (GB300's fp64 rate is a small fraction of fp32's).
+// A non-finite main grad makes the sum non-finite, and finite main grads
+// cannot overflow it, so the non-finite check of prepare_grads is read off
+// the sum.
+__device__ __noinline__ double sumsq_wide(double d, float a, float b, float c, float e) {
+  return d + (double)a * (double)a + (double)b * (double)b + (double)c * (double)c +
+         (double)e * (double)e;
+}
+__device__ __noinline__ double sumsq_flush(double d, float s, float c) {
+  return d + ((double)s + (double)c);
+}
+
 struct SumSq {
   float s = 0.f, c = 0.f;
   double d = 0.0;
-  __device__ __forceinline__ void add(float x) {
-    if (fabsf(x) >= 0x1p62f) {
-      d += (double)x * (double)x;
-      return;
-    }
+  __device__ __forceinline__ void dot2(float x) {
     float p = __fmul_rn(x, x);
     float pe = fmaf(x, x, -p);
     float t = __fadd_rn(s, p);
@@ -233,9 +252,23 @@ struct SumSq {
     s = t;
     c = __fadd_rn(c, __fadd_rn(e, pe));
   }
+  __device__ __forceinline__ void add4(const float* x) {
+    float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    if (mx >= 0x1p62f) {
+      d = sumsq_wide(d, x[0], x[1], x[2], x[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dot2(x[j]);
+    }
+  }
+  __device__ __forceinline__ void add1(float x) {
+    if (fabsf(x) >= 0x1p62f) d = sumsq_wide(d, x, 0.f, 0.f, 0.f);
+    else dot2(x);
+  }
+  // once per tile: keeps |s| below 2^100 (NaN also takes this path)
   __device__ __forceinline__ void maybe_flush() {
-    if (fabsf(s) > 0x1p100f) {
-      d += (double)s + (double)c;
+    if (!(fabsf(s) <= 0x1p100f)) {
+      d = sumsq_flush(d, s, c);
       s = c = 0.f;
     }
   }
@@ -248,36 +281,54 @@ __device__ __forceinline__ double warp_sum(double v) {
   return v;
 }
 
+// Writes this CTA's partial (sum of squares, non-finite flag) and zeroes the
+// slots of its region that this launch leaves unused, so the finalize pass
+// can always sum whole regions.
+__device__ __forceinline__ void write_partial(const SumSq& acc, Partial* partials) {
+  __shared__ double s_sum[kThreads / 32];
+  double v = warp_sum(acc.value());
+  if (threadIdx.x % 32 == 0) s_sum[threadIdx.x / 32] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int i = 0; i < kThreads / 32; ++i) tot += s_sum[i];
+    partials[blockIdx.x] = Partial{tot, isfinite(tot) ? 0 : 1, 0};
+    for (int i = gridDim.x + blockIdx.x; i < kMaxGrid; i += gridDim.x)
+      partials[i] = Partial{0.0, 0, 0};
+  }
+}
+
 // ------------------------------------------------------------------- K1 --
 
+// General reduction: any replica count, instances, average_in_collective.
 template <typename GT, bool FULL, bool STATS>
-__global__ void __launch_bounds__(kThreads) k1_reduce_prepare(const __grid_constant__ K1Params p) {
+__global__ void __launch_bounds__(kThreads, DOPT_K1_MIN_BLOCKS)
+k1_reduce_prepare(const __grid_constant__ K1Params p) {
   const int dpi = p.n_rep / p.n_inst;
   SumSq acc;
-  int bad = 0;
   int si = 0;
   for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
     si = seek(p.tab, si, t);
     const Seg& sg = p.tab.seg[si];
-    const int64_t off = (int64_t)(t - sg.tile0) * kTile;
-    const int n = (int)min((int64_t)kTile, (int64_t)sg.len - off);
+    const int64_t off = (int64_t)(t - sg.tile0) * kTile1;
+    const int n = (int)min((int64_t)kTile1, (int64_t)sg.len - off);
     const int64_t l0 = sg.local + off;
     const int64_t r0 = FULL ? sg.world + off : l0;
     const bool aligned = (sg.flags & kSegAligned) != 0;
 
-    ReduceState st[kUnroll][kVec];
-    bool vec_ok[kUnroll];
+    ReduceState st[kUnroll1][kVec];
+    bool vec_ok[kUnroll1];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) vec_ok[u] = aligned && ((u * kThreads + threadIdx.x) * kVec + kVec <= n);
+    for (int u = 0; u < kUnroll1; ++u) vec_ok[u] = aligned && ((u * kThreads + threadIdx.x) * kVec + kVec <= n);
 
-    // vector path: kBatch replicas x kUnroll accesses of kVec elements in flight
+    // kBatch replicas x kUnroll1 accesses of kVec elements in flight
     for (int k0 = 0; k0 < p.n_rep; k0 += kBatch) {
-      float x[kBatch][kUnroll][kVec];
+      float x[kBatch][kUnroll1][kVec];
 #pragma unroll
       for (int kk = 0; kk < kBatch; ++kk) {
         if (k0 + kk < p.n_rep) {
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u) {
+          for (int u = 0; u < kUnroll1; ++u) {
             const int e = (u * kThreads + threadIdx.x) * kVec;
             if (vec_ok[u]) GradT<GT>::widen4(p.rep[k0 + kk], r0 + e, x[kk][u]);
           }
@@ -288,7 +339,7 @@ __global__ void __launch_bounds__(kThreads) k1_reduce_prepare(const __grid_const
         if (k0 + kk < p.n_rep) {
           const ReplicaPos rp = replica_pos(k0 + kk, dpi);
 #pragma unroll
-          for (int u = 0; u < kUnroll; ++u) {
+          for (int u = 0; u < kUnroll1; ++u) {
             if (vec_ok[u]) {
 #pragma unroll
               for (int j = 0; j < kVec; ++j) reduce_term<GT>(st[u][j], x[kk][u][j], rp, p);
@@ -298,20 +349,14 @@ __global__ void __launch_bounds__(kThreads) k1_reduce_prepare(const __grid_const
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kUnroll1; ++u) {
       const int e = (u * kThreads + threadIdx.x) * kVec;
       if (vec_ok[u]) {
         float m[kVec];
 #pragma unroll
         for (int j = 0; j < kVec; ++j) m[j] = reduce_finish<GT>(st[u][j], p);
         __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
-        if (STATS) {
-#pragma unroll
-          for (int j = 0; j < kVec; ++j) {
-            bad |= is_nonfinite(m[j]);
-            acc.add(m[j]);
-          }
-        }
+        if (STATS) acc.add4(m);
       } else if (e < n) {
         // scalar path: the ragged end of a run, or a run whose starts are
         // not 8-element aligned
@@ -324,41 +369,74 @@ __global__ void __launch_bounds__(kThreads) k1_reduce_prepare(const __grid_const
             reduce_term<GT>(s1, GradT<GT>::widen1(p.rep[k], r0 + e + j), replica_pos(k, dpi), p);
           float m = reduce_finish<GT>(s1, p);
           p.main_grad[l0 + e + j] = m;
-          if (STATS) {
-            bad |= is_nonfinite(m);
-            acc.add(m);
-          }
+          if (STATS) acc.add1(m);
         }
       }
     }
     if (STATS) acc.maybe_flush();
   }
+  if (STATS) write_partial(acc, p.partials);
+}
 
-  if (STATS) {
-    __shared__ double s_sum[kThreads / 32];
-    __shared__ int s_bad[kThreads / 32];
-    double v = warp_sum(acc.value());
-    int b = __any_sync(0xFFFFFFFFu, bad);
-    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (lane == 0) {
-      s_sum[w] = v;
-      s_bad[w] = b;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double tot = 0.0;
-      int any = 0;
-      for (int i = 0; i < kThreads / 32; ++i) {
-        tot += s_sum[i];
-        any |= s_bad[i];
+// The common reduction: one optimizer instance, prescale by 1/N and sum
+// (average_in_collective = false), N known at compile time.  Same arithmetic
+// as the general kernel, in the same order, without its per-element
+// selects.
+template <typename GT, bool FULL, bool STATS, int NREP>
+__global__ void __launch_bounds__(kThreads, DOPT_K1_MIN_BLOCKS)
+k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
+  SumSq acc;
+  int si = 0;
+  const float pre = p.pre, inv_scale = p.inv_scale;
+  for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
+    si = seek(p.tab, si, t);
+    const Seg& sg = p.tab.seg[si];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTile1;
+    const int n = (int)min((int64_t)kTile1, (int64_t)sg.len - off);
+    const int64_t l0 = sg.local + off;
+    const int64_t r0 = FULL ? sg.world + off : l0;
+    const bool aligned = (sg.flags & kSegAligned) != 0;
+
+    bool vec_ok[kUnroll1];
+    float x[NREP][kUnroll1][kVec];
+#pragma unroll
+    for (int u = 0; u < kUnroll1; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      vec_ok[u] = aligned && e + kVec <= n;
+      if (vec_ok[u]) {
+#pragma unroll
+        for (int k = 0; k < NREP; ++k) GradT<GT>::widen4(p.rep[k], r0 + e, x[k][u]);
       }
-      p.partials[blockIdx.x] = Partial{tot, any, 0};
-      // slots this launch does not use are zeroed, so the finalize pass can
-      // always sum whole regions
-      for (int i = gridDim.x + blockIdx.x; i < kMaxGrid; i += gridDim.x)
-        p.partials[i] = Partial{0.0, 0, 0};
     }
+#pragma unroll
+    for (int u = 0; u < kUnroll1; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (vec_ok[u]) {
+        float m[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          float sum = __fmul_rn(x[0][u][j], pre);
+#pragma unroll
+          for (int k = 1; k < NREP; ++k) sum = __fadd_rn(sum, __fmul_rn(x[k][u][j], pre));
+          m[j] = __fmul_rn(GradT<GT>::round_to(sum), inv_scale);
+        }
+        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        if (STATS) acc.add4(m);
+      } else if (e < n) {
+        const int cnt = min(kVec, n - e);
+        for (int j = 0; j < cnt; ++j) {
+          float sum = __fmul_rn(GradT<GT>::widen1(p.rep[0], r0 + e + j), pre);
+          for (int k = 1; k < NREP; ++k)
+            sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::widen1(p.rep[k], r0 + e + j), pre));
+          float m = __fmul_rn(GradT<GT>::round_to(sum), inv_scale);
+          p.main_grad[l0 + e + j] = m;
+          if (STATS) acc.add1(m);
+        }
+      }
+    }
+    if (STATS) acc.maybe_flush();
   }
+  if (STATS) write_partial(acc, p.partials);
 }
 
 // ------------------------------------------------------------------- K2 --
@@ -461,7 +539,7 @@ __device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, 
 }
 
 template <typename PT>
-__global__ void __launch_bounds__(kThreads) k3_adamw(const __grid_constant__ K3Params p) {
+__global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw(const __grid_constant__ K3Params p) {
   if (*p.found_inf) return;  // skipped step: nothing is written
   const float c = *p.coef;
   float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
@@ -469,17 +547,17 @@ __global__ void __launch_bounds__(kThreads) k3_adamw(const __grid_constant__ K3P
   for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
     si = seek(p.tab, si, t);
     const Seg& sg = p.tab.seg[si];
-    const int64_t off = (int64_t)(t - sg.tile0) * kTile;
-    const int n = (int)min((int64_t)kTile, (int64_t)sg.len - off);
+    const int64_t off = (int64_t)(t - sg.tile0) * kTile3;
+    const int n = (int)min((int64_t)kTile3, (int64_t)sg.len - off);
     const int64_t l0 = sg.local + off, w0 = sg.world + off;
     const int64_t m0 = ParamT<PT>::kInPlace ? w0 : l0;  // master index
     const bool aligned = (sg.flags & kSegAligned) != 0;
     const float decay = sg.decay;
 
-    float g[kUnroll][kVec], w[kUnroll][kVec], m[kUnroll][kVec], v[kUnroll][kVec];
-    bool vec_ok[kUnroll];
+    float g[kUnroll3][kVec], w[kUnroll3][kVec], m[kUnroll3][kVec], v[kUnroll3][kVec];
+    bool vec_ok[kUnroll3];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kUnroll3; ++u) {
       const int e = (u * kThreads + threadIdx.x) * kVec;
       vec_ok[u] = aligned && e + kVec <= n;
       if (vec_ok[u]) {
@@ -494,7 +572,7 @@ __global__ void __launch_bounds__(kThreads) k3_adamw(const __grid_constant__ K3P
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < kUnroll3; ++u) {
       const int e = (u * kThreads + threadIdx.x) * kVec;
       if (vec_ok[u]) {
 #pragma unroll
@@ -535,7 +613,6 @@ std::vector<Chunk> chunks_of(const std::vector<dopt::Run>& runs) {
   do {
     Chunk c{i, 0, 0};
     while (i < (int)runs.size() && c.count < kMaxSeg) {
-      c.n_tiles += (int)((runs[i].len + kTile - 1) / kTile);
       ++c.count;
       ++i;
     }
@@ -544,8 +621,10 @@ std::vector<Chunk> chunks_of(const std::vector<dopt::Run>& runs) {
   return out;  // at least one (possibly empty) chunk
 }
 
-void fill_table(SegTable& tab, const std::vector<dopt::Run>& runs, const Chunk& c, double lr,
-                double wd) {
+// Fills the kernel-parameter table of one chunk for tiles of `tile`
+// elements; decay (K3 only) from lr and wd.
+void fill_table(SegTable& tab, const std::vector<dopt::Run>& runs, const Chunk& c, int tile_elems,
+                double lr, double wd) {
   tab.n_seg = c.count;
   int tile = 0;
   for (int k = 0; k < c.count; ++k) {
@@ -557,7 +636,7 @@ void fill_table(SegTable& tab, const std::vector<dopt::Run>& runs, const Chunk& 
     s.tile0 = tile;
     s.decay = (float)(1.0 - lr * wd * r.wd_mult);
     s.flags = ((r.local % 8) == 0 && (r.world % 8) == 0) ? kSegAligned : 0;
-    tile += (int)((r.len + kTile - 1) / kTile);
+    tile += (int)((r.len + tile_elems - 1) / tile_elems);
   }
   tab.n_tiles = tile;
 }
@@ -667,12 +746,38 @@ int launch_k1_t(K1Params& kp, int n_tiles, cudaStream_t s) {
   return check_launch("k1_reduce_prepare launch");
 }
 
+template <typename GT, bool FULL, bool STATS, int NREP>
+int launch_k1_n(K1Params& kp, int n_tiles, cudaStream_t s) {
+  auto kern = k1_reduce_prepare_n<GT, FULL, STATS, NREP>;
+  int grid = 0;
+  int st = grid_for(kern, n_tiles, &grid);
+  if (st) return st;
+  kern<<<grid, kThreads, 0, s>>>(kp);
+  return check_launch("k1_reduce_prepare_n launch");
+}
+
+// The specialised kernel covers one instance with prescale-and-sum and
+// 1, 2, 4 or 8 replicas; everything else runs the general kernel.
+template <typename GT, bool FULL, bool STATS>
+int launch_k1_g(K1Params& kp, int n_tiles, cudaStream_t s) {
+  if (kp.n_inst == 1 && !kp.average) {
+    switch (kp.n_rep) {
+      case 1: return launch_k1_n<GT, FULL, STATS, 1>(kp, n_tiles, s);
+      case 2: return launch_k1_n<GT, FULL, STATS, 2>(kp, n_tiles, s);
+      case 4: return launch_k1_n<GT, FULL, STATS, 4>(kp, n_tiles, s);
+      case 8: return launch_k1_n<GT, FULL, STATS, 8>(kp, n_tiles, s);
+      default: break;
+    }
+  }
+  return launch_k1_t<GT, FULL, STATS>(kp, n_tiles, s);
+}
+
 template <bool FULL, bool STATS>
 int launch_k1_dt(int32_t gdt, K1Params& kp, int n_tiles, cudaStream_t s) {
   switch (gdt) {
-    case DOPT_F32: return launch_k1_t<float, FULL, STATS>(kp, n_tiles, s);
-    case DOPT_BF16: return launch_k1_t<__nv_bfloat16, FULL, STATS>(kp, n_tiles, s);
-    case DOPT_F16: return launch_k1_t<__half, FULL, STATS>(kp, n_tiles, s);
+    case DOPT_F32: return launch_k1_g<float, FULL, STATS>(kp, n_tiles, s);
+    case DOPT_BF16: return launch_k1_g<__nv_bfloat16, FULL, STATS>(kp, n_tiles, s);
+    case DOPT_F16: return launch_k1_g<__half, FULL, STATS>(kp, n_tiles, s);
   }
   return dopt::fail(DOPT_E_INVALID, "unknown grad dtype");
 }
@@ -699,14 +804,15 @@ int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* r
     kp.inv_scale = inv_scale;
     kp.average = average ? 1 : 0;
     kp.pad = 0;
-    fill_table(kp.tab, runs, c, 0.0, 0.0);
+    fill_table(kp.tab, runs, c, kTile1, 0.0, 0.0);
+    const int n_tiles = kp.tab.n_tiles;
     int st;
     if (stats)
-      st = full_layout ? launch_k1_dt<true, true>(gdt, kp, c.n_tiles, s)
-                       : launch_k1_dt<false, true>(gdt, kp, c.n_tiles, s);
+      st = full_layout ? launch_k1_dt<true, true>(gdt, kp, n_tiles, s)
+                       : launch_k1_dt<false, true>(gdt, kp, n_tiles, s);
     else
-      st = full_layout ? launch_k1_dt<true, false>(gdt, kp, c.n_tiles, s)
-                       : launch_k1_dt<false, false>(gdt, kp, c.n_tiles, s);
+      st = full_layout ? launch_k1_dt<true, false>(gdt, kp, n_tiles, s)
+                       : launch_k1_dt<false, false>(gdt, kp, n_tiles, s);
     if (st) return st;
   }
   return DOPT_OK;
@@ -773,12 +879,13 @@ int run_k3(dopt_shard_map* m, int32_t buffer, int32_t rank, const float* main_gr
     kp.step_size = (float)(hp->lr / (1.0 - pow_int(hp->beta1, hp->step)));
     kp.bc2_sqrt = (float)std::sqrt(1.0 - pow_int(hp->beta2, hp->step));
     kp.pad = 0;
-    fill_table(kp.tab, runs, c, hp->lr, hp->weight_decay);
+    fill_table(kp.tab, runs, c, kTile3, hp->lr, hp->weight_decay);
+    const int n_tiles = kp.tab.n_tiles;
     int st;
     switch (pdt) {
-      case DOPT_BF16: st = launch_k3_t<__nv_bfloat16>(kp, c.n_tiles, s); break;
-      case DOPT_F16: st = launch_k3_t<__half>(kp, c.n_tiles, s); break;
-      default: st = launch_k3_t<float>(kp, c.n_tiles, s); break;
+      case DOPT_BF16: st = launch_k3_t<__nv_bfloat16>(kp, n_tiles, s); break;
+      case DOPT_F16: st = launch_k3_t<__half>(kp, n_tiles, s); break;
+      default: st = launch_k3_t<float>(kp, n_tiles, s); break;
     }
     if (st) return st;
   }
