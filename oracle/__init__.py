@@ -64,6 +64,14 @@ def lib():
     return _lib
 
 
+def ctypes_byref(x):
+    return ctypes.byref(x)
+
+
+def ctypes_double(v=0.0):
+    return ctypes.c_double(v)
+
+
 def _ptr(a, offset=0):
     return ctypes.c_void_p(a.ctypes.data + offset * a.itemsize)
 

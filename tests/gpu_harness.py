@@ -310,3 +310,204 @@ def run_parity(cfg, steps=None, separate=False):
         if not ores["found_inf"]:
             hc.t_applied += 1
     return ok, report
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads: inputs filled on the device by the generator, the
+# oracle streams the grad norm over every element and recomputes sampled
+# elements one by one.
+
+class FullCase:
+    """A workload at its full size on the GPU, checked on samples."""
+
+    def __init__(self, cfg):
+        import torch
+        D = dopt()
+        self.torch, self.cfg = torch, cfg
+        dp, bs = cfg["dp"], cfg["bucket_size"]
+        self.om = oracle.ShardMap(cfg["params"], dp, bs, cfg["grad_reduce_in_fp32"])
+        self.pm = D.dopt_build_shard_map(cfg["params"], dp, -1 if bs is None else bs,
+                                         cfg["grad_reduce_in_fp32"], False)
+        self.all_ranks = cfg["ranks"] == "all"
+        self.ranks = list(range(dp)) if self.all_ranks else list(cfg["ranks"])
+        self.rank_arg = D.ALL_RANKS if self.all_ranks else self.ranks[0]
+        self.n_rep = dp * cfg["n_inst"]
+        self.seed = cfg["seed"]
+        self.stream = torch.cuda.current_stream().cuda_stream
+        dev = torch.device("cuda")
+        tdt = {F32: torch.float32, BF16: torch.int16, F16: torch.int16}
+        self.pkey = synth.key(self.seed, synth.STREAM_PARAM, 0, 0)
+        self.params, self.master, self.m, self.v, self.main, self.reps = [], [], [], [], [], []
+        for bi, buf in enumerate(self.om.buffers):
+            S = self.om.shard_numel(bi)
+            n_local = len(self.ranks) * S
+            p = torch.empty(buf.numel, dtype=tdt[buf.param_dtype], device=dev)
+            synth.cuda_normal_(p.data_ptr(), buf.numel, self.pkey, 0, cfg["param_sigma"],
+                               KIND[buf.param_dtype], self.stream)
+            self.params.append(p)
+            if buf.param_dtype == F32:
+                self.master.append(None)
+            else:
+                mt = torch.empty(n_local, dtype=torch.float32, device=dev)
+                self._fill_local(bi, mt, self.pkey, cfg["param_sigma"], VALUE_KIND[buf.param_dtype])
+                self.master.append(mt)
+            self.m.append(torch.zeros(n_local, dtype=torch.float32, device=dev))
+            self.v.append(torch.zeros(n_local, dtype=torch.float32, device=dev))
+            self.main.append(torch.zeros(n_local, dtype=torch.float32, device=dev))
+            n_rep_elems = buf.numel if cfg["layout"] == "full" else S
+            self.reps.append([torch.empty(n_rep_elems, dtype=tdt[buf.grad_dtype], device=dev)
+                              for _ in range(self.n_rep)])
+        self.ws_bytes = D.dopt_workspace_bytes(self.pm, self.rank_arg)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+
+    def _fill_local(self, bi, t, key, sigma, kind):
+        S = self.om.shard_numel(bi)
+        for slot, r in enumerate(self.ranks):
+            for b in range(len(self.om.buffers[bi].buckets)):
+                rg = self.om.bucket_world_range(bi, b, r)
+                off = slot * S + self.om.bucket_shard_base(bi, b)
+                synth.cuda_normal_(t.data_ptr() + off * t.element_size(), rg.size, key, rg.start,
+                                   sigma, kind, self.stream)
+
+    def fill_grads(self, t):
+        cfg = self.cfg
+        for bi, buf in enumerate(self.om.buffers):
+            for k, rep in enumerate(self.reps[bi]):
+                key = synth.key(self.seed, synth.STREAM_GRAD, t, k)
+                if cfg["layout"] == "full":
+                    synth.cuda_normal_(rep.data_ptr(), buf.numel, key, 0, cfg["grad_sigma"],
+                                       KIND[buf.grad_dtype], self.stream)
+                else:
+                    self._fill_local(bi, rep, key, cfg["grad_sigma"], KIND[buf.grad_dtype])
+        self.torch.cuda.synchronize()
+
+    def step(self, t):
+        D = dopt()
+        cfg = self.cfg
+        args = D.StepArgs(self.pm, self.rank_arg, self.reps, self.main, self.master, self.m, self.v,
+                          self.params, cfg["hp"], t, self.ws, self.ws_bytes,
+                          n_instances=cfg["n_inst"],
+                          layout=D.LAYOUT_FULL_BUFFER if cfg["layout"] == "full" else D.LAYOUT_SHARD_ONLY,
+                          average_in_collective=cfg["average"],
+                          inv_loss_scale=float(np.float32(1.0 / cfg["loss_scale"])),
+                          max_norm=cfg["max_norm"], stream=self.torch.cuda.current_stream())
+        return D.dopt_step(args)
+
+    def pieces(self):
+        """(buffer, slot, param id, flat offset, buffer offset, length) of
+        every param piece of the selected ranks."""
+        out = []
+        for bi in range(len(self.om.buffers)):
+            S = self.om.shard_numel(bi)
+            for slot, r in enumerate(self.ranks):
+                for pid, _, v in self.om.rank_pieces(bi, r):
+                    out.append((bi, slot, pid, slot * S + v["shard_offset"], v["gbuf_world"].start,
+                                v["gbuf_local"].size))
+        return out
+
+    def oracle_sumsq(self, t, chunk=1 << 22):
+        """The oracle's fp64 sum of squares of every main grad of step t,
+        streamed from the generator, in parallel over chunks of the pieces
+        (threads: the C oracle releases the GIL)."""
+        import os
+        from concurrent.futures import ThreadPoolExecutor
+        cfg = self.cfg
+        keys = [synth.key(self.seed, synth.STREAM_GRAD, t, k) for k in range(self.n_rep)]
+        inv = float(np.float32(1.0 / cfg["loss_scale"]))
+        jobs = []
+        for bi, slot, pid, lo, w, n in self.pieces():
+            gdt = self.om.buffers[bi].grad_dtype
+            for o in range(0, n, chunk):
+                jobs.append((gdt, w + o, min(chunk, n - o)))
+        fac = synth.factor(cfg["grad_sigma"])
+
+        def run(j):
+            return oracle.stream_sumsq(keys, j[0], fac, j[1], j[2], inv, cfg["n_inst"], cfg["average"])
+        with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+            res = list(ex.map(run, jobs))
+        return sum(r[0] for r in res), sum(r[1] for r in res)
+
+    def choose_samples(self, n_random, seed=0):
+        """First and last element of every piece plus random elements."""
+        rng = np.random.RandomState(seed)
+        pcs = self.pieces()
+        out = []
+        for bi, slot, pid, lo, w, n in pcs:
+            out.append((bi, pid, lo, w))
+            out.append((bi, pid, lo + n - 1, w + n - 1))
+        lens = np.array([p[5] for p in pcs], dtype=np.float64)
+        pick = rng.choice(len(pcs), size=n_random, p=lens / lens.sum())
+        for i in pick:
+            bi, slot, pid, lo, w, n = pcs[i]
+            o = int(rng.randint(0, n))
+            out.append((bi, pid, lo + o, w + o))
+        return sorted(set(out))
+
+    def initial_sample_state(self, samples):
+        cfg = self.cfg
+        st = {}
+        for bi in range(len(self.om.buffers)):
+            sel = [s for s in samples if s[0] == bi]
+            if not sel:
+                continue
+            w = np.array([s[3] for s in sel], dtype=np.uint64)
+            pdt = self.om.buffers[bi].param_dtype
+            kind = synth.OUT_F32 if pdt == F32 else VALUE_KIND[pdt]
+            st[bi] = {"sel": sel, "master": synth.normal_at(w, self.pkey, cfg["param_sigma"], kind),
+                      "exp_avg": np.zeros(len(sel), np.float32),
+                      "exp_avg_sq": np.zeros(len(sel), np.float32)}
+        return st
+
+    def oracle_samples(self, st, t_step, t, coef, clip):
+        """Advances the sampled elements' state by one applied step (oracle).
+        Returns the main grads per buffer; st is updated in place and gains
+        the expected 16-bit param bits under "param"."""
+        cfg = self.cfg
+        L = oracle.lib()
+        h = oracle.Hparams(**cfg["hp"])
+        mains = {}
+        for bi, s in st.items():
+            buf = self.om.buffers[bi]
+            w = np.array([x[3] for x in s["sel"]], dtype=np.uint64)
+            reps = [synth.normal_at(w, synth.key(self.seed, synth.STREAM_GRAD, t_step, k),
+                                    cfg["grad_sigma"], KIND[buf.grad_dtype])
+                    for k in range(self.n_rep)]
+            main, _ = oracle.reduce_prepare(reps, buf.grad_dtype, 0, len(w),
+                                            float(np.float32(1.0 / cfg["loss_scale"])),
+                                            cfg["n_inst"], cfg["average"])
+            mains[bi] = main
+            if t is None:
+                continue
+            wd = np.array([float(cfg["params"][x[1]].get("wd_mult", 1.0)) for x in s["sel"]])
+            out = np.zeros(len(w), np.uint16 if buf.param_dtype != F32 else np.float32)
+            for val in np.unique(wd):
+                idx = np.nonzero(wd == val)[0]
+                sub = {k: np.ascontiguousarray(s[k][idx]) for k in ("master", "exp_avg", "exp_avg_sq")}
+                sub_main = np.ascontiguousarray(main[idx])
+                sub_out = np.zeros(len(idx), out.dtype)
+                L.or_adamw_run(sub_main.ctypes.data, len(idx), coef, int(clip), sub["master"].ctypes.data,
+                               sub["exp_avg"].ctypes.data, sub["exp_avg_sq"].ctypes.data,
+                               oracle.ctypes_byref(h), float(val), t,
+                               sub_out.ctypes.data if buf.param_dtype != F32 else None,
+                               buf.param_dtype)
+                for k in sub:
+                    s[k][idx] = sub[k]
+                out[idx] = sub_out if buf.param_dtype != F32 else sub["master"]
+            s["param"] = out
+        return mains
+
+    def device_samples(self, st):
+        torch = self.torch
+        got = {}
+        for bi, s in st.items():
+            lo = torch.tensor([x[2] for x in s["sel"]], dtype=torch.int64, device="cuda")
+            w = torch.tensor([x[3] for x in s["sel"]], dtype=torch.int64, device="cuda")
+            g = {"main": self.main[bi][lo].cpu().numpy(), "exp_avg": self.m[bi][lo].cpu().numpy(),
+                 "exp_avg_sq": self.v[bi][lo].cpu().numpy()}
+            p = self.params[bi][w].cpu().numpy()
+            g["param"] = p.view(np.uint16) if p.dtype == np.int16 else p
+            g["master"] = (self.master[bi][lo].cpu().numpy() if self.master[bi] is not None
+                           else g["param"])
+            got[bi] = g
+        return got

@@ -1,0 +1,103 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times (same map, layout, rank selection, sizes and entry point).
+
+The oracle cannot hold these inputs, so it checks what it can compute one
+by one: found_inf exactly; the grad norm against its own fp64 sum of squares
+streamed from the generator over every element (rel 1e-5); and thousands of
+sampled elements -- the first and last element of every param piece plus
+random ones -- recomputed from their replica grads (main grad bit-exact,
+master/m/v within 4 ulp or 1e-6 of the operand scale, 16-bit params within
+1 ulp).  A step with an injected inf must leave every sampled state
+bit-identical.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import gpu_harness as H  # noqa: E402
+import oracle  # noqa: E402
+
+INF_BITS = {H.F32: float("inf"), H.BF16: 0x7F80, H.F16: 0x7C00}
+
+
+def _inf_position(fc):
+    buf = fc.om.buffers[0]
+    target = int(buf.numel_unpadded * fc.cfg["inf_at"]["buffer_frac"])
+    best = None
+    for pid in buf.params:
+        s, e, _ = buf.index[pid]
+        if e > target and e > s:
+            w = max(s, target)
+            best = w if best is None else min(best, w)
+    return best
+
+
+def _run(cfg, steps, n_random=3000):
+    fc = H.FullCase(cfg)
+    samples = fc.choose_samples(n_random)
+    st = fc.initial_sample_state(samples)
+    t_applied = 0
+    L = oracle.lib()
+    for t_step in range(1, steps + 1):
+        fc.fill_grads(t_step)
+        spec = cfg.get("inf_at")
+        inject = spec is not None and spec["step"] == t_step
+        if inject:
+            assert cfg["layout"] == "full"
+            fc.reps[0][spec["replica"]][_inf_position(fc)] = INF_BITS[fc.om.buffers[0].grad_dtype]
+        before_dev = fc.device_samples(st)
+        t = t_applied + 1
+        found, norm = fc.step(t)
+        if inject:
+            assert found and math.isnan(norm)
+            after = fc.device_samples(st)
+            for bi in after:
+                for k in ("master", "exp_avg", "exp_avg_sq", "param"):
+                    assert after[bi][k].tobytes() == before_dev[bi][k].tobytes(), (bi, k)
+            continue
+        sumsq, bad = fc.oracle_sumsq(t_step)
+        assert bad == 0 and not found
+        o_norm, coef = oracle.ctypes_double(), oracle.ctypes_double()
+        clip = L.or_clip_coef(sumsq, cfg["max_norm"], oracle.ctypes_byref(o_norm),
+                              oracle.ctypes_byref(coef))
+        assert abs(norm - o_norm.value) <= 1e-5 * o_norm.value, (norm, o_norm.value)
+        prev = {bi: {k: v.copy() for k, v in s.items() if k != "sel"} for bi, s in st.items()}
+        mains = fc.oracle_samples(st, t_step, t, coef.value, clip)
+        got = fc.device_samples(st)
+        for bi, s in st.items():
+            g = got[bi]
+            assert np.array_equal(g["main"].view(np.uint32), mains[bi].view(np.uint32)), bi
+            for k in ("master", "exp_avg", "exp_avg_sq"):
+                ok = H.state_close(g[k], s[k], prev[bi][k])
+                assert ok.all(), (bi, k, int((~ok).sum()))
+            if s["param"].dtype == np.uint16:
+                assert H.ulp16(g["param"], s["param"]).max() <= 1, bi
+        t_applied += 1
+    del fc
+    torch.cuda.empty_cache()
+
+
+def test_bench_workload_llama7b_dp8_rank0():
+    _run(W.config("llama_7b_dp8_rank0"), steps=2)
+
+
+def test_hierarchical_llama7b_dp16_2x8_1m_buckets():
+    _run(W.config("llama_7b_dp16_2x8_1m"), steps=1)
+
+
+def test_gpt2_small_all_ranks_with_skipped_step():
+    _run(W.config("gpt2_small_dp8"), steps=3)
+
+
+def test_llama_1p3b_fp16_loss_scaled():
+    _run(W.config("llama_1p3b_fp16_dp8"), steps=1)
