@@ -45,7 +45,7 @@ namespace {
 #define DOPT_K3_UNROLL 4
 #endif
 #ifndef DOPT_K1_MIN_BLOCKS
-#define DOPT_K1_MIN_BLOCKS 1
+#define DOPT_K1_MIN_BLOCKS 2
 #endif
 #ifndef DOPT_K3_MIN_BLOCKS
 #define DOPT_K3_MIN_BLOCKS 2
@@ -127,10 +127,22 @@ static_assert(sizeof(K1Params) <= 32764 && sizeof(K3Params) <= 32764, "kernel pa
 
 // ---------------------------------------------------------------- helpers --
 
+// Loads of kVec grad elements are held in their raw encoding (float4 for
+// fp32, two packed 16-bit pairs for bf16/fp16) until the reduction widens
+// them, so a 16-bit grad keeps half the registers of an fp32 one and a
+// thread can keep twice as many 16-bit accesses in flight.
 template <typename T>
 struct GradT;
 template <>
 struct GradT<float> {
+  using Raw = float4;
+  static constexpr int kUnroll = 1;  // multiplier of kUnroll1 for this type
+  static __device__ __forceinline__ Raw load4(const void* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    return j == 0 ? r.x : j == 1 ? r.y : j == 2 ? r.z : r.w;
+  }
   static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
     return __ldcs(static_cast<const float*>(p) + i);
   }
@@ -142,6 +154,15 @@ struct GradT<float> {
 };
 template <>
 struct GradT<__nv_bfloat16> {
+  using Raw = uint2;
+  static constexpr int kUnroll = 2;
+  static __device__ __forceinline__ Raw load4(const void* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    const unsigned w = j < 2 ? r.x : r.y;
+    return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
   static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
     unsigned short b = __ldcs(static_cast<const unsigned short*>(p) + i);
     return __uint_as_float((unsigned)b << 16);
@@ -157,6 +178,15 @@ struct GradT<__nv_bfloat16> {
 };
 template <>
 struct GradT<__half> {
+  using Raw = uint2;
+  static constexpr int kUnroll = 2;
+  static __device__ __forceinline__ Raw load4(const void* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    const unsigned w = j < 2 ? r.x : r.y;
+    return __half2float(__ushort_as_half((unsigned short)((j & 1) ? (w >> 16) : (w & 0xFFFFu))));
+  }
   static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
     unsigned short b = __ldcs(static_cast<const unsigned short*>(p) + i);
     return __half2float(__ushort_as_half(b));
@@ -378,58 +408,82 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
   if (STATS) write_partial(acc, p.partials);
 }
 
-// The common reduction: one optimizer instance, prescale by 1/N and sum
-// (average_in_collective = false), N known at compile time.  Same arithmetic
-// as the general kernel, in the same order, without its per-element
-// selects.
-template <typename GT, bool FULL, bool STATS, int NREP>
+// The common reductions: prescale by 1/N and sum (average_in_collective =
+// false), NINST instances of DPI replicas each, both known at compile time.
+// Same arithmetic as the general kernel, in the same order (each instance's
+// replicas summed in order and rounded to the grad dtype, then the instance
+// sums in order, rounded again when there is more than one), without its
+// per-element selects.  Loads of one instance are in flight together.
+template <typename GT, bool FULL, bool STATS, int DPI, int NINST>
 __global__ void __launch_bounds__(kThreads, DOPT_K1_MIN_BLOCKS)
 k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
+  constexpr int U = kUnroll1 * GradT<GT>::kUnroll;  // accesses per thread per tile
+  constexpr int TILE = kThreads * kVec * U;
   SumSq acc;
   int si = 0;
   const float pre = p.pre, inv_scale = p.inv_scale;
   for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
     si = seek(p.tab, si, t);
     const Seg& sg = p.tab.seg[si];
-    const int64_t off = (int64_t)(t - sg.tile0) * kTile1;
-    const int n = (int)min((int64_t)kTile1, (int64_t)sg.len - off);
+    const int64_t off = (int64_t)(t - sg.tile0) * TILE;
+    const int n = (int)min((int64_t)TILE, (int64_t)sg.len - off);
     const int64_t l0 = sg.local + off;
     const int64_t r0 = FULL ? sg.world + off : l0;
     const bool aligned = (sg.flags & kSegAligned) != 0;
 
-    bool vec_ok[kUnroll1];
-    float x[NREP][kUnroll1][kVec];
+    bool vec_ok[U];
 #pragma unroll
-    for (int u = 0; u < kUnroll1; ++u) {
-      const int e = (u * kThreads + threadIdx.x) * kVec;
-      vec_ok[u] = aligned && e + kVec <= n;
-      if (vec_ok[u]) {
+    for (int u = 0; u < U; ++u) vec_ok[u] = aligned && (u * kThreads + threadIdx.x) * kVec + kVec <= n;
+    float total[U][kVec];
+#pragma unroll 1
+    for (int j = 0; j < NINST; ++j) {  // one instance's loads live at a time
+      typename GradT<GT>::Raw x[DPI][U];
 #pragma unroll
-        for (int k = 0; k < NREP; ++k) GradT<GT>::widen4(p.rep[k], r0 + e, x[k][u]);
+      for (int u = 0; u < U; ++u) {
+        const int e = (u * kThreads + threadIdx.x) * kVec;
+        if (vec_ok[u]) {
+#pragma unroll
+          for (int k = 0; k < DPI; ++k) x[k][u] = GradT<GT>::load4(p.rep[j * DPI + k], r0 + e);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          float sum = __fmul_rn(GradT<GT>::at(x[0][u], q), pre);
+#pragma unroll
+          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::at(x[k][u], q), pre));
+          sum = GradT<GT>::round_to(sum);
+          total[u][q] = (j == 0) ? sum : __fadd_rn(total[u][q], sum);
+        }
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll1; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int e = (u * kThreads + threadIdx.x) * kVec;
       if (vec_ok[u]) {
         float m[kVec];
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-          float sum = __fmul_rn(x[0][u][j], pre);
-#pragma unroll
-          for (int k = 1; k < NREP; ++k) sum = __fadd_rn(sum, __fmul_rn(x[k][u][j], pre));
-          m[j] = __fmul_rn(GradT<GT>::round_to(sum), inv_scale);
+        for (int q = 0; q < kVec; ++q) {
+          float tt = NINST > 1 ? GradT<GT>::round_to(total[u][q]) : total[u][q];
+          m[q] = __fmul_rn(tt, inv_scale);
         }
         __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
         if (STATS) acc.add4(m);
       } else if (e < n) {
         const int cnt = min(kVec, n - e);
-        for (int j = 0; j < cnt; ++j) {
-          float sum = __fmul_rn(GradT<GT>::widen1(p.rep[0], r0 + e + j), pre);
-          for (int k = 1; k < NREP; ++k)
-            sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::widen1(p.rep[k], r0 + e + j), pre));
-          float m = __fmul_rn(GradT<GT>::round_to(sum), inv_scale);
-          p.main_grad[l0 + e + j] = m;
+        for (int q = 0; q < cnt; ++q) {
+          float tt = 0.f;
+          for (int j = 0; j < NINST; ++j) {
+            float sum = __fmul_rn(GradT<GT>::widen1(p.rep[j * DPI], r0 + e + q), pre);
+            for (int k = 1; k < DPI; ++k)
+              sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::widen1(p.rep[j * DPI + k], r0 + e + q), pre));
+            sum = GradT<GT>::round_to(sum);
+            tt = (j == 0) ? sum : __fadd_rn(tt, sum);
+          }
+          if (NINST > 1) tt = GradT<GT>::round_to(tt);
+          float m = __fmul_rn(tt, inv_scale);
+          p.main_grad[l0 + e + q] = m;
           if (STATS) acc.add1(m);
         }
       }
@@ -746,9 +800,9 @@ int launch_k1_t(K1Params& kp, int n_tiles, cudaStream_t s) {
   return check_launch("k1_reduce_prepare launch");
 }
 
-template <typename GT, bool FULL, bool STATS, int NREP>
+template <typename GT, bool FULL, bool STATS, int DPI, int NINST>
 int launch_k1_n(K1Params& kp, int n_tiles, cudaStream_t s) {
-  auto kern = k1_reduce_prepare_n<GT, FULL, STATS, NREP>;
+  auto kern = k1_reduce_prepare_n<GT, FULL, STATS, DPI, NINST>;
   int grid = 0;
   int st = grid_for(kern, n_tiles, &grid);
   if (st) return st;
@@ -756,17 +810,27 @@ int launch_k1_n(K1Params& kp, int n_tiles, cudaStream_t s) {
   return check_launch("k1_reduce_prepare_n launch");
 }
 
-// The specialised kernel covers one instance with prescale-and-sum and
-// 1, 2, 4 or 8 replicas; everything else runs the general kernel.
+// The specialised kernel covers prescale-and-sum with one instance of 1, 2,
+// 4 or 8 replicas, or two instances of 4 or 8; everything else runs the
+// general kernel.
 template <typename GT, bool FULL, bool STATS>
 int launch_k1_g(K1Params& kp, int n_tiles, cudaStream_t s) {
-  if (kp.n_inst == 1 && !kp.average) {
-    switch (kp.n_rep) {
-      case 1: return launch_k1_n<GT, FULL, STATS, 1>(kp, n_tiles, s);
-      case 2: return launch_k1_n<GT, FULL, STATS, 2>(kp, n_tiles, s);
-      case 4: return launch_k1_n<GT, FULL, STATS, 4>(kp, n_tiles, s);
-      case 8: return launch_k1_n<GT, FULL, STATS, 8>(kp, n_tiles, s);
-      default: break;
+  if (!kp.average) {
+    const int dpi = kp.n_rep / kp.n_inst;
+    if (kp.n_inst == 1) {
+      switch (dpi) {
+        case 1: return launch_k1_n<GT, FULL, STATS, 1, 1>(kp, n_tiles, s);
+        case 2: return launch_k1_n<GT, FULL, STATS, 2, 1>(kp, n_tiles, s);
+        case 4: return launch_k1_n<GT, FULL, STATS, 4, 1>(kp, n_tiles, s);
+        case 8: return launch_k1_n<GT, FULL, STATS, 8, 1>(kp, n_tiles, s);
+        default: break;
+      }
+    } else if (kp.n_inst == 2) {
+      switch (dpi) {
+        case 4: return launch_k1_n<GT, FULL, STATS, 4, 2>(kp, n_tiles, s);
+        case 8: return launch_k1_n<GT, FULL, STATS, 8, 2>(kp, n_tiles, s);
+        default: break;
+      }
     }
   }
   return launch_k1_t<GT, FULL, STATS>(kp, n_tiles, s);
@@ -780,6 +844,17 @@ int launch_k1_dt(int32_t gdt, K1Params& kp, int n_tiles, cudaStream_t s) {
     case DOPT_F16: return launch_k1_g<__half, FULL, STATS>(kp, n_tiles, s);
   }
   return dopt::fail(DOPT_E_INVALID, "unknown grad dtype");
+}
+
+// Tile size (elements) of the K1 kernel that runs for these arguments: the
+// specialised kernels give 16-bit grads twice the accesses per thread.
+int k1_tile(int32_t gdt, int32_t n_rep, int32_t n_inst, int32_t average) {
+  if (average) return kTile1;
+  const int dpi = n_rep / n_inst;
+  const bool special = (n_inst == 1 && (dpi == 1 || dpi == 2 || dpi == 4 || dpi == 8)) ||
+                       (n_inst == 2 && (dpi == 4 || dpi == 8));
+  if (!special) return kTile1;
+  return gdt == DOPT_F32 ? kTile1 : 2 * kTile1;
 }
 
 // Launches K1 over every chunk of (buffer, rank).  stats: write partials to
@@ -804,7 +879,7 @@ int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* r
     kp.inv_scale = inv_scale;
     kp.average = average ? 1 : 0;
     kp.pad = 0;
-    fill_table(kp.tab, runs, c, kTile1, 0.0, 0.0);
+    fill_table(kp.tab, runs, c, k1_tile(gdt, n_rep, n_inst, average), 0.0, 0.0);
     const int n_tiles = kp.tab.n_tiles;
     int st;
     if (stats)

@@ -101,3 +101,7 @@ def test_gpt2_small_all_ranks_with_skipped_step():
 
 def test_llama_1p3b_fp16_loss_scaled():
     _run(W.config("llama_1p3b_fp16_dp8"), steps=1)
+
+
+def test_bf16_replica_grads_fp32_accumulation():
+    _run(W.config("llama_7b_dp8_rank0_bf16grads"), steps=1)
