@@ -59,6 +59,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--staged", action="store_true",
+                   help="time the bucket-staged step against the fused step, with the grads "
+                        "produced bucket by bucket by a stand-in for the backward pass")
     return p.parse_args(argv)
 
 
@@ -481,10 +484,96 @@ def run_ours(args):
     return 0
 
 
+def run_staged(args):
+    """Overlap of the per-bucket reduce with the production of the grads.
+
+    Each step first produces the replica grads (the generator's fill kernel
+    writing every replica's slice of a bucket stands in for the backward pass
+    finishing that bucket), then steps.  Sequential: produce every bucket,
+    then the fused step.  Staged: as soon as a bucket is produced, its
+    reduce/prepare runs on a side stream; after the last bucket, the norm
+    finalize, then AdamW and the write-back bucket by bucket in forward order
+    (last bucket first)."""
+    import torch
+    import synth
+    import mixed_precision_adam_gb300 as D
+    cfg = workload_config(args.workload, args.layers)
+    wl = Workload(cfg)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    kinds = {F32: synth.OUT_F32, BF16: synth.OUT_BF16, F16: synth.OUT_F16}
+    buckets = []
+    for b in range(D.dopt_num_buffers(wl.pm)):
+        info = D.dopt_buffer_info_get(wl.pm, b)
+        for k in range(info["n_buckets"]):
+            buckets.append((b, k, info, D.dopt_bucket_info_get(wl.pm, b, k)))
+
+    def produce(b, k, info, bk):
+        s = bk["shard_numel"]
+        for r, t in enumerate(wl.reps[b]):
+            synth.cuda_normal_(t.data_ptr() + bk["shard_base"] * t.element_size(), s,
+                               synth.key(cfg["seed"], synth.STREAM_GRAD, 1, r),
+                               bk["offset"] + wl.rank * s, cfg["grad_sigma"],
+                               kinds[info["grad_dtype"]], main.cuda_stream)
+
+    fused = wl.args()
+    staged = wl.args()
+    ws_b = D.dopt_workspace_bytes_bucketed(wl.pm, wl.rank)
+    bws = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+    staged.c.workspace, staged.c.workspace_bytes = bws.data_ptr(), ws_b
+
+    def step_fused():
+        for x in buckets:
+            produce(*x)
+        fused.set_step(wl.t_applied + 1)
+        D.dopt_step_async(fused)
+
+    def step_staged():
+        staged.set_step(wl.t_applied + 1)
+        staged.set_stream(side)
+        for (b, k, info, bk) in buckets:
+            produce(b, k, info, bk)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            side.wait_event(ev)
+            D.dopt_step_reduce_buckets(staged, b, k, 1)
+        done = torch.cuda.Event()
+        done.record(side)
+        main.wait_event(done)
+        staged.set_stream(main)
+        D.dopt_step_finalize(staged)
+        for (b, k, info, bk) in reversed(buckets):
+            D.dopt_step_update_buckets(staged, b, k, 1)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    t_fused = timed(step_fused)
+    t_staged = timed(step_staged)
+    line = {"metric": "grad production + step, fused vs bucket-staged (ms per step)",
+            "workload": describe(cfg, wl.elements), "buckets": len(buckets),
+            "steps": args.steps, "warmup": args.warmup,
+            "produce_then_fused_ms": t_fused, "bucket_staged_overlapped_ms": t_staged,
+            "saving_ms": t_fused - t_staged}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.staged:
+        return run_staged(args)
     return run_ours(args)
 
 

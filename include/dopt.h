@@ -301,6 +301,34 @@ int dopt_step(const dopt_step_args* args, int32_t* found_inf_out, float* grad_no
 int dopt_step_async(const dopt_step_args* args, int32_t* d_found_inf, float* d_norm);
 
 /*
+ * Bucket-staged step: the same arithmetic as dopt_step, split so the
+ * reduce/prepare pass can run bucket by bucket as each bucket's grads become
+ * ready, and the AdamW/write-back pass bucket by bucket in the order the next
+ * forward pass needs the params.  distrib_optimizer page section 7.1
+ * (overlap_grad_reduce: a bucket's reduce-scatter starts as soon as all its
+ * grads are ready) and 7.2 (overlap_param_gather: the param all-gather of a
+ * bucket is waited on by the forward pre-hook, which then launches the next
+ * bucket's).
+ *
+ * Sequence for one step, all with the same args (args->stream may change
+ * between calls; the caller orders the streams with events):
+ *   1. dopt_step_reduce_buckets for every bucket of every buffer, exactly
+ *      once (any grouping, any order);
+ *   2. dopt_step_finalize (norm, clip coefficient, skip decision);
+ *   3. dopt_step_update_buckets for every bucket of every buffer (skipped on
+ *      the device when found_inf).
+ * The workspace must hold dopt_workspace_bytes_bucketed(map, rank) bytes (one
+ * partial-sum region per bucket); args->stage_events is not used.  A bucket
+ * left out of step 1 leaves stale partials behind, and the norm is wrong.
+ */
+size_t dopt_workspace_bytes_bucketed(const dopt_shard_map* map, int32_t rank);
+int dopt_step_reduce_buckets(const dopt_step_args* args, int32_t buffer, int32_t bucket_first,
+                             int32_t bucket_count);
+int dopt_step_finalize(const dopt_step_args* args, int32_t* d_found_inf, float* d_norm);
+int dopt_step_update_buckets(const dopt_step_args* args, int32_t buffer, int32_t bucket_first,
+                             int32_t bucket_count);
+
+/*
  * dopt_step_noalloc -- the fused step of dopt_step for callers that cannot
  * allocate device memory.  No page describes this entry point; it exists for
  * the library's users, not for the method.

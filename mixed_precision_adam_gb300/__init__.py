@@ -117,6 +117,13 @@ _c = {
                               _P, _P),
     "dopt_step_noalloc": _proto("dopt_step_noalloc", ctypes.c_int, ctypes.POINTER(dopt_step_args),
                                 ctypes.POINTER(_I32), ctypes.POINTER(_F)),
+    "dopt_workspace_bytes_bucketed": _proto("dopt_workspace_bytes_bucketed", _SZ, _P, _I32),
+    "dopt_step_reduce_buckets": _proto("dopt_step_reduce_buckets", ctypes.c_int,
+                                       ctypes.POINTER(dopt_step_args), _I32, _I32, _I32),
+    "dopt_step_finalize": _proto("dopt_step_finalize", ctypes.c_int, ctypes.POINTER(dopt_step_args),
+                                 _P, _P),
+    "dopt_step_update_buckets": _proto("dopt_step_update_buckets", ctypes.c_int,
+                                       ctypes.POINTER(dopt_step_args), _I32, _I32, _I32),
     "dopt_memory_ledger": _proto("dopt_memory_ledger", _I64, _I64, _I32, _I32,
                                  ctypes.POINTER(_I64)),
     "dopt_comm_bytes": _proto("dopt_comm_bytes", _I64, _I64, _I32, _I32, _I32),
@@ -326,6 +333,9 @@ class StepArgs:
         self._events = (_P * 4)(*[getattr(e, "cuda_event", e) for e in events])
         self.c.stage_events = ctypes.cast(self._events, ctypes.POINTER(_P))
 
+    def set_stream(self, stream):
+        self.c.stream = _stream(stream)
+
     def set_step(self, step, lr=None):
         self.c.hp.step = int(step)
         if lr is not None:
@@ -352,6 +362,25 @@ def dopt_step_noalloc(args):
 
 def dopt_step_async(args, d_found_inf=None, d_norm=None):
     _check(_c["dopt_step_async"](ctypes.byref(args.c), _ptr(d_found_inf), _ptr(d_norm)))
+
+
+def dopt_workspace_bytes_bucketed(m, rank):
+    v = _c["dopt_workspace_bytes_bucketed"](m, rank)
+    if v == 0:
+        raise DoptError(E_INVALID, dopt_last_error())
+    return v
+
+
+def dopt_step_reduce_buckets(args, buffer, bucket_first, bucket_count=1):
+    _check(_c["dopt_step_reduce_buckets"](ctypes.byref(args.c), buffer, bucket_first, bucket_count))
+
+
+def dopt_step_finalize(args, d_found_inf=None, d_norm=None):
+    _check(_c["dopt_step_finalize"](ctypes.byref(args.c), _ptr(d_found_inf), _ptr(d_norm)))
+
+
+def dopt_step_update_buckets(args, buffer, bucket_first, bucket_count=1):
+    _check(_c["dopt_step_update_buckets"](ctypes.byref(args.c), buffer, bucket_first, bucket_count))
 
 
 def dopt_kernel_launches():

@@ -857,14 +857,13 @@ int k1_tile(int32_t gdt, int32_t n_rep, int32_t n_inst, int32_t average) {
   return gdt == DOPT_F32 ? kTile1 : 2 * kTile1;
 }
 
-// Launches K1 over every chunk of (buffer, rank).  stats: write partials to
-// the buffer's regions of the workspace.
-int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* replicas,
-           int32_t n_rep, int32_t n_inst, int32_t full_layout, int32_t average, float inv_scale,
-           int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s) {
-  const std::vector<dopt::Run>& runs = dopt::runs_for(m, buffer, rank);
+// Launches K1 over every chunk of a run list; with stats, chunk i writes its
+// partials to workspace region region_first + i.
+int run_k1_runs(const std::vector<dopt::Run>& runs, int region_first, const void* const* replicas,
+                int32_t n_rep, int32_t n_inst, int32_t full_layout, int32_t average, float inv_scale,
+                int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s) {
   std::vector<Chunk> chunks = chunks_of(runs);
-  int region = stats ? regions_before(m, buffer, rank) : 0;
+  int region = region_first;
   for (const Chunk& c : chunks) {
     K1Params& kp = k1_scratch();
     for (int k = 0; k < n_rep; ++k) kp.rep[k] = replicas[k];
@@ -893,12 +892,27 @@ int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* r
   return DOPT_OK;
 }
 
-int run_k2(dopt_shard_map* m, int32_t rank, void* ws, double remote_sumsq, int32_t remote_found,
-           double max_norm, float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
-  int n_slots = total_regions(m, rank) * kMaxGrid;
+// K1 over every run of (buffer, rank); partials go to the buffer's regions
+// of the fused-step workspace layout.
+int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* replicas,
+           int32_t n_rep, int32_t n_inst, int32_t full_layout, int32_t average, float inv_scale,
+           int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s) {
+  return run_k1_runs(dopt::runs_for(m, buffer, rank), stats ? regions_before(m, buffer, rank) : 0,
+                     replicas, n_rep, n_inst, full_layout, average, inv_scale, gdt, main_grad, stats,
+                     ws, s);
+}
+
+int run_k2_slots(int n_slots, void* ws, double remote_sumsq, int32_t remote_found, double max_norm,
+                 float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
   k2_finalize<<<1, kThreads, 0, s>>>(region_ptr(ws, 0), n_slots, remote_sumsq, remote_found ? 1 : 0,
                                      max_norm, scalars_ptr(ws), d_norm, d_coef, d_found);
   return check_launch("k2_finalize launch");
+}
+
+int run_k2(dopt_shard_map* m, int32_t rank, void* ws, double remote_sumsq, int32_t remote_found,
+           double max_norm, float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
+  return run_k2_slots(total_regions(m, rank) * kMaxGrid, ws, remote_sumsq, remote_found, max_norm,
+                      d_norm, d_coef, d_found, s);
 }
 
 int check_hparams(const dopt_adamw_hparams* hp, const char* fn) {
@@ -931,12 +945,10 @@ int launch_k3_t(K3Params& kp, int n_tiles, cudaStream_t s) {
   return check_launch("k3_adamw launch");
 }
 
-int run_k3(dopt_shard_map* m, int32_t buffer, int32_t rank, const float* main_grad, float* master,
-           float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
-           const float* d_coef, const int32_t* d_found, cudaStream_t s) {
-  const std::vector<dopt::Run>& runs = dopt::runs_for(m, buffer, rank);
+int run_k3_runs(const std::vector<dopt::Run>& runs, int32_t pdt, const float* main_grad, float* master,
+                float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
+                const float* d_coef, const int32_t* d_found, cudaStream_t s) {
   std::vector<Chunk> chunks = chunks_of(runs);
-  const int32_t pdt = m->buffers[buffer].param_dtype;
   for (const Chunk& c : chunks) {
     K3Params& kp = k3_scratch();
     kp.main_grad = main_grad;
@@ -965,6 +977,39 @@ int run_k3(dopt_shard_map* m, int32_t buffer, int32_t rank, const float* main_gr
     if (st) return st;
   }
   return DOPT_OK;
+}
+
+int run_k3(dopt_shard_map* m, int32_t buffer, int32_t rank, const float* main_grad, float* master,
+           float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
+           const float* d_coef, const int32_t* d_found, cudaStream_t s) {
+  return run_k3_runs(dopt::runs_for(m, buffer, rank), m->buffers[buffer].param_dtype, main_grad, master,
+                     exp_avg, exp_avg_sq, param, hp, d_coef, d_found, s);
+}
+
+// ---- bucket-staged step: one partial region per (buffer, bucket, chunk) --
+
+std::vector<std::vector<dopt::Run>> runs_by_bucket(dopt_shard_map* m, int32_t buffer, int32_t rank) {
+  std::vector<std::vector<dopt::Run>> out(m->buffers[buffer].buckets.size());
+  for (const dopt::Run& r : dopt::runs_for(m, buffer, rank)) out[r.bucket].push_back(r);
+  return out;
+}
+
+// Region index of (buffer, bucket)'s first chunk; (nbuffers, 0) gives the total.
+int bucketed_region(dopt_shard_map* m, int32_t rank, int32_t buffer, int32_t bucket) {
+  int n = 0;
+  for (int32_t b = 0; b < (int32_t)m->buffers.size(); ++b) {
+    std::vector<std::vector<dopt::Run>> by = runs_by_bucket(m, b, rank);
+    for (int32_t k = 0; k < (int32_t)by.size(); ++k) {
+      if (b == buffer && k == bucket) return n;
+      n += (int)chunks_of(by[k]).size();
+    }
+  }
+  return n;
+}
+
+size_t bucketed_workspace_bytes(dopt_shard_map* m, int32_t rank) {
+  return kScalarBytes +
+         (size_t)bucketed_region(m, rank, (int32_t)m->buffers.size(), 0) * kMaxGrid * sizeof(Partial);
 }
 
 int check_state_ptrs(const dopt_shard_map* m, int32_t buffer, const float* master,
@@ -996,6 +1041,52 @@ int check_replicas(const dopt_shard_map* m, int32_t rank, const void* const* rep
     if (!aligned16(replicas[k]))
       return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": replica pointer not 16-byte aligned");
   }
+  return DOPT_OK;
+}
+
+// Checks a dopt_step_args for the fused step (bucketed = false) or the
+// bucket-staged step (bucketed = true: the workspace uses that layout).
+int check_step_args(const dopt_step_args* a, bool bucketed, const char* fn) {
+  if (!a) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL args");
+  int st = check_map_buffer_rank(a->map, 0, a->rank, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  const int32_t nb = (int32_t)m->buffers.size();
+  const int32_t n_rep = m->dp * a->n_instances;
+  if (bucketed) {
+    if (!a->workspace) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL workspace");
+    if (!aligned16(a->workspace))
+      return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": workspace not 16-byte aligned");
+    size_t need = bucketed_workspace_bytes(m, a->rank);
+    if (a->workspace_bytes < need)
+      return dopt::fail(DOPT_E_SIZE, std::string(fn) + ": workspace needs " + std::to_string(need) +
+                                         " bytes (dopt_workspace_bytes_bucketed), got " +
+                                         std::to_string(a->workspace_bytes));
+  } else if ((st = check_workspace(m, a->rank, a->workspace, a->workspace_bytes, fn))) {
+    return st;
+  }
+  if ((st = check_hparams(&a->hp, fn))) return st;
+  if (!a->replica_grads || !a->main_grad || !a->master || !a->exp_avg || !a->exp_avg_sq || !a->param_buffer)
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL per-buffer array");
+  if (!std::isfinite(a->inv_loss_scale) || !(a->remote_sumsq >= 0) || std::isnan(a->max_norm))
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": bad inv_loss_scale, remote_sumsq or max_norm");
+  for (int32_t b = 0; b < nb; ++b) {
+    if ((st = check_replicas(m, a->rank, a->replica_grads[b], n_rep, a->n_instances, a->layout, fn))) return st;
+    if ((st = check_state_ptrs(m, b, a->master[b], a->exp_avg[b], a->exp_avg_sq[b], a->param_buffer[b], fn)))
+      return st;
+    if (!a->main_grad[b]) return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL main_grad");
+    if (!aligned16(a->main_grad[b])) return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": main_grad not aligned");
+  }
+  return DOPT_OK;
+}
+
+int check_bucket_range(const dopt_shard_map* m, int32_t buffer, int32_t first, int32_t count,
+                       const char* fn) {
+  if (buffer < 0 || buffer >= (int32_t)m->buffers.size())
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": buffer out of range");
+  const int32_t nbk = (int32_t)m->buffers[buffer].buckets.size();
+  if (first < 0 || count < 1 || first > nbk - count)
+    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": bucket range out of range");
   return DOPT_OK;
 }
 
@@ -1087,26 +1178,11 @@ int dopt_adam_step(const dopt_shard_map* map, int32_t buffer, int32_t rank, cons
 }
 
 int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm) {
-  const char* fn = "dopt_step";
-  if (!a) return dopt::fail(DOPT_E_INVALID, "dopt_step: NULL args");
-  int st = check_map_buffer_rank(a->map, 0, a->rank, fn);
+  int st = check_step_args(a, false, "dopt_step");
   if (st) return st;
   dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
   const int32_t nb = (int32_t)m->buffers.size();
   const int32_t n_rep = m->dp * a->n_instances;
-  if ((st = check_workspace(m, a->rank, a->workspace, a->workspace_bytes, fn))) return st;
-  if ((st = check_hparams(&a->hp, fn))) return st;
-  if (!a->replica_grads || !a->main_grad || !a->master || !a->exp_avg || !a->exp_avg_sq || !a->param_buffer)
-    return dopt::fail(DOPT_E_INVALID, "dopt_step: NULL per-buffer array");
-  if (!std::isfinite(a->inv_loss_scale) || !(a->remote_sumsq >= 0) || std::isnan(a->max_norm))
-    return dopt::fail(DOPT_E_INVALID, "dopt_step: bad inv_loss_scale, remote_sumsq or max_norm");
-  for (int32_t b = 0; b < nb; ++b) {
-    if ((st = check_replicas(m, a->rank, a->replica_grads[b], n_rep, a->n_instances, a->layout, fn))) return st;
-    if ((st = check_state_ptrs(m, b, a->master[b], a->exp_avg[b], a->exp_avg_sq[b], a->param_buffer[b], fn)))
-      return st;
-    if (!a->main_grad[b]) return dopt::fail(DOPT_E_INVALID, "dopt_step: NULL main_grad");
-    if (!aligned16(a->main_grad[b])) return dopt::fail(DOPT_E_ALIGN, "dopt_step: main_grad not aligned");
-  }
   cudaStream_t s = (cudaStream_t)a->stream;
   if ((st = record_stage(a, 0, s))) return st;
   for (int32_t b = 0; b < nb; ++b) {
@@ -1127,6 +1203,60 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
     if (st) return st;
   }
   return record_stage(a, 3, s);
+}
+
+size_t dopt_workspace_bytes_bucketed(const dopt_shard_map* map, int32_t rank) {
+  if (!map || (rank != DOPT_ALL_RANKS && (rank < 0 || rank >= map->dp))) {
+    dopt::fail(DOPT_E_INVALID, "dopt_workspace_bytes_bucketed: bad map or rank");
+    return 0;
+  }
+  return bucketed_workspace_bytes(const_cast<dopt_shard_map*>(map), rank);
+}
+
+int dopt_step_reduce_buckets(const dopt_step_args* a, int32_t buffer, int32_t bucket_first,
+                             int32_t bucket_count) {
+  const char* fn = "dopt_step_reduce_buckets";
+  int st = check_step_args(a, true, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  if ((st = check_bucket_range(m, buffer, bucket_first, bucket_count, fn))) return st;
+  std::vector<std::vector<dopt::Run>> by = runs_by_bucket(m, buffer, a->rank);
+  const int32_t n_rep = m->dp * a->n_instances;
+  for (int32_t k = bucket_first; k < bucket_first + bucket_count; ++k) {
+    st = run_k1_runs(by[k], bucketed_region(m, a->rank, buffer, k), a->replica_grads[buffer], n_rep,
+                     a->n_instances, a->layout == DOPT_LAYOUT_FULL_BUFFER, a->average_in_collective,
+                     a->inv_loss_scale, m->buffers[buffer].grad_dtype, a->main_grad[buffer], true,
+                     a->workspace, (cudaStream_t)a->stream);
+    if (st) return st;
+  }
+  return DOPT_OK;
+}
+
+int dopt_step_finalize(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm) {
+  const char* fn = "dopt_step_finalize";
+  int st = check_step_args(a, true, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  const int n_slots = bucketed_region(m, a->rank, (int32_t)m->buffers.size(), 0) * kMaxGrid;
+  return run_k2_slots(n_slots, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm, d_norm,
+                      nullptr, d_found_inf, (cudaStream_t)a->stream);
+}
+
+int dopt_step_update_buckets(const dopt_step_args* a, int32_t buffer, int32_t bucket_first,
+                             int32_t bucket_count) {
+  const char* fn = "dopt_step_update_buckets";
+  int st = check_step_args(a, true, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  if ((st = check_bucket_range(m, buffer, bucket_first, bucket_count, fn))) return st;
+  std::vector<std::vector<dopt::Run>> by = runs_by_bucket(m, buffer, a->rank);
+  std::vector<dopt::Run> runs;
+  for (int32_t k = bucket_first; k < bucket_first + bucket_count; ++k)
+    runs.insert(runs.end(), by[k].begin(), by[k].end());
+  Scalars* sc = scalars_ptr(a->workspace);
+  return run_k3_runs(runs, m->buffers[buffer].param_dtype, a->main_grad[buffer], a->master[buffer],
+                     a->exp_avg[buffer], a->exp_avg_sq[buffer], a->param_buffer[buffer], &a->hp, &sc->coef,
+                     &sc->found_inf, (cudaStream_t)a->stream);
 }
 
 namespace {

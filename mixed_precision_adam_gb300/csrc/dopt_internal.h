@@ -42,6 +42,7 @@ struct Run {
   int64_t world = 0;
   int64_t len = 0;
   double wd_mult = 1.0;
+  int32_t bucket = 0;  // runs never span two buckets
 };
 
 }  // namespace dopt

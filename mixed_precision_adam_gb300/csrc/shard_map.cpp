@@ -100,18 +100,19 @@ const std::vector<Run>& runs_for(dopt_shard_map* m, int32_t buffer, int32_t rank
   int32_t last = rank == DOPT_ALL_RANKS ? m->dp - 1 : rank;
   for (int32_t r = first; r <= last; ++r) {
     int64_t slot_base = (int64_t)(r - first) * S;
-    for (const Bucket& bk : buf.buckets) {
+    for (int32_t k = 0; k < (int32_t)buf.buckets.size(); ++k) {
+      const Bucket& bk = buf.buckets[k];
       int64_t s = bk.numel / m->dp;
       int64_t w0 = bk.offset + (int64_t)r * s, w1 = w0 + s;
       for (int32_t pid : bk.params) {
         const Param& p = m->params[pid];
         int64_t lo = std::max(p.start, w0), hi = std::min(p.end, w1);
         if (hi <= lo) continue;
-        Run run{slot_base + bk.shard_base + (lo - w0), lo, hi - lo, p.wd_mult};
+        Run run{slot_base + bk.shard_base + (lo - w0), lo, hi - lo, p.wd_mult, k};
         if (!runs.empty()) {
           Run& prev = runs.back();
           if (prev.local + prev.len == run.local && prev.world + prev.len == run.world &&
-              prev.wd_mult == run.wd_mult) {
+              prev.wd_mult == run.wd_mult && prev.bucket == run.bucket) {
             prev.len += run.len;
             continue;
           }
@@ -124,7 +125,7 @@ const std::vector<Run>& runs_for(dopt_shard_map* m, int32_t buffer, int32_t rank
   std::vector<Run> split;
   for (const Run& r : runs) {
     for (int64_t o = 0; o < r.len; o += kMaxRunLen)
-      split.push_back(Run{r.local + o, r.world + o, std::min(kMaxRunLen, r.len - o), r.wd_mult});
+      split.push_back(Run{r.local + o, r.world + o, std::min(kMaxRunLen, r.len - o), r.wd_mult, r.bucket});
   }
   return m->runs_cache.emplace(key, std::move(split)).first->second;
 }
