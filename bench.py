@@ -296,7 +296,8 @@ class OracleSample:
     def step(self):
         c, L = self.ctypes, self.L
         bad = L.or_reduce_prepare_run(self.arr, self.n_rep, self.cfg["n_inst"], 0, 0, 0,
-                                      self.elements, c.c_float(1.0), self.main.ctypes.data)
+                                      self.elements, c.c_float(1.0), c.c_float(1.0),
+                                      self.main.ctypes.data)
         sumsq = L.or_sumsq_run(self.main.ctypes.data, self.elements)
         norm, coef = c.c_double(), c.c_double()
         clip = L.or_clip_coef(sumsq, self.cfg["max_norm"], c.byref(norm), c.byref(coef))
@@ -451,7 +452,7 @@ def run_ours(args):
         barrier(world)
         e2e_value, _ = aggregate(max(e0.elapsed_time(e1), wall), wl.elements, n_e2e, world)
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": 24, "steps": n_e2e,
+               "d2h_bytes_per_step": 32, "steps": n_e2e,
                "note": "replica grads copied from pinned host memory each step"}
         del host_reps
 

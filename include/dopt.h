@@ -278,7 +278,31 @@ typedef struct {
    * the norm finalize and after the AdamW pass, so a caller can time each
    * stage of the step with cudaEventElapsedTime. */
   void* const* stage_events;
+  /* scale_gradients factor (per-token loss normalization, 1/num_tokens):
+   * multiplies the reduced grads in the grad dtype (one rounding) before
+   * prepare_grads; Megatron distributed-package page section 4.6.  0 or 1
+   * means no scaling. */
+  float grad_scale;
+  int32_t reserved;
 } dopt_step_args;
+
+/* Statistics of the last step, kept at the start of its workspace:
+ * the fp64 sum of squares (with the remote term), the reported norm (NaN
+ * when skipped), the clip coefficient applied (1 when not clipping),
+ * found_inf, whether the grads were clipped, and the number of main grads
+ * equal to zero (MegatronOptimizer's count_zeros). */
+typedef struct {
+  double sumsq;
+  float grad_norm;
+  float clip_coef;
+  int32_t found_inf;
+  int32_t clipped;
+  int64_t num_zeros;
+} dopt_step_stats;
+
+/* Copies the statistics of the last step run with `workspace` (fused or
+ * bucket-staged layout) to the host; waits for `stream`. */
+int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_stream stream);
 
 /*
  * One fused optimizer step (steps A2..A6): for every buffer, reduce the

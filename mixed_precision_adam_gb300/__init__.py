@@ -71,7 +71,12 @@ class dopt_step_args(ctypes.Structure):
                 ("inv_loss_scale", _F), ("remote_found_inf", _I32),
                 ("max_norm", _D), ("remote_sumsq", _D), ("hp", dopt_adamw_hparams),
                 ("workspace", _P), ("workspace_bytes", _SZ), ("stream", _P),
-                ("stage_events", ctypes.POINTER(_P))]
+                ("stage_events", ctypes.POINTER(_P)), ("grad_scale", _F), ("reserved", _I32)]
+
+
+class dopt_step_stats(ctypes.Structure):
+    _fields_ = [("sumsq", _D), ("grad_norm", _F), ("clip_coef", _F), ("found_inf", _I32),
+                ("clipped", _I32), ("num_zeros", _I64)]
 
 
 class dopt_loss_scaler(ctypes.Structure):
@@ -132,6 +137,8 @@ _c = {
     "dopt_loss_scaler_update": _proto("dopt_loss_scaler_update", ctypes.c_int,
                                       ctypes.POINTER(dopt_loss_scaler), _I32),
     "dopt_kernel_launches": _proto("dopt_kernel_launches", ctypes.c_uint64),
+    "dopt_read_step_stats": _proto("dopt_read_step_stats", ctypes.c_int, _P,
+                                   ctypes.POINTER(dopt_step_stats), _P),
     "dopt_last_error": _proto("dopt_last_error", ctypes.c_char_p),
 }
 
@@ -292,7 +299,8 @@ class StepArgs:
     def __init__(self, m, rank, replica_grads, main_grad, master, exp_avg, exp_avg_sq,
                  param_buffer, hp, step, workspace, workspace_bytes, *, n_instances=1,
                  layout=LAYOUT_FULL_BUFFER, average_in_collective=False, inv_loss_scale=1.0,
-                 max_norm=1.0, remote_sumsq=0.0, remote_found_inf=False, stream=None):
+                 max_norm=1.0, remote_sumsq=0.0, remote_found_inf=False, stream=None,
+                 grad_scale=1.0):
         self.map = m
         self._reps = [_ptr_array(r) for r in replica_grads]
         self._rep_arr = (ctypes.POINTER(_P) * len(self._reps))(
@@ -323,6 +331,7 @@ class StepArgs:
         c.workspace = _ptr(workspace)
         c.workspace_bytes = workspace_bytes
         c.stream = _stream(stream)
+        c.grad_scale = grad_scale
 
     def set_stage_events(self, events):
         """events: None, or 4 CUDA events (objects with cuda_event, or ints)."""
@@ -381,6 +390,13 @@ def dopt_step_finalize(args, d_found_inf=None, d_norm=None):
 
 def dopt_step_update_buckets(args, buffer, bucket_first, bucket_count=1):
     _check(_c["dopt_step_update_buckets"](ctypes.byref(args.c), buffer, bucket_first, bucket_count))
+
+
+def dopt_read_step_stats(workspace, stream=None):
+    """The last step's statistics (waits for the stream) as a dict."""
+    st = dopt_step_stats()
+    _check(_c["dopt_read_step_stats"](_ptr(workspace), ctypes.byref(st), _stream(stream)))
+    return _struct_dict(st)
 
 
 def dopt_kernel_launches():

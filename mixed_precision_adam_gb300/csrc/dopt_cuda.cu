@@ -83,18 +83,14 @@ struct SegTable {
 struct Partial {
   double sumsq;
   int32_t nonfinite;
-  int32_t pad;
+  int32_t zeros;  // main grads equal to zero
 };
 static_assert(sizeof(Partial) == 16, "Partial layout");
 
-// Device scalars of one step, at the start of the workspace.
-struct Scalars {
-  double sumsq;
-  float norm;
-  float coef;
-  int32_t found_inf;
-  int32_t clip;
-};
+// Device scalars of one step, at the start of the workspace: the public
+// dopt_step_stats layout.
+using Scalars = dopt_step_stats;
+static_assert(sizeof(Scalars) == 32, "dopt_step_stats layout");
 
 struct K1Params {
   const void* rep[DOPT_MAX_REPLICAS];
@@ -106,7 +102,7 @@ struct K1Params {
   float inv_ninst;  // (float)(1 / n_inst)
   float inv_scale;  // 1 / loss scale
   int32_t average;
-  int32_t pad;
+  float post_scale; // scale_gradients factor on the reduced grad (1 = none)
   SegTable tab;
 };
 
@@ -241,6 +237,13 @@ __device__ __forceinline__ void reduce_term(ReduceState& st, float x, ReplicaPos
   }
 }
 
+// The reduced grad in the grad dtype, times the scale_gradients factor
+// (rounded to the grad dtype again; skipped for a factor of 1).
+template <typename GT>
+__device__ __forceinline__ float post_scaled(float red, float post_scale) {
+  return post_scale == 1.0f ? red : GradT<GT>::round_to(__fmul_rn(red, post_scale));
+}
+
 template <typename GT>
 __device__ __forceinline__ float reduce_finish(const ReduceState& st, const K1Params& p) {
   float total = st.total;
@@ -248,7 +251,7 @@ __device__ __forceinline__ float reduce_finish(const ReduceState& st, const K1Pa
     if (p.average) total = __fmul_rn(total, p.inv_ninst);
     total = GradT<GT>::round_to(total);
   }
-  return __fmul_rn(total, p.inv_scale);
+  return __fmul_rn(post_scaled<GT>(total, p.post_scale), p.inv_scale);
 }
 
 // Sum of squares of a thread's main grads, accurate to about fp64 while
@@ -273,6 +276,7 @@ __device__ __noinline__ double sumsq_flush(double d, float s, float c) {
 struct SumSq {
   float s = 0.f, c = 0.f;
   double d = 0.0;
+  int zeros = 0;  // main grads equal to zero (count_zeros)
   __device__ __forceinline__ void dot2(float x) {
     float p = __fmul_rn(x, x);
     float pe = fmaf(x, x, -p);
@@ -283,6 +287,7 @@ struct SumSq {
     c = __fadd_rn(c, __fadd_rn(e, pe));
   }
   __device__ __forceinline__ void add4(const float* x) {
+    zeros += (x[0] == 0.f) + (x[1] == 0.f) + (x[2] == 0.f) + (x[3] == 0.f);
     float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
     if (mx >= 0x1p62f) {
       d = sumsq_wide(d, x[0], x[1], x[2], x[3]);
@@ -292,6 +297,7 @@ struct SumSq {
     }
   }
   __device__ __forceinline__ void add1(float x) {
+    zeros += (x == 0.f);
     if (fabsf(x) >= 0x1p62f) d = sumsq_wide(d, x, 0.f, 0.f, 0.f);
     else dot2(x);
   }
@@ -316,13 +322,24 @@ __device__ __forceinline__ double warp_sum(double v) {
 // can always sum whole regions.
 __device__ __forceinline__ void write_partial(const SumSq& acc, Partial* partials) {
   __shared__ double s_sum[kThreads / 32];
+  __shared__ int s_zero[kThreads / 32];
   double v = warp_sum(acc.value());
-  if (threadIdx.x % 32 == 0) s_sum[threadIdx.x / 32] = v;
+  int z = acc.zeros;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+  if (threadIdx.x % 32 == 0) {
+    s_sum[threadIdx.x / 32] = v;
+    s_zero[threadIdx.x / 32] = z;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     double tot = 0.0;
-    for (int i = 0; i < kThreads / 32; ++i) tot += s_sum[i];
-    partials[blockIdx.x] = Partial{tot, isfinite(tot) ? 0 : 1, 0};
+    int zt = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+      tot += s_sum[i];
+      zt += s_zero[i];
+    }
+    partials[blockIdx.x] = Partial{tot, isfinite(tot) ? 0 : 1, zt};
     for (int i = gridDim.x + blockIdx.x; i < kMaxGrid; i += gridDim.x)
       partials[i] = Partial{0.0, 0, 0};
   }
@@ -466,7 +483,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
 #pragma unroll
         for (int q = 0; q < kVec; ++q) {
           float tt = NINST > 1 ? GradT<GT>::round_to(total[u][q]) : total[u][q];
-          m[q] = __fmul_rn(tt, inv_scale);
+          m[q] = __fmul_rn(post_scaled<GT>(tt, p.post_scale), inv_scale);
         }
         __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
         if (STATS) acc.add4(m);
@@ -482,7 +499,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
             tt = (j == 0) ? sum : __fadd_rn(tt, sum);
           }
           if (NINST > 1) tt = GradT<GT>::round_to(tt);
-          float m = __fmul_rn(tt, inv_scale);
+          float m = __fmul_rn(post_scaled<GT>(tt, p.post_scale), inv_scale);
           p.main_grad[l0 + e + q] = m;
           if (STATS) acc.add1(m);
         }
@@ -501,19 +518,24 @@ k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
             float* d_norm, float* d_coef, int32_t* d_found) {
   __shared__ double s_sum[kThreads];
   __shared__ int s_bad[kThreads];
+  __shared__ long long s_zero[kThreads];
   double v = 0.0;
   int b = 0;
+  long long z = 0;
   for (int i = threadIdx.x; i < n_slots; i += kThreads) {
     v += parts[i].sumsq;
     b |= parts[i].nonfinite;
+    z += parts[i].zeros;
   }
   s_sum[threadIdx.x] = v;
   s_bad[threadIdx.x] = b;
+  s_zero[threadIdx.x] = z;
   __syncthreads();
   for (int w = kThreads / 2; w > 0; w >>= 1) {
     if (threadIdx.x < w) {
       s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
       s_bad[threadIdx.x] |= s_bad[threadIdx.x + w];
+      s_zero[threadIdx.x] += s_zero[threadIdx.x + w];
     }
     __syncthreads();
   }
@@ -530,10 +552,11 @@ k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
     const float coef_f = clip ? (float)coef : 1.0f;
     const float norm_f = found ? __int_as_float(0x7FC00000) : (float)norm;
     sc->sumsq = sumsq;
-    sc->norm = norm_f;
-    sc->coef = coef_f;
+    sc->grad_norm = norm_f;
+    sc->clip_coef = coef_f;
     sc->found_inf = found;
-    sc->clip = clip;
+    sc->clipped = clip;
+    sc->num_zeros = s_zero[0];
     if (d_norm) *d_norm = norm_f;
     if (d_coef) *d_coef = coef_f;
     if (d_found) *d_found = found;
@@ -861,7 +884,8 @@ int k1_tile(int32_t gdt, int32_t n_rep, int32_t n_inst, int32_t average) {
 // partials to workspace region region_first + i.
 int run_k1_runs(const std::vector<dopt::Run>& runs, int region_first, const void* const* replicas,
                 int32_t n_rep, int32_t n_inst, int32_t full_layout, int32_t average, float inv_scale,
-                int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s) {
+                int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s,
+                float post_scale = 1.0f) {
   std::vector<Chunk> chunks = chunks_of(runs);
   int region = region_first;
   for (const Chunk& c : chunks) {
@@ -877,7 +901,7 @@ int run_k1_runs(const std::vector<dopt::Run>& runs, int region_first, const void
     kp.inv_ninst = (float)(1.0 / (double)n_inst);
     kp.inv_scale = inv_scale;
     kp.average = average ? 1 : 0;
-    kp.pad = 0;
+    kp.post_scale = post_scale;
     fill_table(kp.tab, runs, c, k1_tile(gdt, n_rep, n_inst, average), 0.0, 0.0);
     const int n_tiles = kp.tab.n_tiles;
     int st;
@@ -896,11 +920,15 @@ int run_k1_runs(const std::vector<dopt::Run>& runs, int region_first, const void
 // of the fused-step workspace layout.
 int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* replicas,
            int32_t n_rep, int32_t n_inst, int32_t full_layout, int32_t average, float inv_scale,
-           int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s) {
+           int32_t gdt, float* main_grad, bool stats, void* ws, cudaStream_t s,
+           float post_scale = 1.0f) {
   return run_k1_runs(dopt::runs_for(m, buffer, rank), stats ? regions_before(m, buffer, rank) : 0,
                      replicas, n_rep, n_inst, full_layout, average, inv_scale, gdt, main_grad, stats,
-                     ws, s);
+                     ws, s, post_scale);
 }
+
+// scale_gradients factor of a step: 0 (unset) means 1.
+float grad_scale_of(const dopt_step_args* a) { return a->grad_scale == 0.0f ? 1.0f : a->grad_scale; }
 
 int run_k2_slots(int n_slots, void* ws, double remote_sumsq, int32_t remote_found, double max_norm,
                  float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
@@ -1068,8 +1096,10 @@ int check_step_args(const dopt_step_args* a, bool bucketed, const char* fn) {
   if ((st = check_hparams(&a->hp, fn))) return st;
   if (!a->replica_grads || !a->main_grad || !a->master || !a->exp_avg || !a->exp_avg_sq || !a->param_buffer)
     return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL per-buffer array");
-  if (!std::isfinite(a->inv_loss_scale) || !(a->remote_sumsq >= 0) || std::isnan(a->max_norm))
-    return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": bad inv_loss_scale, remote_sumsq or max_norm");
+  if (!std::isfinite(a->inv_loss_scale) || !(a->remote_sumsq >= 0) || std::isnan(a->max_norm) ||
+      !std::isfinite(a->grad_scale))
+    return dopt::fail(DOPT_E_INVALID,
+                      std::string(fn) + ": bad inv_loss_scale, grad_scale, remote_sumsq or max_norm");
   for (int32_t b = 0; b < nb; ++b) {
     if ((st = check_replicas(m, a->rank, a->replica_grads[b], n_rep, a->n_instances, a->layout, fn))) return st;
     if ((st = check_state_ptrs(m, b, a->master[b], a->exp_avg[b], a->exp_avg_sq[b], a->param_buffer[b], fn)))
@@ -1102,6 +1132,16 @@ int record_stage(const dopt_step_args* a, int i, cudaStream_t s) {
 extern "C" {
 
 uint64_t dopt_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_stream stream) {
+  if (!workspace || !out) return dopt::fail(DOPT_E_INVALID, "dopt_read_step_stats: NULL workspace or out");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(out, workspace, sizeof(dopt_step_stats), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess)
+    return dopt::fail(DOPT_E_CUDA, std::string("dopt_read_step_stats: ") + cudaGetErrorString(e));
+  return DOPT_OK;
+}
 
 size_t dopt_workspace_bytes(const dopt_shard_map* map, int32_t rank) {
   if (!map || (rank != DOPT_ALL_RANKS && (rank < 0 || rank >= map->dp))) {
@@ -1188,7 +1228,7 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
   for (int32_t b = 0; b < nb; ++b) {
     st = run_k1(m, b, a->rank, a->replica_grads[b], n_rep, a->n_instances,
                 a->layout == DOPT_LAYOUT_FULL_BUFFER, a->average_in_collective, a->inv_loss_scale,
-                m->buffers[b].grad_dtype, a->main_grad[b], true, a->workspace, s);
+                m->buffers[b].grad_dtype, a->main_grad[b], true, a->workspace, s, grad_scale_of(a));
     if (st) return st;
   }
   if ((st = record_stage(a, 1, s))) return st;
@@ -1199,7 +1239,7 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
   if ((st = record_stage(a, 2, s))) return st;
   for (int32_t b = 0; b < nb; ++b) {
     st = run_k3(m, b, a->rank, a->main_grad[b], a->master[b], a->exp_avg[b], a->exp_avg_sq[b],
-                a->param_buffer[b], &a->hp, &sc->coef, &sc->found_inf, s);
+                a->param_buffer[b], &a->hp, &sc->clip_coef, &sc->found_inf, s);
     if (st) return st;
   }
   return record_stage(a, 3, s);
@@ -1226,7 +1266,7 @@ int dopt_step_reduce_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
     st = run_k1_runs(by[k], bucketed_region(m, a->rank, buffer, k), a->replica_grads[buffer], n_rep,
                      a->n_instances, a->layout == DOPT_LAYOUT_FULL_BUFFER, a->average_in_collective,
                      a->inv_loss_scale, m->buffers[buffer].grad_dtype, a->main_grad[buffer], true,
-                     a->workspace, (cudaStream_t)a->stream);
+                     a->workspace, (cudaStream_t)a->stream, grad_scale_of(a));
     if (st) return st;
   }
   return DOPT_OK;
@@ -1255,7 +1295,7 @@ int dopt_step_update_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
     runs.insert(runs.end(), by[k].begin(), by[k].end());
   Scalars* sc = scalars_ptr(a->workspace);
   return run_k3_runs(runs, m->buffers[buffer].param_dtype, a->main_grad[buffer], a->master[buffer],
-                     a->exp_avg[buffer], a->exp_avg_sq[buffer], a->param_buffer[buffer], &a->hp, &sc->coef,
+                     a->exp_avg[buffer], a->exp_avg_sq[buffer], a->param_buffer[buffer], &a->hp, &sc->clip_coef,
                      &sc->found_inf, (cudaStream_t)a->stream);
 }
 
@@ -1310,7 +1350,7 @@ int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
   if (found_inf_out) *found_inf_out = host.found_inf;
-  if (grad_norm_out) *grad_norm_out = host.norm;
+  if (grad_norm_out) *grad_norm_out = host.grad_norm;
   return DOPT_OK;
 }
 

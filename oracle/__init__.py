@@ -41,7 +41,7 @@ def lib():
         L = ctypes.CDLL(path)
         P, I32, I64, F, D = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                              ctypes.c_float, ctypes.c_double)
-        L.or_reduce_prepare_run.argtypes = [ctypes.POINTER(P), I32, I32, I32, I32, I64, I64, F, P]
+        L.or_reduce_prepare_run.argtypes = [ctypes.POINTER(P), I32, I32, I32, I32, I64, I64, F, F, P]
         L.or_reduce_prepare_run.restype = I64
         L.or_sumsq_run.argtypes = [P, I64]
         L.or_sumsq_run.restype = D
@@ -50,7 +50,7 @@ def lib():
         L.or_adamw_run.argtypes = [P, I64, D, I32, P, P, P, ctypes.POINTER(Hparams), D, I64, P, I32]
         L.or_adamw_run.restype = None
         L.or_stream_sumsq.argtypes = [ctypes.POINTER(ctypes.c_uint64), I32, I32, I32, I32, F,
-                                      ctypes.c_uint64, I64, F, ctypes.POINTER(I64)]
+                                      ctypes.c_uint64, I64, F, F, ctypes.POINTER(I64)]
         L.or_stream_sumsq.restype = D
         L.or_round_bf16.argtypes = [F]
         L.or_round_bf16.restype = ctypes.c_uint16
@@ -90,14 +90,16 @@ def round_f16(x):
     return np.array([L.or_round_f16(float(v)) for v in x], dtype=np.uint16)
 
 
-def reduce_prepare(replicas, gdt, index0, length, inv_scale, n_inst=1, average=False):
-    """A2 + A3 on a run: returns (main grads fp32, count of non-finite)."""
+def reduce_prepare(replicas, gdt, index0, length, inv_scale, n_inst=1, average=False,
+                   grad_scale=1.0):
+    """A2 (+ A2' scale_gradients) + A3 on a run: returns (main grads fp32,
+    count of non-finite)."""
     L = lib()
     n = len(replicas)
     arr = (ctypes.c_void_p * n)(*[r.ctypes.data for r in replicas])
     out = np.empty(length, dtype=np.float32)
     bad = L.or_reduce_prepare_run(arr, n, n_inst, gdt, int(average), index0, length,
-                                  inv_scale, _ptr(out))
+                                  grad_scale, inv_scale, _ptr(out))
     if bad < 0:
         raise ValueError("invalid replica / instance counts")
     return out, bad
@@ -105,7 +107,7 @@ def reduce_prepare(replicas, gdt, index0, length, inv_scale, n_inst=1, average=F
 
 def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.0,
          layout="full", n_inst=1, average=False, remote_sumsq=0.0,
-         remote_found_inf=False):
+         remote_found_inf=False, grad_scale=1.0):
     """One optimizer step over the shards of `ranks` in every buffer of `smap`.
 
     grads[bi]  : list of n_rep replica arrays for buffer bi, in its grad dtype
@@ -119,14 +121,17 @@ def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.
                  buffer it is also the master (updated in place).
     hp         : dict lr, beta1, beta2, eps, weight_decay.
     t          : the step number used for bias correction if not skipped.
+    grad_scale : scale_gradients factor applied to the reduced grads (1 = none).
     Arrays in state and params are updated in place.  Returns a dict with
-    found_inf, norm (NaN when skipped), coef, clip and main (per buffer).
+    found_inf, norm (NaN when skipped), coef, clip, main (per buffer),
+    sumsq and num_zeros (main grads equal to zero, Megatron's count_zeros).
     """
     L = lib()
     n_rep = len(grads[0]) if grads else 0
     mains = []
     sumsq = 0.0
     bad = 0
+    zeros = 0
     pieces = []
     for bi, buf in enumerate(smap.buffers):
         S = smap.shard_numel(bi)
@@ -139,16 +144,18 @@ def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.
                 local = slot * S + v["shard_offset"]
                 rep0 = v["gbuf_world"].start if layout == "full" else v["shard_offset"]
                 k = L.or_reduce_prepare_run(arr, n_rep, n_inst, buf.grad_dtype, int(average),
-                                            rep0, n, ctypes.c_float(inv_scale), _ptr(main, local))
+                                            rep0, n, ctypes.c_float(grad_scale),
+                                            ctypes.c_float(inv_scale), _ptr(main, local))
                 if k < 0:
                     raise ValueError("invalid replica / instance counts")
                 bad += k
                 sumsq += L.or_sumsq_run(_ptr(main, local), n)
+                zeros += int(np.count_nonzero(main[local:local + n] == 0))
                 pieces.append((bi, pid, local, v))
         mains.append(main)
     sumsq += remote_sumsq
     found = bad > 0 or bool(remote_found_inf)
-    result = {"found_inf": found, "main": mains, "sumsq": sumsq}
+    result = {"found_inf": found, "main": mains, "sumsq": sumsq, "num_zeros": zeros}
     if found:
         result.update(norm=float("nan"), coef=1.0, clip=False)
         return result
@@ -175,7 +182,8 @@ def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.
     return result
 
 
-def stream_sumsq(keys, gdt, factor, index0, length, inv_scale=1.0, n_inst=1, average=False):
+def stream_sumsq(keys, gdt, factor, index0, length, inv_scale=1.0, n_inst=1, average=False,
+                 grad_scale=1.0):
     """A2 + A3 + the fp64 sum of squares over a run whose replica gradients
     are drawn from the seeded generator (keys: one generator key per replica).
     Returns (sumsq, count of non-finite main grads)."""
@@ -184,7 +192,8 @@ def stream_sumsq(keys, gdt, factor, index0, length, inv_scale=1.0, n_inst=1, ave
     karr = (ctypes.c_uint64 * n)(*keys)
     bad = ctypes.c_int64()
     s = L.or_stream_sumsq(karr, n, n_inst, gdt, int(average), ctypes.c_float(factor),
-                          index0, length, ctypes.c_float(inv_scale), ctypes.byref(bad))
+                          index0, length, ctypes.c_float(grad_scale), ctypes.c_float(inv_scale),
+                          ctypes.byref(bad))
     if bad.value < 0:
         raise ValueError("invalid replica / instance counts")
     return s, bad.value

@@ -17,6 +17,11 @@
  *      page (llm-infra-atlas 02_zero_and_distributed_optimizer), section 5
  *      (distributed-optimizer instances: reduce-scatter inside an instance,
  *      all-reduce between instances).
+ *   A2' scale_gradients: the Megatron distributed-package page, section 4.6
+ *      (per-token loss normalization: after the data-parallel grad sync, the
+ *      reduced grads are multiplied by 1/num_tokens in the grad buffer; read
+ *      as one multiply rounded to the grad dtype).  A factor of 1 is the
+ *      identity and skips the step.
  *   A3 prepare_grads: distrib_optimizer page, "MixedPrecisionOptimizer" layer
  *      (copy to fp32 main grad, unscale, inf/NaN detection) and the grad copy
  *      listing (bf16 -> fp32 .float()).
@@ -171,22 +176,30 @@ static float or_reduce_element(const float* g, int32_t n_rep, int32_t n_inst,
   return total;
 }
 
+/* A2': the reduced grad (in the grad dtype) times the scale_gradients
+ * factor, rounded to the grad dtype; factor 1 leaves it unchanged. */
+static float or_scale_gradients(float red, float factor, int32_t gdt) {
+  if (factor == 1.0f) return red;
+  return or_round_to(red * factor, gdt);
+}
+
 /*
- * A2 + A3 over a run of len elements.  rep[k] is replica k's array in the
- * grad dtype gdt; element j of the run sits at index rep_index0 + j in every
- * replica.  main_out[j] = fp32(reduced) * inv_scale.  Returns the number of
- * non-finite main-grad values written.
+ * A2 + A2' + A3 over a run of len elements.  rep[k] is replica k's array in
+ * the grad dtype gdt; element j of the run sits at index rep_index0 + j in
+ * every replica.  main_out[j] = fp32(scaled reduced grad) * inv_scale.
+ * Returns the number of non-finite main-grad values written.
  */
 int64_t or_reduce_prepare_run(const void* const* rep, int32_t n_rep, int32_t n_inst,
                               int32_t gdt, int32_t average, int64_t rep_index0,
-                              int64_t len, float inv_scale, float* main_out) {
+                              int64_t len, float grad_scale, float inv_scale, float* main_out) {
   float g[256];
   int64_t bad = 0;
   if (n_rep <= 0 || n_rep > 256 || n_inst <= 0 || n_rep % n_inst) return -1;
   for (int64_t j = 0; j < len; ++j) {
     for (int32_t k = 0; k < n_rep; ++k) g[k] = or_widen(rep[k], gdt, rep_index0 + j);
     {
-      float red = or_reduce_element(g, n_rep, n_inst, gdt, average);
+      float red = or_scale_gradients(or_reduce_element(g, n_rep, n_inst, gdt, average),
+                                     grad_scale, gdt);
       float mg = red * inv_scale;
       main_out[j] = mg;
       if (!or_is_finite(mg)) ++bad;
@@ -282,7 +295,8 @@ void or_adamw_run(const float* main_grad, int64_t len, double coef, int32_t clip
  * count of non-finite main grads. */
 double or_stream_sumsq(const uint64_t* keys, int32_t n_rep, int32_t n_inst,
                        int32_t gdt, int32_t average, float factor,
-                       uint64_t index0, int64_t len, float inv_scale, int64_t* n_bad) {
+                       uint64_t index0, int64_t len, float grad_scale, float inv_scale,
+                       int64_t* n_bad) {
   float g[256];
   double s = 0.0;
   int64_t bad = 0;
@@ -295,7 +309,8 @@ double or_stream_sumsq(const uint64_t* keys, int32_t n_rep, int32_t n_inst,
       else g[k] = x;
     }
     {
-      float mg = or_reduce_element(g, n_rep, n_inst, gdt, average) * inv_scale;
+      float mg = or_scale_gradients(or_reduce_element(g, n_rep, n_inst, gdt, average),
+                                    grad_scale, gdt) * inv_scale;
       if (!or_is_finite(mg)) ++bad;
       s += (double)mg * (double)mg;
     }

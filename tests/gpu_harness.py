@@ -132,7 +132,8 @@ class HostCase:
                            inv_scale=float(np.float32(1.0 / cfg["loss_scale"])),
                            max_norm=cfg["max_norm"], layout=cfg["layout"], n_inst=cfg["n_inst"],
                            average=cfg["average"], remote_sumsq=cfg.get("remote_sumsq", 0.0),
-                           remote_found_inf=cfg.get("remote_found_inf", False))
+                           remote_found_inf=cfg.get("remote_found_inf", False),
+                           grad_scale=float(np.float32(cfg.get("grad_scale", 1.0))))
 
 
 class DeviceCase:
@@ -168,7 +169,8 @@ class DeviceCase:
                           inv_loss_scale=float(np.float32(1.0 / cfg["loss_scale"])),
                           max_norm=cfg["max_norm"], remote_sumsq=cfg.get("remote_sumsq", 0.0),
                           remote_found_inf=cfg.get("remote_found_inf", False),
-                          stream=stream if stream is not None else self.torch.cuda.current_stream())
+                          stream=stream if stream is not None else self.torch.cuda.current_stream(),
+                          grad_scale=float(np.float32(cfg.get("grad_scale", 1.0))))
 
     def step(self, grads, t):
         reps = [[self._up(r) for r in g] for g in grads]
@@ -245,6 +247,10 @@ def compare_step(hc, dc, ores, found, norm, before, report):
         if not rel <= 1e-5:
             report.append(f"grad_norm device={norm} oracle={ores['norm']} rel={rel:.3g}")
             ok = False
+    stats = dopt().dopt_read_step_stats(dc.ws)
+    if stats["num_zeros"] != ores["num_zeros"]:
+        report.append(f"num_zeros device={stats['num_zeros']} oracle={ores['num_zeros']}")
+        ok = False
     params, master, exp_avg, exp_avg_sq, mains = dc.download()
     for bi, buf in enumerate(hc.om.buffers):
         mask = hc.piece_mask(bi)

@@ -205,6 +205,24 @@ def test_reduce_rounds_once_to_grad_dtype():
         assert (out == want).all()
 
 
+def test_scale_gradients_rounds_once_in_grad_dtype():
+    """scale_gradients multiplies the reduced grad in its own dtype: the same
+    as torch's in-dtype multiply of the reduced tensor."""
+    rng = np.random.RandomState(4)
+    reps32 = [(rng.standard_normal(777) * 1e-2).astype(np.float32) for _ in range(4)]
+    f = float(np.float32(1.0 / 3.0))
+    for gdt, tdt in ((F32, torch.float32), (BF16, torch.bfloat16), (F16, torch.float16)):
+        reps = [torch.from_numpy(r).to(tdt) for r in reps32]
+        arrs = [r.numpy() if tdt == torch.float32 else r.view(torch.int16).numpy().view(np.uint16)
+                for r in reps]
+        plain, _ = oracle.reduce_prepare(arrs, gdt, 0, 777, 1.0)
+        scaled, _ = oracle.reduce_prepare(arrs, gdt, 0, 777, 0.5, grad_scale=f)
+        want = (torch.from_numpy(plain).to(tdt) * f).float() * 0.5
+        assert (scaled == want.numpy()).all()
+        same, _ = oracle.reduce_prepare(arrs, gdt, 0, 777, 1.0, grad_scale=1.0)
+        assert (same == plain).all()
+
+
 def test_prepare_unscale_and_inf_detection():
     reps = [np.full(64, 65536.0 * 3, np.float32) for _ in range(4)]
     out, bad = oracle.reduce_prepare(reps, F32, 0, 64, 1.0 / 65536)

@@ -143,3 +143,25 @@ def test_repeat_is_deterministic():
         norms = [dc.step(hc.grads(t), t)[1] for t in (1, 2)]
         outs.append((norms, [a.tobytes() for a in dc.download()[1] if a is not None]))
     assert outs[0] == outs[1]
+
+
+@pytest.mark.parametrize("grad_fp32", [True, False])
+def test_scale_gradients_and_zero_count(grad_fp32):
+    """scale_gradients(1/num_tokens) with a factor that rounds (1/3), and
+    main grads that are exactly zero (zero in every replica) for count_zeros."""
+    cfg = _tiny(RAGGED, 4, bucket_size=5000, grad_reduce_in_fp32=grad_fp32, grad_scale=1.0 / 3.0,
+                grad_sigma=1e-2, steps=2)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    report = []
+    for t in (1, 2):
+        grads = hc.grads(t)
+        for bi, reps in enumerate(grads):
+            for r in reps:
+                r[3::97] = 0  # the same positions in every replica
+        before = H.snapshot(hc)
+        ores = hc.oracle_step(grads, t)
+        assert ores["num_zeros"] > 0
+        found, norm = dc.step(grads, t)
+        assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
+        hc.t_applied += 1
