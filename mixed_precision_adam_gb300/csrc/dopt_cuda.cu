@@ -42,13 +42,16 @@ namespace {
 #define DOPT_K1_UNROLL 2
 #endif
 #ifndef DOPT_K3_UNROLL
-#define DOPT_K3_UNROLL 4
+#define DOPT_K3_UNROLL 1
+#endif
+#ifndef DOPT_K3_PIPE
+#define DOPT_K3_PIPE 1  // 1: the AdamW pass loads the next tile before computing this one
 #endif
 #ifndef DOPT_K1_MIN_BLOCKS
 #define DOPT_K1_MIN_BLOCKS 2
 #endif
 #ifndef DOPT_K3_MIN_BLOCKS
-#define DOPT_K3_MIN_BLOCKS 2
+#define DOPT_K3_MIN_BLOCKS 4
 #endif
 
 constexpr int kThreads = 256;              // threads per CTA
@@ -673,6 +676,84 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw(const _
   }
 }
 
+// The AdamW pass with the loads of a thread's next tile issued before the
+// current tile is computed and stored, so the memory pipe stays busy while
+// the thread does arithmetic (software pipelining across tiles).
+struct K3Tile {
+  float4 g[kUnroll3], w[kUnroll3], m[kUnroll3], v[kUnroll3];
+  int64_t l0, w0, m0;
+  int n;
+  float decay;
+  bool aligned;
+};
+
+template <typename PT>
+__device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, int& si, K3Tile& T) {
+  si = seek(p.tab, si, t);
+  const Seg& sg = p.tab.seg[si];
+  const int64_t off = (int64_t)(t - sg.tile0) * kTile3;
+  T.n = (int)min((int64_t)kTile3, (int64_t)sg.len - off);
+  T.l0 = sg.local + off;
+  T.w0 = sg.world + off;
+  T.m0 = ParamT<PT>::kInPlace ? T.w0 : T.l0;
+  T.aligned = (sg.flags & kSegAligned) != 0;
+  T.decay = sg.decay;
+#pragma unroll
+  for (int u = 0; u < kUnroll3; ++u) {
+    const int e = (u * kThreads + threadIdx.x) * kVec;
+    if (T.aligned && e + kVec <= T.n) {
+      T.g[u] = __ldcs(reinterpret_cast<const float4*>(p.main_grad + T.l0 + e));
+      T.w[u] = __ldcs(reinterpret_cast<const float4*>(wbase + T.m0 + e));
+      T.m[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg + T.l0 + e));
+      T.v[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg_sq + T.l0 + e));
+    }
+  }
+}
+
+template <typename PT>
+__global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(const __grid_constant__ K3Params p) {
+  if (*p.found_inf) return;  // skipped step: nothing is written
+  const float c = *p.coef;
+  float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
+  int si = 0;
+  int t = blockIdx.x;
+  if (t >= p.tab.n_tiles) return;
+  K3Tile cur;
+  k3_load<PT>(p, wbase, t, si, cur);
+  for (; t < p.tab.n_tiles; t += gridDim.x) {
+    K3Tile nxt;
+    const bool more = t + (int)gridDim.x < p.tab.n_tiles;
+    if (more) k3_load<PT>(p, wbase, t + gridDim.x, si, nxt);
+#pragma unroll
+    for (int u = 0; u < kUnroll3; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (cur.aligned && e + kVec <= cur.n) {
+        float g[kVec] = {cur.g[u].x, cur.g[u].y, cur.g[u].z, cur.g[u].w};
+        float w[kVec] = {cur.w[u].x, cur.w[u].y, cur.w[u].z, cur.w[u].w};
+        float m[kVec] = {cur.m[u].x, cur.m[u].y, cur.m[u].z, cur.m[u].w};
+        float v[kVec] = {cur.v[u].x, cur.v[u].y, cur.v[u].z, cur.v[u].w};
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[j], c), cur.decay, p, w[j], m[j], v[j]);
+        __stcs(reinterpret_cast<float4*>(wbase + cur.m0 + e), make_float4(w[0], w[1], w[2], w[3]));
+        __stcs(reinterpret_cast<float4*>(p.exp_avg + cur.l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + cur.l0 + e), make_float4(v[0], v[1], v[2], v[3]));
+        ParamT<PT>::store4(p.param, cur.w0 + e, w);
+      } else if (e < cur.n) {
+        const int cnt = min(kVec, cur.n - e);
+        for (int j = 0; j < cnt; ++j) {
+          float ww = wbase[cur.m0 + e + j], mm = p.exp_avg[cur.l0 + e + j], vv = p.exp_avg_sq[cur.l0 + e + j];
+          adamw1(__fmul_rn(p.main_grad[cur.l0 + e + j], c), cur.decay, p, ww, mm, vv);
+          wbase[cur.m0 + e + j] = ww;
+          p.exp_avg[cur.l0 + e + j] = mm;
+          p.exp_avg_sq[cur.l0 + e + j] = vv;
+          ParamT<PT>::store1(p.param, cur.w0 + e + j, ww);
+        }
+      }
+    }
+    if (more) cur = nxt;
+  }
+}
+
 // ------------------------------------------------------------ host side --
 
 thread_local std::vector<char> t_param_scratch;  // kernel-parameter staging
@@ -965,7 +1046,7 @@ double pow_int(double b, int64_t t) {
 
 template <typename PT>
 int launch_k3_t(K3Params& kp, int n_tiles, cudaStream_t s) {
-  auto kern = k3_adamw<PT>;
+  auto kern = DOPT_K3_PIPE ? k3_adamw_pipe<PT> : k3_adamw<PT>;
   int grid = 0;
   int st = grid_for(kern, n_tiles, &grid);
   if (st) return st;
