@@ -423,6 +423,32 @@ def test_skip_leaves_state_untouched():
     assert res["found_inf"]
 
 
+def test_inf_anywhere_in_params_skips_but_padding_does_not():
+    """Brute force over a tiny two-buffer map with padding: a non-finite grad
+    at any param element of any rank's shard sets found_inf; one in a
+    padding position is never read (padding is not a parameter)."""
+    params = [dict(numel=n, dtype=d) for n, d in [(70, BF16), (5, F32), (130, BF16), (33, F32)]]
+    m = oracle.ShardMap(params, 4, 100, True)
+    owned = [np.zeros(b.numel, bool) for b in m.buffers]
+    for bi, buf in enumerate(m.buffers):
+        for pid in buf.params:
+            s0, e0, _ = buf.index[pid]
+            owned[bi][s0:e0] = True
+    assert not all(o.all() for o in owned)  # the map has padding
+    for bi, buf in enumerate(m.buffers):
+        for w in range(buf.numel):
+            grads = [[np.zeros(b.numel, np.float32) for _ in range(4)] for b in m.buffers]
+            grads[bi][w % 4][w] = np.inf
+            st = [{"exp_avg": np.zeros(4 * m.shard_numel(i), np.float32),
+                   "exp_avg_sq": np.zeros(4 * m.shard_numel(i), np.float32),
+                   **({"master": np.zeros(4 * m.shard_numel(i), np.float32)}
+                      if b.param_dtype != F32 else {})} for i, b in enumerate(m.buffers)]
+            pb = [np.zeros(b.numel, np.uint16 if b.param_dtype != F32 else np.float32)
+                  for b in m.buffers]
+            res = oracle.step(m, [0, 1, 2, 3], grads, st, pb, W.HP, 1)
+            assert res["found_inf"] == bool(owned[bi][w]), (bi, w)
+
+
 def test_stream_sumsq_equals_array_path():
     n_rep = 8
     keys = [synth.key(3, synth.STREAM_GRAD, 1, k) for k in range(n_rep)]

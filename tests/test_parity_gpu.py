@@ -165,3 +165,32 @@ def test_scale_gradients_and_zero_count(grad_fp32):
         found, norm = dc.step(grads, t)
         assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
         hc.t_applied += 1
+
+
+def test_dynamic_loss_scaler_through_a_skipped_step():
+    """fp16 with the library's dynamic loss scaler driving inv_loss_scale:
+    an overflow at step 2 skips the step and halves the scale; the next
+    steps run with the new scale (both sides follow the same trajectory)."""
+    D = H.dopt()
+    cfg = W.mini("llama_1p3b_fp16_dp8")
+    cfg = dict(cfg, inf_at=dict(step=2, replica=3, buffer_frac=0.3), steps=4)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    scaler = D.dopt_loss_scaler_init(65536.0, 2.0, 0.5, growth_interval=2, hysteresis=1)
+    report = []
+    scales = []
+    for step in range(1, 5):
+        hc.cfg["loss_scale"] = scaler.scale
+        scales.append(scaler.scale)
+        grads = hc.grads(step)
+        t = hc.t_applied + 1
+        before = H.snapshot(hc)
+        ores = hc.oracle_step(grads, t)
+        found, norm = dc.step(grads, t)
+        assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
+        assert found == (step == 2)
+        if not found:
+            hc.t_applied += 1
+        D.dopt_loss_scaler_update(scaler, found)
+    assert scales == [65536.0, 65536.0, 32768.0, 32768.0]
+    assert scaler.scale == 65536.0  # two clean steps after the backoff: growth
