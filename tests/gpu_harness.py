@@ -442,6 +442,9 @@ class FullCase:
         for bi, slot, pid, lo, w, n in pcs:
             out.append((bi, pid, lo, w))
             out.append((bi, pid, lo + n - 1, w + n - 1))
+            for cut in range(1 << 30, n, 1 << 30):  # both sides of a 2^30-element run cut
+                out.append((bi, pid, lo + cut - 1, w + cut - 1))
+                out.append((bi, pid, lo + cut, w + cut))
         lens = np.array([p[5] for p in pcs], dtype=np.float64)
         pick = rng.choice(len(pcs), size=n_random, p=lens / lens.sum())
         for i in pick:

@@ -105,3 +105,14 @@ def test_llama_1p3b_fp16_loss_scaled():
 
 def test_bf16_replica_grads_fp32_accumulation():
     _run(W.config("llama_7b_dp8_rank0_bf16grads"), steps=1)
+
+
+def test_param_larger_than_2_pow_31_elements():
+    """One bf16 param of 2^31 + 12345 elements (DP=2, shard-only layout):
+    runs are cut at 2^30 elements and every index is 64-bit; the sampled
+    elements include both sides of every cut and the ragged end."""
+    n = (1 << 31) + 12345
+    cfg = W._cfg(name="huge", params=[dict(name="huge", numel=n, dtype=W.BF16),
+                                      dict(name="tail", numel=77, dtype=W.F32)],
+                 dp=2, bucket_size=None, layout="shard", ranks=[1], steps=1, seed=21)
+    _run(cfg, steps=1, n_random=2000)
