@@ -324,7 +324,7 @@ class OracleSample:
                 f"{self.rank}'s bf16 shard of {self.cfg['name']}, {self.n_rep} fp32 replicas")
 
 
-def cpu_baseline(cfg, seconds_target=10.0, max_passes=8):
+def cpu_baseline(cfg, seconds_target=12.0, max_passes=40):
     """The oracle timed on the host over a bounded sample: repeated full
     oracle steps on CPU_SAMPLE_ELEMENTS elements, at least seconds_target
     seconds (at most max_passes steps)."""

@@ -298,10 +298,14 @@ typedef struct {
   int32_t found_inf;
   int32_t clipped;
   int64_t num_zeros;
+  int32_t kernel_error; /* nonzero: a kernel gave up waiting for its own data
+                           copies; the step was skipped (found_inf set) */
+  int32_t reserved;
 } dopt_step_stats;
 
 /* Copies the statistics of the last step run with `workspace` (fused or
- * bucket-staged layout) to the host; waits for `stream`. */
+ * bucket-staged layout) to the host; waits for `stream`.  dopt_step and
+ * dopt_step_noalloc return DOPT_E_CUDA when kernel_error is set. */
 int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_stream stream);
 
 /*

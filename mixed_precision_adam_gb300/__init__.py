@@ -76,7 +76,7 @@ class dopt_step_args(ctypes.Structure):
 
 class dopt_step_stats(ctypes.Structure):
     _fields_ = [("sumsq", _D), ("grad_norm", _F), ("clip_coef", _F), ("found_inf", _I32),
-                ("clipped", _I32), ("num_zeros", _I64)]
+                ("clipped", _I32), ("num_zeros", _I64), ("kernel_error", _I32), ("reserved", _I32)]
 
 
 class dopt_loss_scaler(ctypes.Structure):

@@ -22,6 +22,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -46,6 +47,12 @@ namespace {
 #endif
 #ifndef DOPT_K3_PIPE
 #define DOPT_K3_PIPE 1  // 1: the AdamW pass loads the next tile before computing this one
+#endif
+#ifndef DOPT_K1_TMA
+#define DOPT_K1_TMA 1  // 1: single-instance reduce stages replica tiles through shared memory with TMA
+#endif
+#ifndef DOPT_TMA_STAGES
+#define DOPT_TMA_STAGES 2
 #endif
 #ifndef DOPT_K1_MIN_BLOCKS
 #define DOPT_K1_MIN_BLOCKS 2
@@ -93,7 +100,12 @@ static_assert(sizeof(Partial) == 16, "Partial layout");
 // Device scalars of one step, at the start of the workspace: the public
 // dopt_step_stats layout.
 using Scalars = dopt_step_stats;
-static_assert(sizeof(Scalars) == 32, "dopt_step_stats layout");
+static_assert(sizeof(Scalars) == 40, "dopt_step_stats layout");
+// Byte offset, inside the workspace's scalar area, of the word a reduce
+// kernel sets when it gives up waiting for its own copies; the finalize
+// pass reports it as dopt_step_stats.kernel_error and clears it.
+constexpr size_t kErrorFlagOffset = 128;
+constexpr int32_t kErrorMagic = 0x4B31544D;  // the flag's "set" value
 
 struct K1Params {
   const void* rep[DOPT_MAX_REPLICAS];
@@ -106,6 +118,9 @@ struct K1Params {
   float inv_scale;  // 1 / loss scale
   int32_t average;
   float post_scale; // scale_gradients factor on the reduced grad (1 = none)
+  int32_t* error_flag;  // set by a kernel that gave up waiting (TMA path)
+  int32_t use_tma;      // host's choice: launch the TMA-staged kernel
+  int32_t pad2;
   SegTable tab;
 };
 
@@ -513,12 +528,194 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
   if (STATS) write_partial(acc, p.partials);
 }
 
+// ---------------------------------------------------------- K1 with TMA --
+//
+// The single-instance reduction with every replica tile staged through
+// shared memory by the bulk-copy engine (cp.async.bulk, one 1-D copy per
+// replica per tile, completion counted in bytes on a per-stage mbarrier).
+// A ring of DOPT_TMA_STAGES stages keeps up to stages x replicas x tile bytes
+// in flight per SM independently of registers; thread 0 issues, every thread
+// consumes.  Every wait is bounded: a CTA that gives up (decided uniformly)
+// sets the error flag, marks its partial non-finite so the step is skipped,
+// waits (bounded) for its copies still in flight and leaves.  Used for
+// fp32 replicas when every run of the launch is 8-element aligned.
+
+#ifndef DOPT_TMA_TILE
+#define DOPT_TMA_TILE 2048
+#endif
+constexpr int kTmaTile = DOPT_TMA_TILE;     // elements per tile (a multiple of kThreads * kVec)
+static_assert(kTmaTile % (kThreads * kVec) == 0, "TMA tile");
+constexpr long long kWaitPolls = 1ll << 22; // try_wait polls before giving up
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Polls an mbarrier phase at most kWaitPolls times.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+  for (long long i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+#ifndef DOPT_TMA_EVICT_FIRST
+#define DOPT_TMA_EVICT_FIRST 1  // 1: the replica tiles are marked first to leave L2
+#endif
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+#if DOPT_TMA_EVICT_FIRST
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"((unsigned long long)__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+#else
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"((unsigned long long)__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+#endif
+}
+
+template <typename GT>
+struct GradBits {
+  using T = typename std::conditional<std::is_same<GT, float>::value, float, unsigned short>::type;
+};
+
+template <typename GT, int DPI>
+__host__ __device__ constexpr size_t tma_smem_bytes() {
+  return (size_t)DOPT_TMA_STAGES * DPI * kTmaTile * sizeof(typename GradBits<GT>::T) +
+         DOPT_TMA_STAGES * sizeof(uint64_t);
+}
+
+template <typename GT, bool FULL, bool STATS, int DPI>
+__global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __grid_constant__ K1Params p) {
+  using E = typename GradBits<GT>::T;
+  constexpr int S = DOPT_TMA_STAGES;
+  constexpr int VALIGN = 16 / sizeof(E);  // elements per 16 bytes: bulk sizes are multiples of it
+  extern __shared__ __align__(128) unsigned char smem[];
+  E* tiles = reinterpret_cast<E*>(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * DPI * kTmaTile * sizeof(E));
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int G = gridDim.x;
+  const int my = p.tab.n_tiles > (int)blockIdx.x ? (p.tab.n_tiles - (int)blockIdx.x + G - 1) / G : 0;
+  int si_issue = 0;
+  // thread 0: start the copies of this CTA's i-th tile into stage i % S
+  auto issue = [&](int i) {
+    const int t = blockIdx.x + i * G;
+    si_issue = seek(p.tab, si_issue, t);
+    const Seg& sg = p.tab.seg[si_issue];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTmaTile;
+    const int n = (int)min((int64_t)kTmaTile, (int64_t)sg.len - off);
+    const int nv = n & ~(VALIGN - 1);
+    const int64_t r0 = FULL ? sg.world + off : sg.local + off;
+    const int stage = i % S;
+    mbar_arrive_expect_tx(&bars[stage], (unsigned)(nv * sizeof(E)) * DPI);
+    if (nv > 0) {
+#pragma unroll
+      for (int k = 0; k < DPI; ++k)
+        bulk_load(tiles + ((size_t)stage * DPI + k) * kTmaTile, static_cast<const E*>(p.rep[k]) + r0,
+                  (unsigned)(nv * sizeof(E)), &bars[stage]);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(S, my); ++i) issue(i);
+
+  SumSq acc;
+  int si = 0;
+  bool failed = false;
+  const float pre = p.pre, inv_scale = p.inv_scale;
+  int i = 0;
+  for (; i < my; ++i) {
+    const int stage = i % S;
+    const bool ok = mbar_wait_bounded(&bars[stage], (unsigned)((i / S) & 1));
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    const int t = blockIdx.x + i * G;
+    si = seek(p.tab, si, t);
+    const Seg& sg = p.tab.seg[si];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTmaTile;
+    const int n = (int)min((int64_t)kTmaTile, (int64_t)sg.len - off);
+    const int nv = n & ~(VALIGN - 1);
+    const int64_t l0 = sg.local + off;
+    const int64_t r0 = FULL ? sg.world + off : l0;
+    const E* st = tiles + (size_t)stage * DPI * kTmaTile;
+#pragma unroll
+    for (int u = 0; u < kTmaTile / (kThreads * kVec); ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (e + kVec <= nv) {
+        float m[kVec];
+        typename GradT<GT>::Raw x[DPI];
+#pragma unroll
+        for (int k = 0; k < DPI; ++k)
+          x[k] = *reinterpret_cast<const typename GradT<GT>::Raw*>(st + (size_t)k * kTmaTile + e);
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          float sum = __fmul_rn(GradT<GT>::at(x[0], q), pre);
+#pragma unroll
+          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::at(x[k], q), pre));
+          m[q] = __fmul_rn(post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale), inv_scale);
+        }
+        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        if (STATS) acc.add4(m);
+      } else if (e < n) {
+        // the last few elements of a run: not in the staged copy
+        const int cnt = min(kVec, n - e);
+        for (int q = 0; q < cnt; ++q) {
+          float sum = __fmul_rn(GradT<GT>::widen1(p.rep[0], r0 + e + q), pre);
+          for (int k = 1; k < DPI; ++k)
+            sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::widen1(p.rep[k], r0 + e + q), pre));
+          float m = __fmul_rn(post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale), inv_scale);
+          p.main_grad[l0 + e + q] = m;
+          if (STATS) acc.add1(m);
+        }
+      }
+    }
+    if (STATS) acc.maybe_flush();
+    __syncthreads();  // every thread is done with this stage
+    if (threadIdx.x == 0 && i + S < my) issue(i + S);
+  }
+  if (failed) {
+    if (threadIdx.x == 0) {
+      *p.error_flag = kErrorMagic;
+      // let the copies already issued land before the shared memory goes away
+      for (int j = i; j < min(i + S, my); ++j) mbar_wait_bounded(&bars[j % S], (unsigned)((j / S) & 1));
+    }
+    __syncthreads();
+    acc.s = __int_as_float(0x7FC00000);  // a NaN partial skips the step
+  }
+  if (STATS) write_partial(acc, p.partials);
+}
+
 // ------------------------------------------------------------------- K2 --
 
 __global__ void __launch_bounds__(kThreads)
 k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
             int remote_found_inf, double max_norm, Scalars* __restrict__ sc,
-            float* d_norm, float* d_coef, int32_t* d_found) {
+            float* d_norm, float* d_coef, int32_t* d_found, int32_t* err_flag) {
   __shared__ double s_sum[kThreads];
   __shared__ int s_bad[kThreads];
   __shared__ long long s_zero[kThreads];
@@ -543,8 +740,10 @@ k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
     __syncthreads();
   }
   if (threadIdx.x == 0) {
+    const int kernel_error = *err_flag == kErrorMagic ? 1 : 0;
+    *err_flag = 0;
     const double sumsq = s_sum[0] + remote_sumsq;
-    const int found = (s_bad[0] || remote_found_inf) ? 1 : 0;
+    const int found = (s_bad[0] || remote_found_inf || kernel_error) ? 1 : 0;
     const double norm = sqrt(sumsq);
     double coef = 1.0;
     int clip = 0;
@@ -560,6 +759,8 @@ k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
     sc->found_inf = found;
     sc->clipped = clip;
     sc->num_zeros = s_zero[0];
+    sc->kernel_error = kernel_error;
+    sc->reserved = 0;
     if (d_norm) *d_norm = norm_f;
     if (d_coef) *d_coef = coef_f;
     if (d_found) *d_found = found;
@@ -904,8 +1105,27 @@ int launch_k1_t(K1Params& kp, int n_tiles, cudaStream_t s) {
   return check_launch("k1_reduce_prepare launch");
 }
 
+template <typename GT, bool FULL, bool STATS, int DPI>
+int launch_k1_tma(K1Params& kp, int n_tiles, cudaStream_t s) {
+  auto kern = k1_reduce_prepare_tma<GT, FULL, STATS, DPI>;
+  const size_t smem = tma_smem_bytes<GT, DPI>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess)
+    return dopt::fail(DOPT_E_CUDA, std::string("k1 tma smem attribute: ") + cudaGetErrorString(e));
+  int sms = 0, per_sm = 0;
+  int st = device_sms(&sms);
+  if (st) return st;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess || per_sm < 1)
+    return dopt::fail(DOPT_E_CUDA, "k1 tma occupancy query failed");
+  const int grid = std::max(1, std::min({per_sm * sms, kMaxGrid, std::max(1, n_tiles)}));
+  kern<<<grid, kThreads, smem, s>>>(kp);
+  return check_launch("k1_reduce_prepare_tma launch");
+}
+
 template <typename GT, bool FULL, bool STATS, int DPI, int NINST>
 int launch_k1_n(K1Params& kp, int n_tiles, cudaStream_t s) {
+  if (STATS && NINST == 1 && kp.use_tma) return launch_k1_tma<GT, FULL, STATS, DPI>(kp, n_tiles, s);
   auto kern = k1_reduce_prepare_n<GT, FULL, STATS, DPI, NINST>;
   int grid = 0;
   int st = grid_for(kern, n_tiles, &grid);
@@ -983,7 +1203,19 @@ int run_k1_runs(const std::vector<dopt::Run>& runs, int region_first, const void
     kp.inv_scale = inv_scale;
     kp.average = average ? 1 : 0;
     kp.post_scale = post_scale;
-    fill_table(kp.tab, runs, c, k1_tile(gdt, n_rep, n_inst, average), 0.0, 0.0);
+    kp.error_flag = ws ? reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset) : nullptr;
+    bool all_aligned = true;
+    for (int k = 0; k < c.count; ++k) {
+      const dopt::Run& r = runs[c.first + k];
+      all_aligned &= (r.local % 8) == 0 && (r.world % 8) == 0;
+    }
+    const int dpi = n_rep / n_inst;
+    // fp32 replicas only: 16-bit replicas stream faster through registers
+    // (packed loads, four accesses per thread)
+    kp.use_tma = (DOPT_K1_TMA && stats && ws && all_aligned && n_inst == 1 && !average &&
+                  gdt == DOPT_F32 && (dpi == 1 || dpi == 2 || dpi == 4 || dpi == 8)) ? 1 : 0;
+    kp.pad2 = 0;
+    fill_table(kp.tab, runs, c, kp.use_tma ? kTmaTile : k1_tile(gdt, n_rep, n_inst, average), 0.0, 0.0);
     const int n_tiles = kp.tab.n_tiles;
     int st;
     if (stats)
@@ -1014,7 +1246,8 @@ float grad_scale_of(const dopt_step_args* a) { return a->grad_scale == 0.0f ? 1.
 int run_k2_slots(int n_slots, void* ws, double remote_sumsq, int32_t remote_found, double max_norm,
                  float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
   k2_finalize<<<1, kThreads, 0, s>>>(region_ptr(ws, 0), n_slots, remote_sumsq, remote_found ? 1 : 0,
-                                     max_norm, scalars_ptr(ws), d_norm, d_coef, d_found);
+                                     max_norm, scalars_ptr(ws), d_norm, d_coef, d_found,
+                                     reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset));
   return check_launch("k2_finalize launch");
 }
 
