@@ -432,6 +432,14 @@ int dopt_loss_scaler_init(dopt_loss_scaler* s, double initial_scale, double grow
                           double min_scale);
 int dopt_loss_scaler_update(dopt_loss_scaler* s, int32_t found_inf);
 
+/* Test hook for the bounded waits of the TMA-staged reduce pass: while set
+ * to tile >= 0, CTA 0 of every such launch announces its tile of that
+ * (CTA-local) index but never copies it, so its wait runs out after about a
+ * second; the step then reports kernel_error, returns DOPT_E_CUDA from
+ * dopt_step and is skipped, and the CUDA context stays usable.  -1 turns the
+ * hook off (the default).  Not for production use. */
+int dopt_debug_starve_copy(int32_t tile);
+
 /* Number of kernels this library has launched in this process (all
  * devices, all threads); a caller can difference it around a region. */
 uint64_t dopt_kernel_launches(void);

@@ -120,7 +120,7 @@ struct K1Params {
   float post_scale; // scale_gradients factor on the reduced grad (1 = none)
   int32_t* error_flag;  // set by a kernel that gave up waiting (TMA path)
   int32_t use_tma;      // host's choice: launch the TMA-staged kernel
-  int32_t pad2;
+  int32_t starve_tile;  // test hook: CTA 0 never copies its tile of this index (-1: off)
   SegTable tab;
 };
 
@@ -545,7 +545,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
 #endif
 constexpr int kTmaTile = DOPT_TMA_TILE;     // elements per tile (a multiple of kThreads * kVec)
 static_assert(kTmaTile % (kThreads * kVec) == 0, "TMA tile");
-constexpr long long kWaitPolls = 1ll << 22; // try_wait polls before giving up
+constexpr unsigned long long kWaitNs = 1000000000ull;  // give up a wait after 1 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -566,11 +566,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
       : "memory");
   return ok != 0;
 }
-// Polls an mbarrier phase at most kWaitPolls times.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Polls an mbarrier phase for at most kWaitNs nanoseconds.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
-  for (long long i = 0; i < kWaitPolls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
 }
 #ifndef DOPT_TMA_EVICT_FIRST
 #define DOPT_TMA_EVICT_FIRST 1  // 1: the replica tiles are marked first to leave L2
@@ -632,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
     const int64_t r0 = FULL ? sg.world + off : sg.local + off;
     const int stage = i % S;
     mbar_arrive_expect_tx(&bars[stage], (unsigned)(nv * sizeof(E)) * DPI);
-    if (nv > 0) {
+    if (nv > 0 && !(blockIdx.x == 0 && i == p.starve_tile)) {
 #pragma unroll
       for (int k = 0; k < DPI; ++k)
         bulk_load(tiles + ((size_t)stage * DPI + k) * kTmaTile, static_cast<const E*>(p.rep[k]) + r0,
@@ -959,6 +968,7 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
 
 thread_local std::vector<char> t_param_scratch;  // kernel-parameter staging
 std::atomic<uint64_t> g_launches{0};             // kernels launched by this library
+std::atomic<int32_t> g_starve_tile{-1};           // test hook, see dopt_debug_starve_copy
 
 // The run table of one launch: runs [first, first + count) of a rank
 // selection, with per-run decay for K3.
@@ -1214,7 +1224,7 @@ int run_k1_runs(const std::vector<dopt::Run>& runs, int region_first, const void
     // (packed loads, four accesses per thread)
     kp.use_tma = (DOPT_K1_TMA && stats && ws && all_aligned && n_inst == 1 && !average &&
                   gdt == DOPT_F32 && (dpi == 1 || dpi == 2 || dpi == 4 || dpi == 8)) ? 1 : 0;
-    kp.pad2 = 0;
+    kp.starve_tile = g_starve_tile.load(std::memory_order_relaxed);
     fill_table(kp.tab, runs, c, kp.use_tma ? kTmaTile : k1_tile(gdt, n_rep, n_inst, average), 0.0, 0.0);
     const int n_tiles = kp.tab.n_tiles;
     int st;
@@ -1447,6 +1457,12 @@ extern "C" {
 
 uint64_t dopt_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int dopt_debug_starve_copy(int32_t tile) {
+  if (tile < -1) return dopt::fail(DOPT_E_INVALID, "dopt_debug_starve_copy: tile < -1");
+  g_starve_tile.store(tile, std::memory_order_relaxed);
+  return DOPT_OK;
+}
+
 int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_stream stream) {
   if (!workspace || !out) return dopt::fail(DOPT_E_INVALID, "dopt_read_step_stats: NULL workspace or out");
   cudaStream_t s = (cudaStream_t)stream;
@@ -1665,6 +1681,9 @@ int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_
   if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
   if (found_inf_out) *found_inf_out = host.found_inf;
   if (grad_norm_out) *grad_norm_out = host.grad_norm;
+  if (host.kernel_error)
+    return dopt::fail(DOPT_E_CUDA,
+                      "dopt_step: a kernel gave up waiting for its own data copies; the step was skipped");
   return DOPT_OK;
 }
 

@@ -194,3 +194,37 @@ def test_dynamic_loss_scaler_through_a_skipped_step():
         D.dopt_loss_scaler_update(scaler, found)
     assert scales == [65536.0, 65536.0, 32768.0, 32768.0]
     assert scaler.scale == 65536.0  # two clean steps after the backoff: growth
+
+
+def test_bounded_wait_runs_out_and_reports():
+    """A tile whose copy is never issued (test hook): the TMA-staged reduce
+    gives up after its bounded wait, the step is skipped and reported as a
+    kernel error, the state is untouched, and the next step is correct."""
+    D = H.dopt()
+    params = [dict(numel=300_000, dtype=1), dict(numel=4096, dtype=1)]
+    cfg = _tiny(params, 2, bucket_size=None, steps=2)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    grads = hc.grads(1)
+    before = dc.download()
+    D.dopt_debug_starve_copy(0)
+    try:
+        with pytest.raises(D.DoptError) as e:
+            dc.step(grads, 1)
+    finally:
+        D.dopt_debug_starve_copy(-1)
+    assert e.value.status == D.E_CUDA and "gave up waiting" in str(e.value)
+    stats = D.dopt_read_step_stats(dc.ws)
+    assert stats["kernel_error"] == 1 and stats["found_inf"] == 1
+    after = dc.download()
+    for b_list, a_list in zip(before[:4], after[:4]):
+        for b, a in zip(b_list, a_list):
+            if b is not None:
+                assert b.tobytes() == a.tobytes()
+    # the context is usable and the next step matches the oracle
+    report = []
+    snap = H.snapshot(hc)
+    ores = hc.oracle_step(grads, 1)
+    found, norm = dc.step(grads, 1)
+    assert H.compare_step(hc, dc, ores, found, norm, snap, report), "\n".join(report)
+    assert D.dopt_read_step_stats(dc.ws)["kernel_error"] == 0
