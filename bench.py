@@ -79,16 +79,35 @@ def workload_config(name, layers=None):
     return cfg
 
 
+SHAPES = {
+    "toy_mlp_dp4": "toy MLP, 4 x {W [1024,512], b [1024], W2 [512,1024], b2 [512]}",
+    "gpt2_small_dp8": "GPT-2-small-shaped (12 layers, d=768, ffn 3072, vocab 50257), fp32 LayerNorm group",
+    "llama_1p3b_fp16_dp8": "Llama-1.3B-shaped (24 layers, d=2048, ffn 5504, vocab 32000), fp16 params, "
+                           "fp32 RMSNorm group, loss scale 65536",
+}
+
+
 def describe(cfg, n_elems):
-    n_layers = sum(1 for p in cfg["params"] if p["name"].endswith("q_proj"))
-    return (f"{cfg['name']}: Llama-7B-shaped ({n_layers} layers, d=4096, ffn 11008, vocab 32000), "
-            f"bf16 params + fp32 RMSNorm group, DP={cfg['dp']} x {cfg['n_inst']} instance(s) "
-            f"emulated, rank {cfg['ranks'][0]}'s shard of {n_elems} param elements, "
-            f"{cfg['dp'] * cfg['n_inst']} fp32 replica grad shards, bucket "
-            f"{cfg['bucket_size']}, AdamW lr 1e-4 betas (0.9, 0.95) eps 1e-8 wd 0.1, clip 1.0")
+    n_rep = cfg["dp"] * cfg["n_inst"]
+    gtype = "fp32" if cfg["grad_reduce_in_fp32"] else "16-bit"
+    if cfg["ranks"] == "all":
+        who = f"all {cfg['dp']} ranks' shards ({n_elems} param elements)"
+        reps = f"{n_rep} {gtype} replica grad buffers (whole buffers)"
+    else:
+        who = f"rank {cfg['ranks'][0]}'s shard of {n_elems} param elements"
+        reps = f"{n_rep} {gtype} replica grad shards"
+    base = cfg["name"].split("_2layers")[0]
+    shape = SHAPES.get(base)
+    if shape is None:
+        n_layers = sum(1 for p in cfg["params"] if p["name"].endswith("q_proj"))
+        shape = (f"Llama-7B-shaped ({n_layers} layers, d=4096, ffn 11008, vocab 32000), bf16 params + "
+                 f"fp32 RMSNorm group")
+    return (f"{cfg['name']}: {shape}, DP={cfg['dp']} x {cfg['n_inst']} instance(s) emulated, {who}, "
+            f"{reps}, bucket {cfg['bucket_size']}, AdamW lr 1e-4 betas (0.9, 0.95) eps 1e-8 "
+            f"wd 0.1, clip 1.0")
 
 
-def algorithmic_bytes(D, pm, n_rep, rank):
+def algorithmic_bytes(D, pm, n_rep, ranks):
     """Per-stage algorithmic DRAM bytes of one step and the stepped element count.
     K1 reads every replica element once and writes the fp32 main grad once;
     K3 reads main grad, master, m, v once and writes master, m, v and (16-bit
@@ -96,7 +115,8 @@ def algorithmic_bytes(D, pm, n_rep, rank):
     k1 = k3 = elems = 0
     for b in range(D.dopt_num_buffers(pm)):
         info = D.dopt_buffer_info_get(pm, b)
-        n = sum(s["gbuf_local"][1] - s["gbuf_local"][0] for s in D.dopt_rank_shards(pm, b, rank))
+        n = sum(s["gbuf_local"][1] - s["gbuf_local"][0]
+                for r in ranks for s in D.dopt_rank_shards(pm, b, r))
         elems += n
         k1 += n * (n_rep * ELEM_BYTES[info["grad_dtype"]] + 4)
         k3 += n * (16 + 12 + (ELEM_BYTES[info["param_dtype"]] if info["param_dtype"] != F32 else 0))
@@ -111,7 +131,10 @@ class Workload:
         import synth
         import mixed_precision_adam_gb300 as D
         self.D, self.torch, self.cfg = D, torch, cfg
-        self.rank = cfg["ranks"][0]
+        self.all_ranks = cfg["ranks"] == "all"
+        self.ranks = list(range(cfg["dp"])) if self.all_ranks else list(cfg["ranks"])
+        self.rank = D.ALL_RANKS if self.all_ranks else self.ranks[0]
+        self.full = cfg["layout"] == "full"
         self.n_rep = cfg["dp"] * cfg["n_inst"]
         self.pm = D.dopt_build_shard_map(cfg["params"], cfg["dp"], cfg["bucket_size"],
                                          cfg["grad_reduce_in_fp32"], False)
@@ -124,16 +147,22 @@ class Workload:
         for b in range(D.dopt_num_buffers(self.pm)):
             info = D.dopt_buffer_info_get(self.pm, b)
             S = info["shard_numel"]
+            n_local = S * len(self.ranks)
             buckets = [D.dopt_bucket_info_get(self.pm, b, k) for k in range(info["n_buckets"])]
             reps = []
             for k in range(self.n_rep):
-                t = torch.empty(S, dtype=tdt[info["grad_dtype"]], device=dev)
                 gkey = synth.key(cfg["seed"], synth.STREAM_GRAD, 1, k)
-                for bk in buckets:
-                    s = bk["shard_numel"]
-                    synth.cuda_normal_(t.data_ptr() + bk["shard_base"] * t.element_size(), s, gkey,
-                                       bk["offset"] + self.rank * s, cfg["grad_sigma"],
+                if self.full:
+                    t = torch.empty(info["numel"], dtype=tdt[info["grad_dtype"]], device=dev)
+                    synth.cuda_normal_(t.data_ptr(), info["numel"], gkey, 0, cfg["grad_sigma"],
                                        kinds[info["grad_dtype"]], stream)
+                else:
+                    t = torch.empty(S, dtype=tdt[info["grad_dtype"]], device=dev)
+                    for bk in buckets:
+                        s = bk["shard_numel"]
+                        synth.cuda_normal_(t.data_ptr() + bk["shard_base"] * t.element_size(), s,
+                                           gkey, bk["offset"] + self.ranks[0] * s, cfg["grad_sigma"],
+                                           kinds[info["grad_dtype"]], stream)
                 reps.append(t)
             self.reps.append(reps)
             p = torch.empty(info["numel"], dtype=tdt[info["param_dtype"]], device=dev)
@@ -143,27 +172,30 @@ class Workload:
             if info["param_dtype"] == F32:
                 self.master.append(None)
             else:
-                mt = torch.empty(S, dtype=torch.float32, device=dev)
+                mt = torch.empty(n_local, dtype=torch.float32, device=dev)
                 vk = synth.OUT_F32_OF_BF16 if info["param_dtype"] == BF16 else synth.OUT_F32_OF_F16
-                for bk in buckets:
-                    s = bk["shard_numel"]
-                    synth.cuda_normal_(mt.data_ptr() + bk["shard_base"] * 4, s, pkey,
-                                       bk["offset"] + self.rank * s, cfg["param_sigma"], vk, stream)
+                for slot, r in enumerate(self.ranks):
+                    for bk in buckets:
+                        s = bk["shard_numel"]
+                        synth.cuda_normal_(mt.data_ptr() + (slot * S + bk["shard_base"]) * 4, s, pkey,
+                                           bk["offset"] + r * s, cfg["param_sigma"], vk, stream)
                 self.master.append(mt)
-            self.m.append(torch.zeros(S, dtype=torch.float32, device=dev))
-            self.v.append(torch.zeros(S, dtype=torch.float32, device=dev))
-            self.main.append(torch.empty(S, dtype=torch.float32, device=dev))
+            self.m.append(torch.zeros(n_local, dtype=torch.float32, device=dev))
+            self.v.append(torch.zeros(n_local, dtype=torch.float32, device=dev))
+            self.main.append(torch.empty(n_local, dtype=torch.float32, device=dev))
         self.ws_bytes = D.dopt_workspace_bytes(self.pm, self.rank)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
-        self.k1_bytes, self.k3_bytes, self.elements = algorithmic_bytes(D, self.pm, self.n_rep, self.rank)
+        self.k1_bytes, self.k3_bytes, self.elements = algorithmic_bytes(D, self.pm, self.n_rep,
+                                                                        self.ranks)
         self.t_applied = 0
 
     def args(self, reps=None):
         D = self.D
         return D.StepArgs(self.pm, self.rank, reps or self.reps, self.main, self.master, self.m,
                           self.v, self.params, self.cfg["hp"], self.t_applied + 1, self.ws,
-                          self.ws_bytes, n_instances=self.cfg["n_inst"], layout=D.LAYOUT_SHARD_ONLY,
+                          self.ws_bytes, n_instances=self.cfg["n_inst"],
+                          layout=D.LAYOUT_FULL_BUFFER if self.full else D.LAYOUT_SHARD_ONLY,
                           inv_loss_scale=1.0 / self.cfg["loss_scale"], max_norm=self.cfg["max_norm"],
                           stream=self.torch.cuda.current_stream())
 
@@ -280,7 +312,7 @@ class OracleSample:
         self.ctypes, self.oracle = ctypes, oracle
         om = oracle.ShardMap(cfg["params"], cfg["dp"], cfg["bucket_size"], cfg["grad_reduce_in_fp32"])
         self.cfg = cfg
-        self.rank = cfg["ranks"][0]
+        self.rank = 0 if cfg["ranks"] == "all" else cfg["ranks"][0]
         self.n_rep = cfg["dp"] * cfg["n_inst"]
         pieces, total = [], 0
         for pid, b, v in om.rank_pieces(0, self.rank):
@@ -290,16 +322,21 @@ class OracleSample:
             pieces.append((pid, v["gbuf_world"].start, take))
             total += take
         self.pieces, self.elements = pieces, total
+        buf = om.buffers[0]
+        self.gdt, self.pdt = buf.grad_dtype, buf.param_dtype
+        gkind = {F32: synth.OUT_F32, BF16: synth.OUT_BF16, F16: synth.OUT_F16}[self.gdt]
         self.reps = [np.concatenate([synth.normal(n, synth.key(cfg["seed"], synth.STREAM_GRAD, 1, k),
-                                                  w, cfg["grad_sigma"]) for _, w, n in pieces])
+                                                  w, cfg["grad_sigma"], gkind) for _, w, n in pieces])
                      for k in range(self.n_rep)]
         pkey = synth.key(cfg["seed"], synth.STREAM_PARAM, 0, 0)
-        self.master = np.concatenate([synth.normal(n, pkey, w, cfg["param_sigma"],
-                                                   synth.OUT_F32_OF_BF16) for _, w, n in pieces])
+        mkind = {F32: synth.OUT_F32, BF16: synth.OUT_F32_OF_BF16, F16: synth.OUT_F32_OF_F16}[self.pdt]
+        self.master = np.concatenate([synth.normal(n, pkey, w, cfg["param_sigma"], mkind)
+                                      for _, w, n in pieces])
         self.m = np.zeros(total, np.float32)
         self.v = np.zeros(total, np.float32)
-        self.out = np.zeros(total, np.uint16)
+        self.out = np.zeros(total, np.uint16 if self.pdt != F32 else np.float32)
         self.main = np.zeros(total, np.float32)
+        self.inv_scale = float(np.float32(1.0 / cfg["loss_scale"]))
         self.L = oracle.lib()
         self.arr = (ctypes.c_void_p * self.n_rep)(*[x.ctypes.data for x in self.reps])
         self.h = oracle.Hparams(**cfg["hp"])
@@ -307,8 +344,8 @@ class OracleSample:
 
     def step(self):
         c, L = self.ctypes, self.L
-        bad = L.or_reduce_prepare_run(self.arr, self.n_rep, self.cfg["n_inst"], 0, 0, 0,
-                                      self.elements, c.c_float(1.0), c.c_float(1.0),
+        bad = L.or_reduce_prepare_run(self.arr, self.n_rep, self.cfg["n_inst"], self.gdt, 0, 0,
+                                      self.elements, c.c_float(1.0), c.c_float(self.inv_scale),
                                       self.main.ctypes.data)
         sumsq = L.or_sumsq_run(self.main.ctypes.data, self.elements)
         norm, coef = c.c_double(), c.c_double()
@@ -317,11 +354,13 @@ class OracleSample:
             self.t += 1
             L.or_adamw_run(self.main.ctypes.data, self.elements, coef.value, clip,
                            self.master.ctypes.data, self.m.ctypes.data, self.v.ctypes.data,
-                           c.byref(self.h), 1.0, self.t, self.out.ctypes.data, BF16)
+                           c.byref(self.h), 1.0, self.t, self.out.ctypes.data, self.pdt)
 
     def describe(self):
+        names = {F32: "fp32", BF16: "bf16", F16: "fp16"}
         return (f"{self.elements} elements ({len(self.pieces)} param pieces) at the start of rank "
-                f"{self.rank}'s bf16 shard of {self.cfg['name']}, {self.n_rep} fp32 replicas")
+                f"{self.rank}'s {names[self.pdt]} shard of {self.cfg['name']}, {self.n_rep} "
+                f"{names[self.gdt]} replicas")
 
 
 def cpu_baseline(cfg, seconds_target=12.0, max_passes=40):
@@ -528,6 +567,8 @@ def run_staged(args):
     import synth
     import mixed_precision_adam_gb300 as D
     cfg = workload_config(args.workload, args.layers)
+    if cfg["layout"] != "shard":
+        raise SystemExit("--staged takes a shard-layout workload")
     wl = Workload(cfg)
     main = torch.cuda.current_stream()
     side = torch.cuda.Stream()
@@ -543,7 +584,7 @@ def run_staged(args):
         for r, t in enumerate(wl.reps[b]):
             synth.cuda_normal_(t.data_ptr() + bk["shard_base"] * t.element_size(), s,
                                synth.key(cfg["seed"], synth.STREAM_GRAD, 1, r),
-                               bk["offset"] + wl.rank * s, cfg["grad_sigma"],
+                               bk["offset"] + wl.ranks[0] * s, cfg["grad_sigma"],
                                kinds[info["grad_dtype"]], main.cuda_stream)
 
     fused = wl.args()
