@@ -284,6 +284,21 @@ typedef struct {
    * means no scaling. */
   float grad_scale;
   int32_t reserved;
+  /* Optional device-resident step state, for steps replayed from a CUDA
+   * graph (whose launch parameters cannot change between replays):
+   *   d_step -- device int64: the count of applied steps.  When set, hp.step
+   *             is ignored; the finalize pass uses *d_step + 1 for the bias
+   *             corrections and writes it back only if the step is applied
+   *             (a skipped step does not count).
+   *   d_lr   -- device double: the learning rate, read by the finalize pass
+   *             (only with d_step); NULL uses hp.lr.
+   * Both 8-byte aligned.  With d_step, dopt_step_async, the bucket-staged
+   * entry points and dopt_step_noalloc issue only kernel launches on the
+   * stream once each kernel has run once on the device (its shared-memory
+   * attribute is set on first use), so a step can be captured in a graph
+   * after a warm-up step. */
+  int64_t* d_step;
+  const double* d_lr;
 } dopt_step_args;
 
 /* Statistics of the last step, kept at the start of its workspace:

@@ -71,7 +71,8 @@ class dopt_step_args(ctypes.Structure):
                 ("inv_loss_scale", _F), ("remote_found_inf", _I32),
                 ("max_norm", _D), ("remote_sumsq", _D), ("hp", dopt_adamw_hparams),
                 ("workspace", _P), ("workspace_bytes", _SZ), ("stream", _P),
-                ("stage_events", ctypes.POINTER(_P)), ("grad_scale", _F), ("reserved", _I32)]
+                ("stage_events", ctypes.POINTER(_P)), ("grad_scale", _F), ("reserved", _I32),
+                ("d_step", _P), ("d_lr", _P)]
 
 
 class dopt_step_stats(ctypes.Structure):
@@ -345,6 +346,12 @@ class StepArgs:
 
     def set_stream(self, stream):
         self.c.stream = _stream(stream)
+
+    def set_device_step(self, d_step, d_lr=None):
+        """Use a device int64 step counter (and optionally a device double
+        learning rate) instead of the host step number."""
+        self.c.d_step = _ptr(d_step)
+        self.c.d_lr = _ptr(d_lr)
 
     def set_step(self, step, lr=None):
         self.c.hp.step = int(step)

@@ -72,15 +72,18 @@ constexpr int kMaxGrid = 2048;             // partial slots per launch region
 constexpr int kBatch = 8;                  // replicas loaded together
 constexpr size_t kScalarBytes = 256;
 
-constexpr int32_t kSegAligned = 1;  // local and world starts are multiples of 8
+// A run whose flat-shard and buffer starts are both multiples of 8 elements
+// takes the vector paths.
+__host__ __device__ __forceinline__ bool seg_aligned(int64_t local, int64_t world) {
+  return ((local | world) & 7) == 0;
+}
 
 struct Seg {
-  int64_t local;  // first element in the flat shard arrays (rank slot included)
-  int64_t world;  // first element in the buffer
-  int32_t len;    // elements
-  int32_t tile0;  // first tile of this run in the launch
-  float decay;    // (float)(1 - lr*wd*wd_mult); K3 only
-  int32_t flags;
+  int64_t local;   // first element in the flat shard arrays (rank slot included)
+  int64_t world;   // first element in the buffer
+  int32_t len;     // elements
+  int32_t tile0;   // first tile of this run in the launch
+  double wd_mult;  // weight-decay multiplier of the run's param (K3)
 };
 static_assert(sizeof(Seg) == 32, "Seg layout");
 
@@ -105,6 +108,14 @@ static_assert(sizeof(Scalars) == 40, "dopt_step_stats layout");
 // kernel sets when it gives up waiting for its own copies; the finalize
 // pass reports it as dopt_step_stats.kernel_error and clears it.
 constexpr size_t kErrorFlagOffset = 128;
+// Byte offset of the step scalars the finalize pass computes when the step
+// number (and learning rate) live in device memory.
+constexpr size_t kDevStepOffset = 64;
+struct DevStep {
+  float step_size;  // (float)(lr / (1 - beta1^t))
+  float bc2_sqrt;   // (float)sqrt(1 - beta2^t)
+  double lr_wd;     // lr * weight_decay
+};
 constexpr int32_t kErrorMagic = 0x4B31544D;  // the flag's "set" value
 
 struct K1Params {
@@ -132,6 +143,8 @@ struct K3Params {
   void* param;        // the whole param buffer
   const float* coef;  // device scalar
   const int32_t* found_inf;
+  const DevStep* dev;  // step scalars from the finalize pass, or NULL: use the fields below
+  double lr_wd;        // lr * weight_decay (host step)
   float b1, b2, omb1, omb2, eps, step_size, bc2_sqrt;
   int32_t pad;
   SegTable tab;
@@ -379,7 +392,7 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
     const int n = (int)min((int64_t)kTile1, (int64_t)sg.len - off);
     const int64_t l0 = sg.local + off;
     const int64_t r0 = FULL ? sg.world + off : l0;
-    const bool aligned = (sg.flags & kSegAligned) != 0;
+    const bool aligned = seg_aligned(sg.local, sg.world);
 
     ReduceState st[kUnroll1][kVec];
     bool vec_ok[kUnroll1];
@@ -464,7 +477,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
     const int n = (int)min((int64_t)TILE, (int64_t)sg.len - off);
     const int64_t l0 = sg.local + off;
     const int64_t r0 = FULL ? sg.world + off : l0;
-    const bool aligned = (sg.flags & kSegAligned) != 0;
+    const bool aligned = seg_aligned(sg.local, sg.world);
 
     bool vec_ok[U];
 #pragma unroll
@@ -721,10 +734,31 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
 
 // ------------------------------------------------------------------- K2 --
 
+// The step number and learning rate of a step whose counter lives in device
+// memory: the finalize pass reads them, computes the step scalars for the
+// next step number and advances the counter only when the step is applied.
+struct K2Step {
+  int64_t* d_step;      // NULL: the host supplied the step scalars
+  const double* d_lr;   // NULL: lr below
+  double lr, wd, beta1, beta2;
+  DevStep* out;
+};
+
+// beta^t by binary powering in fp64 (the host computes it the same way).
+__host__ __device__ __forceinline__ double pow_int(double b, int64_t t) {
+  double r = 1.0, x = b;
+  while (t > 0) {
+    if (t & 1) r *= x;
+    x *= x;
+    t >>= 1;
+  }
+  return r;
+}
+
 __global__ void __launch_bounds__(kThreads)
 k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
             int remote_found_inf, double max_norm, Scalars* __restrict__ sc,
-            float* d_norm, float* d_coef, int32_t* d_found, int32_t* err_flag) {
+            float* d_norm, float* d_coef, int32_t* d_found, int32_t* err_flag, K2Step step) {
   __shared__ double s_sum[kThreads];
   __shared__ int s_bad[kThreads];
   __shared__ long long s_zero[kThreads];
@@ -773,6 +807,14 @@ k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
     if (d_norm) *d_norm = norm_f;
     if (d_coef) *d_coef = coef_f;
     if (d_found) *d_found = found;
+    if (step.d_step) {
+      const int64_t t = *step.d_step + 1;
+      const double lr = step.d_lr ? *step.d_lr : step.lr;
+      step.out->step_size = (float)(lr / (1.0 - pow_int(step.beta1, t)));
+      step.out->bc2_sqrt = (float)sqrt(1.0 - pow_int(step.beta2, t));
+      step.out->lr_wd = lr * step.wd;
+      if (!found) *step.d_step = t;  // a skipped step does not count
+    }
   }
 }
 
@@ -816,13 +858,29 @@ struct ParamT<float> {
 };
 
 // One element of AdamW, in the order of the reference arithmetic.
-__device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, float& w, float& m,
-                                       float& v) {
+// (float)(1 - lr*wd*wd_mult), in fp64 like the host reference; out of line so
+// no fp64 instruction is issued per element -- it runs once per run change.
+__device__ __noinline__ float decay_of(double lr_wd, double wd_mult) {
+  return (float)(1.0 - lr_wd * wd_mult);
+}
+
+struct StepScalars {
+  float step_size, bc2_sqrt;
+  double lr_wd;
+};
+
+__device__ __forceinline__ StepScalars step_scalars(const K3Params& p) {
+  if (p.dev) return StepScalars{p.dev->step_size, p.dev->bc2_sqrt, p.dev->lr_wd};
+  return StepScalars{p.step_size, p.bc2_sqrt, p.lr_wd};
+}
+
+__device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, const StepScalars& ss,
+                                       float& w, float& m, float& v) {
   float pp = __fmul_rn(w, decay);
   float mm = __fadd_rn(__fmul_rn(p.b1, m), __fmul_rn(p.omb1, g));
   float vv = __fadd_rn(__fmul_rn(p.b2, v), __fmul_rn(__fmul_rn(p.omb2, g), g));
-  float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(vv), p.bc2_sqrt), p.eps);
-  pp = __fsub_rn(pp, __fmul_rn(p.step_size, __fdiv_rn(mm, denom)));
+  float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(vv), ss.bc2_sqrt), p.eps);
+  pp = __fsub_rn(pp, __fmul_rn(ss.step_size, __fdiv_rn(mm, denom)));
   w = pp;
   m = mm;
   v = vv;
@@ -832,8 +890,10 @@ template <typename PT>
 __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw(const __grid_constant__ K3Params p) {
   if (*p.found_inf) return;  // skipped step: nothing is written
   const float c = *p.coef;
+  const StepScalars ss = step_scalars(p);
   float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
-  int si = 0;
+  int si = 0, decay_si = -1;
+  float decay = 1.f;
   for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
     si = seek(p.tab, si, t);
     const Seg& sg = p.tab.seg[si];
@@ -841,8 +901,11 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw(const _
     const int n = (int)min((int64_t)kTile3, (int64_t)sg.len - off);
     const int64_t l0 = sg.local + off, w0 = sg.world + off;
     const int64_t m0 = ParamT<PT>::kInPlace ? w0 : l0;  // master index
-    const bool aligned = (sg.flags & kSegAligned) != 0;
-    const float decay = sg.decay;
+    const bool aligned = seg_aligned(sg.local, sg.world);
+    if (si != decay_si) {
+      decay = decay_of(ss.lr_wd, sg.wd_mult);
+      decay_si = si;
+    }
 
     float g[kUnroll3][kVec], w[kUnroll3][kVec], m[kUnroll3][kVec], v[kUnroll3][kVec];
     bool vec_ok[kUnroll3];
@@ -866,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw(const _
       const int e = (u * kThreads + threadIdx.x) * kVec;
       if (vec_ok[u]) {
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[u][j], c), decay, p, w[u][j], m[u][j], v[u][j]);
+        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[u][j], c), decay, p, ss, w[u][j], m[u][j], v[u][j]);
         __stcs(reinterpret_cast<float4*>(wbase + m0 + e), make_float4(w[u][0], w[u][1], w[u][2], w[u][3]));
         __stcs(reinterpret_cast<float4*>(p.exp_avg + l0 + e), make_float4(m[u][0], m[u][1], m[u][2], m[u][3]));
         __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + l0 + e), make_float4(v[u][0], v[u][1], v[u][2], v[u][3]));
@@ -875,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw(const _
         const int cnt = min(kVec, n - e);
         for (int j = 0; j < cnt; ++j) {
           float ww = wbase[m0 + e + j], mm = p.exp_avg[l0 + e + j], vv = p.exp_avg_sq[l0 + e + j];
-          adamw1(__fmul_rn(p.main_grad[l0 + e + j], c), decay, p, ww, mm, vv);
+          adamw1(__fmul_rn(p.main_grad[l0 + e + j], c), decay, p, ss, ww, mm, vv);
           wbase[m0 + e + j] = ww;
           p.exp_avg[l0 + e + j] = mm;
           p.exp_avg_sq[l0 + e + j] = vv;
@@ -898,16 +961,21 @@ struct K3Tile {
 };
 
 template <typename PT>
-__device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, int& si, K3Tile& T) {
+__device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, int& si, K3Tile& T,
+                                        int& decay_si, float& decay, double lr_wd) {
   si = seek(p.tab, si, t);
   const Seg& sg = p.tab.seg[si];
+  if (si != decay_si) {
+    decay = decay_of(lr_wd, sg.wd_mult);
+    decay_si = si;
+  }
   const int64_t off = (int64_t)(t - sg.tile0) * kTile3;
   T.n = (int)min((int64_t)kTile3, (int64_t)sg.len - off);
   T.l0 = sg.local + off;
   T.w0 = sg.world + off;
   T.m0 = ParamT<PT>::kInPlace ? T.w0 : T.l0;
-  T.aligned = (sg.flags & kSegAligned) != 0;
-  T.decay = sg.decay;
+  T.aligned = seg_aligned(sg.local, sg.world);
+  T.decay = decay;
 #pragma unroll
   for (int u = 0; u < kUnroll3; ++u) {
     const int e = (u * kThreads + threadIdx.x) * kVec;
@@ -924,16 +992,18 @@ template <typename PT>
 __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(const __grid_constant__ K3Params p) {
   if (*p.found_inf) return;  // skipped step: nothing is written
   const float c = *p.coef;
+  const StepScalars ss = step_scalars(p);
   float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
-  int si = 0;
+  int si = 0, decay_si = -1;
+  float decay = 1.f;
   int t = blockIdx.x;
   if (t >= p.tab.n_tiles) return;
   K3Tile cur;
-  k3_load<PT>(p, wbase, t, si, cur);
+  k3_load<PT>(p, wbase, t, si, cur, decay_si, decay, ss.lr_wd);
   for (; t < p.tab.n_tiles; t += gridDim.x) {
     K3Tile nxt;
     const bool more = t + (int)gridDim.x < p.tab.n_tiles;
-    if (more) k3_load<PT>(p, wbase, t + gridDim.x, si, nxt);
+    if (more) k3_load<PT>(p, wbase, t + gridDim.x, si, nxt, decay_si, decay, ss.lr_wd);
 #pragma unroll
     for (int u = 0; u < kUnroll3; ++u) {
       const int e = (u * kThreads + threadIdx.x) * kVec;
@@ -943,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
         float m[kVec] = {cur.m[u].x, cur.m[u].y, cur.m[u].z, cur.m[u].w};
         float v[kVec] = {cur.v[u].x, cur.v[u].y, cur.v[u].z, cur.v[u].w};
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[j], c), cur.decay, p, w[j], m[j], v[j]);
+        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[j], c), cur.decay, p, ss, w[j], m[j], v[j]);
         __stcs(reinterpret_cast<float4*>(wbase + cur.m0 + e), make_float4(w[0], w[1], w[2], w[3]));
         __stcs(reinterpret_cast<float4*>(p.exp_avg + cur.l0 + e), make_float4(m[0], m[1], m[2], m[3]));
         __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + cur.l0 + e), make_float4(v[0], v[1], v[2], v[3]));
@@ -952,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
         const int cnt = min(kVec, cur.n - e);
         for (int j = 0; j < cnt; ++j) {
           float ww = wbase[cur.m0 + e + j], mm = p.exp_avg[cur.l0 + e + j], vv = p.exp_avg_sq[cur.l0 + e + j];
-          adamw1(__fmul_rn(p.main_grad[cur.l0 + e + j], c), cur.decay, p, ww, mm, vv);
+          adamw1(__fmul_rn(p.main_grad[cur.l0 + e + j], c), cur.decay, p, ss, ww, mm, vv);
           wbase[cur.m0 + e + j] = ww;
           p.exp_avg[cur.l0 + e + j] = mm;
           p.exp_avg_sq[cur.l0 + e + j] = vv;
@@ -991,9 +1061,8 @@ std::vector<Chunk> chunks_of(const std::vector<dopt::Run>& runs) {
 }
 
 // Fills the kernel-parameter table of one chunk for tiles of `tile`
-// elements; decay (K3 only) from lr and wd.
-void fill_table(SegTable& tab, const std::vector<dopt::Run>& runs, const Chunk& c, int tile_elems,
-                double lr, double wd) {
+// elements.
+void fill_table(SegTable& tab, const std::vector<dopt::Run>& runs, const Chunk& c, int tile_elems) {
   tab.n_seg = c.count;
   int tile = 0;
   for (int k = 0; k < c.count; ++k) {
@@ -1003,8 +1072,7 @@ void fill_table(SegTable& tab, const std::vector<dopt::Run>& runs, const Chunk& 
     s.world = r.world;
     s.len = (int32_t)r.len;
     s.tile0 = tile;
-    s.decay = (float)(1.0 - lr * wd * r.wd_mult);
-    s.flags = ((r.local % 8) == 0 && (r.world % 8) == 0) ? kSegAligned : 0;
+    s.wd_mult = r.wd_mult;
     tile += (int)((r.len + tile_elems - 1) / tile_elems);
   }
   tab.n_tiles = tile;
@@ -1119,9 +1187,19 @@ template <typename GT, bool FULL, bool STATS, int DPI>
 int launch_k1_tma(K1Params& kp, int n_tiles, cudaStream_t s) {
   auto kern = k1_reduce_prepare_tma<GT, FULL, STATS, DPI>;
   const size_t smem = tma_smem_bytes<GT, DPI>();
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess)
-    return dopt::fail(DOPT_E_CUDA, std::string("k1 tma smem attribute: ") + cudaGetErrorString(e));
+  // the dynamic shared-memory limit is raised once per device (a later call,
+  // e.g. inside a stream capture, then issues nothing but the launch)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (!bit || !(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+      return dopt::fail(DOPT_E_CUDA, std::string("k1 tma smem attribute: ") + cudaGetErrorString(e));
+    attr_set.fetch_or(bit);
+  }
   int sms = 0, per_sm = 0;
   int st = device_sms(&sms);
   if (st) return st;
@@ -1225,7 +1303,7 @@ int run_k1_runs(const std::vector<dopt::Run>& runs, int region_first, const void
     kp.use_tma = (DOPT_K1_TMA && stats && ws && all_aligned && n_inst == 1 && !average &&
                   gdt == DOPT_F32 && (dpi == 1 || dpi == 2 || dpi == 4 || dpi == 8)) ? 1 : 0;
     kp.starve_tile = g_starve_tile.load(std::memory_order_relaxed);
-    fill_table(kp.tab, runs, c, kp.use_tma ? kTmaTile : k1_tile(gdt, n_rep, n_inst, average), 0.0, 0.0);
+    fill_table(kp.tab, runs, c, kp.use_tma ? kTmaTile : k1_tile(gdt, n_rep, n_inst, average));
     const int n_tiles = kp.tab.n_tiles;
     int st;
     if (stats)
@@ -1253,18 +1331,34 @@ int run_k1(dopt_shard_map* m, int32_t buffer, int32_t rank, const void* const* r
 // scale_gradients factor of a step: 0 (unset) means 1.
 float grad_scale_of(const dopt_step_args* a) { return a->grad_scale == 0.0f ? 1.0f : a->grad_scale; }
 
+DevStep* dev_step_ptr(void* ws) {
+  return reinterpret_cast<DevStep*>(static_cast<char*>(ws) + kDevStepOffset);
+}
+
 int run_k2_slots(int n_slots, void* ws, double remote_sumsq, int32_t remote_found, double max_norm,
-                 float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
+                 float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s,
+                 const dopt_step_args* a = nullptr) {
+  K2Step step{nullptr, nullptr, 0.0, 0.0, 0.0, 0.0, dev_step_ptr(ws)};
+  if (a && a->d_step) {
+    step.d_step = a->d_step;
+    step.d_lr = a->d_lr;
+    step.lr = a->hp.lr;
+    step.wd = a->hp.weight_decay;
+    step.beta1 = a->hp.beta1;
+    step.beta2 = a->hp.beta2;
+  }
   k2_finalize<<<1, kThreads, 0, s>>>(region_ptr(ws, 0), n_slots, remote_sumsq, remote_found ? 1 : 0,
                                      max_norm, scalars_ptr(ws), d_norm, d_coef, d_found,
-                                     reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset));
+                                     reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset),
+                                     step);
   return check_launch("k2_finalize launch");
 }
 
 int run_k2(dopt_shard_map* m, int32_t rank, void* ws, double remote_sumsq, int32_t remote_found,
-           double max_norm, float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s) {
+           double max_norm, float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s,
+           const dopt_step_args* a = nullptr) {
   return run_k2_slots(total_regions(m, rank) * kMaxGrid, ws, remote_sumsq, remote_found, max_norm,
-                      d_norm, d_coef, d_found, s);
+                      d_norm, d_coef, d_found, s, a);
 }
 
 int check_hparams(const dopt_adamw_hparams* hp, const char* fn) {
@@ -1276,16 +1370,6 @@ int check_hparams(const dopt_adamw_hparams* hp, const char* fn) {
   return DOPT_OK;
 }
 
-// beta^t by binary powering in double.
-double pow_int(double b, int64_t t) {
-  double r = 1.0, x = b;
-  while (t > 0) {
-    if (t & 1) r *= x;
-    x *= x;
-    t >>= 1;
-  }
-  return r;
-}
 
 template <typename PT>
 int launch_k3_t(K3Params& kp, int n_tiles, cudaStream_t s) {
@@ -1299,7 +1383,8 @@ int launch_k3_t(K3Params& kp, int n_tiles, cudaStream_t s) {
 
 int run_k3_runs(const std::vector<dopt::Run>& runs, int32_t pdt, const float* main_grad, float* master,
                 float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
-                const float* d_coef, const int32_t* d_found, cudaStream_t s) {
+                const float* d_coef, const int32_t* d_found, cudaStream_t s,
+                const DevStep* dev = nullptr) {
   std::vector<Chunk> chunks = chunks_of(runs);
   for (const Chunk& c : chunks) {
     K3Params& kp = k3_scratch();
@@ -1310,6 +1395,8 @@ int run_k3_runs(const std::vector<dopt::Run>& runs, int32_t pdt, const float* ma
     kp.param = param;
     kp.coef = d_coef;
     kp.found_inf = d_found;
+    kp.dev = dev;
+    kp.lr_wd = hp->lr * hp->weight_decay;
     kp.b1 = (float)hp->beta1;
     kp.b2 = (float)hp->beta2;
     kp.omb1 = (float)(1.0 - hp->beta1);
@@ -1318,7 +1405,7 @@ int run_k3_runs(const std::vector<dopt::Run>& runs, int32_t pdt, const float* ma
     kp.step_size = (float)(hp->lr / (1.0 - pow_int(hp->beta1, hp->step)));
     kp.bc2_sqrt = (float)std::sqrt(1.0 - pow_int(hp->beta2, hp->step));
     kp.pad = 0;
-    fill_table(kp.tab, runs, c, kTile3, hp->lr, hp->weight_decay);
+    fill_table(kp.tab, runs, c, kTile3);
     const int n_tiles = kp.tab.n_tiles;
     int st;
     switch (pdt) {
@@ -1333,9 +1420,9 @@ int run_k3_runs(const std::vector<dopt::Run>& runs, int32_t pdt, const float* ma
 
 int run_k3(dopt_shard_map* m, int32_t buffer, int32_t rank, const float* main_grad, float* master,
            float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
-           const float* d_coef, const int32_t* d_found, cudaStream_t s) {
+           const float* d_coef, const int32_t* d_found, cudaStream_t s, const DevStep* dev = nullptr) {
   return run_k3_runs(dopt::runs_for(m, buffer, rank), m->buffers[buffer].param_dtype, main_grad, master,
-                     exp_avg, exp_avg_sq, param, hp, d_coef, d_found, s);
+                     exp_avg, exp_avg_sq, param, hp, d_coef, d_found, s, dev);
 }
 
 // ---- bucket-staged step: one partial region per (buffer, bucket, chunk) --
@@ -1418,6 +1505,9 @@ int check_step_args(const dopt_step_args* a, bool bucketed, const char* fn) {
     return st;
   }
   if ((st = check_hparams(&a->hp, fn))) return st;
+  if ((a->d_step && (reinterpret_cast<uintptr_t>(a->d_step) & 7)) ||
+      (a->d_lr && (reinterpret_cast<uintptr_t>(a->d_lr) & 7)))
+    return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": d_step / d_lr not 8-byte aligned");
   if (!a->replica_grads || !a->main_grad || !a->master || !a->exp_avg || !a->exp_avg_sq || !a->param_buffer)
     return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL per-buffer array");
   if (!std::isfinite(a->inv_loss_scale) || !(a->remote_sumsq >= 0) || std::isnan(a->max_norm) ||
@@ -1564,12 +1654,13 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
   if ((st = record_stage(a, 1, s))) return st;
   Scalars* sc = scalars_ptr(a->workspace);
   if ((st = run_k2(m, a->rank, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm, d_norm,
-                   nullptr, d_found_inf, s)))
+                   nullptr, d_found_inf, s, a)))
     return st;
   if ((st = record_stage(a, 2, s))) return st;
+  const DevStep* dev = a->d_step ? dev_step_ptr(a->workspace) : nullptr;
   for (int32_t b = 0; b < nb; ++b) {
     st = run_k3(m, b, a->rank, a->main_grad[b], a->master[b], a->exp_avg[b], a->exp_avg_sq[b],
-                a->param_buffer[b], &a->hp, &sc->clip_coef, &sc->found_inf, s);
+                a->param_buffer[b], &a->hp, &sc->clip_coef, &sc->found_inf, s, dev);
     if (st) return st;
   }
   return record_stage(a, 3, s);
@@ -1609,7 +1700,7 @@ int dopt_step_finalize(const dopt_step_args* a, int32_t* d_found_inf, float* d_n
   dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
   const int n_slots = bucketed_region(m, a->rank, (int32_t)m->buffers.size(), 0) * kMaxGrid;
   return run_k2_slots(n_slots, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm, d_norm,
-                      nullptr, d_found_inf, (cudaStream_t)a->stream);
+                      nullptr, d_found_inf, (cudaStream_t)a->stream, a);
 }
 
 int dopt_step_update_buckets(const dopt_step_args* a, int32_t buffer, int32_t bucket_first,
@@ -1626,7 +1717,8 @@ int dopt_step_update_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
   Scalars* sc = scalars_ptr(a->workspace);
   return run_k3_runs(runs, m->buffers[buffer].param_dtype, a->main_grad[buffer], a->master[buffer],
                      a->exp_avg[buffer], a->exp_avg_sq[buffer], a->param_buffer[buffer], &a->hp, &sc->clip_coef,
-                     &sc->found_inf, (cudaStream_t)a->stream);
+                     &sc->found_inf, (cudaStream_t)a->stream,
+                     a->d_step ? dev_step_ptr(a->workspace) : nullptr);
 }
 
 namespace {
