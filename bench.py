@@ -59,6 +59,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--graph", action="store_true",
+                   help="time the step replayed from a CUDA graph (device step counter) "
+                        "against dopt_step calls")
     p.add_argument("--staged", action="store_true",
                    help="time the bucket-staged step against the fused step, with the grads "
                         "produced bucket by bucket by a stand-in for the backward pass")
@@ -639,12 +642,60 @@ def run_staged(args):
     return 0
 
 
+def run_graph(args):
+    """The fused step three ways: dopt_step calls (each waits for found_inf),
+    dopt_step_async calls back to back, and one CUDA-graph replay per step
+    (step counter in device memory, no host work between steps)."""
+    import torch
+    import mixed_precision_adam_gb300 as D
+    cfg = workload_config(args.workload, args.layers)
+    wl = Workload(cfg)
+    sargs = wl.args()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    t_sync = timed(lambda: wl.step(sargs))
+    t_async = timed(lambda: D.dopt_step_async(sargs))
+    d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    gargs = wl.args()
+    gargs.set_device_step(d_step)
+    D.dopt_step_async(gargs)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        gargs.set_stream(s)
+        with torch.cuda.graph(graph, stream=s):
+            D.dopt_step_async(gargs)
+    torch.cuda.synchronize()
+    t_graph = timed(graph.replay)
+    line = {"metric": "fused step latency: dopt_step vs async vs CUDA-graph replay (ms per step)",
+            "workload": describe(cfg, wl.elements), "steps": args.steps, "warmup": args.warmup,
+            "dopt_step_ms": t_sync, "dopt_step_async_ms": t_async, "graph_replay_ms": t_graph,
+            "elements_per_step": wl.elements}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.staged:
         return run_staged(args)
+    if args.graph:
+        return run_graph(args)
     return run_ours(args)
 
 
