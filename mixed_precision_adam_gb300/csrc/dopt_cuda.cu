@@ -45,9 +45,6 @@ namespace {
 #ifndef DOPT_K3_UNROLL
 #define DOPT_K3_UNROLL 1
 #endif
-#ifndef DOPT_K3_PIPE
-#define DOPT_K3_PIPE 1  // 1: the AdamW pass loads the next tile before computing this one
-#endif
 #ifndef DOPT_K1_TMA
 #define DOPT_K1_TMA 1  // 1: single-instance reduce stages replica tiles through shared memory with TMA
 #endif
@@ -857,9 +854,9 @@ struct ParamT<float> {
   static __device__ __forceinline__ void store1(void*, int64_t, float) {}
 };
 
-// One element of AdamW, in the order of the reference arithmetic.
-// (float)(1 - lr*wd*wd_mult), in fp64 like the host reference; out of line so
-// no fp64 instruction is issued per element -- it runs once per run change.
+// The decoupled weight-decay factor (float)(1 - lr*wd*wd_mult), formed in
+// fp64; out of line so no fp64 instruction is issued per element -- it runs
+// once per run change.
 __device__ __noinline__ float decay_of(double lr_wd, double wd_mult) {
   return (float)(1.0 - lr_wd * wd_mult);
 }
@@ -874,6 +871,9 @@ __device__ __forceinline__ StepScalars step_scalars(const K3Params& p) {
   return StepScalars{p.step_size, p.bc2_sqrt, p.lr_wd};
 }
 
+// One element of AdamW (torch semantics: decay the weight, update m and v,
+// divide the bias-corrected sqrt(v) + eps into m, step), each operation
+// rounded once in fp32.
 __device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, const StepScalars& ss,
                                        float& w, float& m, float& v) {
   float pp = __fmul_rn(w, decay);
@@ -884,69 +884,6 @@ __device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, 
   w = pp;
   m = mm;
   v = vv;
-}
-
-template <typename PT>
-__global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw(const __grid_constant__ K3Params p) {
-  if (*p.found_inf) return;  // skipped step: nothing is written
-  const float c = *p.coef;
-  const StepScalars ss = step_scalars(p);
-  float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
-  int si = 0, decay_si = -1;
-  float decay = 1.f;
-  for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
-    si = seek(p.tab, si, t);
-    const Seg& sg = p.tab.seg[si];
-    const int64_t off = (int64_t)(t - sg.tile0) * kTile3;
-    const int n = (int)min((int64_t)kTile3, (int64_t)sg.len - off);
-    const int64_t l0 = sg.local + off, w0 = sg.world + off;
-    const int64_t m0 = ParamT<PT>::kInPlace ? w0 : l0;  // master index
-    const bool aligned = seg_aligned(sg.local, sg.world);
-    if (si != decay_si) {
-      decay = decay_of(ss.lr_wd, sg.wd_mult);
-      decay_si = si;
-    }
-
-    float g[kUnroll3][kVec], w[kUnroll3][kVec], m[kUnroll3][kVec], v[kUnroll3][kVec];
-    bool vec_ok[kUnroll3];
-#pragma unroll
-    for (int u = 0; u < kUnroll3; ++u) {
-      const int e = (u * kThreads + threadIdx.x) * kVec;
-      vec_ok[u] = aligned && e + kVec <= n;
-      if (vec_ok[u]) {
-        float4 a = __ldcs(reinterpret_cast<const float4*>(p.main_grad + l0 + e));
-        float4 b = __ldcs(reinterpret_cast<const float4*>(wbase + m0 + e));
-        float4 cc = __ldcs(reinterpret_cast<const float4*>(p.exp_avg + l0 + e));
-        float4 d = __ldcs(reinterpret_cast<const float4*>(p.exp_avg_sq + l0 + e));
-        g[u][0] = a.x; g[u][1] = a.y; g[u][2] = a.z; g[u][3] = a.w;
-        w[u][0] = b.x; w[u][1] = b.y; w[u][2] = b.z; w[u][3] = b.w;
-        m[u][0] = cc.x; m[u][1] = cc.y; m[u][2] = cc.z; m[u][3] = cc.w;
-        v[u][0] = d.x; v[u][1] = d.y; v[u][2] = d.z; v[u][3] = d.w;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll3; ++u) {
-      const int e = (u * kThreads + threadIdx.x) * kVec;
-      if (vec_ok[u]) {
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[u][j], c), decay, p, ss, w[u][j], m[u][j], v[u][j]);
-        __stcs(reinterpret_cast<float4*>(wbase + m0 + e), make_float4(w[u][0], w[u][1], w[u][2], w[u][3]));
-        __stcs(reinterpret_cast<float4*>(p.exp_avg + l0 + e), make_float4(m[u][0], m[u][1], m[u][2], m[u][3]));
-        __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + l0 + e), make_float4(v[u][0], v[u][1], v[u][2], v[u][3]));
-        ParamT<PT>::store4(p.param, w0 + e, w[u]);
-      } else if (e < n) {
-        const int cnt = min(kVec, n - e);
-        for (int j = 0; j < cnt; ++j) {
-          float ww = wbase[m0 + e + j], mm = p.exp_avg[l0 + e + j], vv = p.exp_avg_sq[l0 + e + j];
-          adamw1(__fmul_rn(p.main_grad[l0 + e + j], c), decay, p, ss, ww, mm, vv);
-          wbase[m0 + e + j] = ww;
-          p.exp_avg[l0 + e + j] = mm;
-          p.exp_avg_sq[l0 + e + j] = vv;
-          ParamT<PT>::store1(p.param, w0 + e + j, ww);
-        }
-      }
-    }
-  }
 }
 
 // The AdamW pass with the loads of a thread's next tile issued before the
@@ -1373,7 +1310,7 @@ int check_hparams(const dopt_adamw_hparams* hp, const char* fn) {
 
 template <typename PT>
 int launch_k3_t(K3Params& kp, int n_tiles, cudaStream_t s) {
-  auto kern = DOPT_K3_PIPE ? k3_adamw_pipe<PT> : k3_adamw<PT>;
+  auto kern = k3_adamw_pipe<PT>;
   int grid = 0;
   int st = grid_for(kern, n_tiles, &grid);
   if (st) return st;
