@@ -43,6 +43,8 @@ def lib():
                              ctypes.c_float, ctypes.c_double)
         L.or_reduce_prepare_run.argtypes = [ctypes.POINTER(P), I32, I32, I32, I32, I64, I64, F, F, P]
         L.or_reduce_prepare_run.restype = I64
+        L.or_grad_amax_run.argtypes = [P, I32, I64, I64]
+        L.or_grad_amax_run.restype = D
         L.or_sumsq_run.argtypes = [P, I64]
         L.or_sumsq_run.restype = D
         L.or_clip_coef.argtypes = [D, D, ctypes.POINTER(D), ctypes.POINTER(D)]
@@ -105,9 +107,24 @@ def reduce_prepare(replicas, gdt, index0, length, inv_scale, n_inst=1, average=F
     return out, bad
 
 
+def grad_amax_run(rep, gdt, index0, length):
+    """The pre-reduction grad check over a run of one replica (see
+    or_grad_amax_run): NaN if the run holds a NaN, else the largest |g|."""
+    return lib().or_grad_amax_run(_ptr(rep), gdt, index0, length)
+
+
+def bucket_number(smap, bi, b):
+    """Number of bucket b of buffer bi among all buffers' buckets."""
+    return sum(len(buf.buckets) for buf in smap.buffers[:bi]) + b
+
+
+def _amax_merge(a, b):
+    return float("nan") if (a != a or b != b) else max(a, b)
+
+
 def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.0,
          layout="full", n_inst=1, average=False, remote_sumsq=0.0,
-         remote_found_inf=False, grad_scale=1.0):
+         remote_found_inf=False, grad_scale=1.0, check_grads=False):
     """One optimizer step over the shards of `ranks` in every buffer of `smap`.
 
     grads[bi]  : list of n_rep replica arrays for buffer bi, in its grad dtype
@@ -122,6 +139,10 @@ def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.
     hp         : dict lr, beta1, beta2, eps, weight_decay.
     t          : the step number used for bias correction if not skipped.
     grad_scale : scale_gradients factor applied to the reduced grads (1 = none).
+    check_grads: also return grad_amax, the pre-reduction check of every
+                 replica: an (n_rep, total buckets) float64 array holding, per
+                 replica and bucket, the largest |g| among the elements the
+                 step reads (NaN if one is NaN; 0 when it reads none).
     Arrays in state and params are updated in place.  Returns a dict with
     found_inf, norm (NaN when skipped), coef, clip, main (per buffer),
     sumsq and num_zeros (main grads equal to zero, Megatron's count_zeros).
@@ -133,6 +154,7 @@ def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.
     bad = 0
     zeros = 0
     pieces = []
+    amax = np.zeros((n_rep, bucket_number(smap, len(smap.buffers), 0)))
     for bi, buf in enumerate(smap.buffers):
         S = smap.shard_numel(bi)
         main = np.zeros(len(ranks) * S, dtype=np.float32)
@@ -149,6 +171,11 @@ def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.
                 if k < 0:
                     raise ValueError("invalid replica / instance counts")
                 bad += k
+                if check_grads:
+                    col = bucket_number(smap, bi, b)
+                    for q in range(n_rep):
+                        amax[q, col] = _amax_merge(amax[q, col],
+                                                   L.or_grad_amax_run(_ptr(reps[q]), buf.grad_dtype, rep0, n))
                 sumsq += L.or_sumsq_run(_ptr(main, local), n)
                 zeros += int(np.count_nonzero(main[local:local + n] == 0))
                 pieces.append((bi, pid, local, v))
@@ -156,6 +183,8 @@ def step(smap, ranks, grads, state, params, hp, t, *, inv_scale=1.0, max_norm=1.
     sumsq += remote_sumsq
     found = bad > 0 or bool(remote_found_inf)
     result = {"found_inf": found, "main": mains, "sumsq": sumsq, "num_zeros": zeros}
+    if check_grads:
+        result["grad_amax"] = amax
     if found:
         result.update(norm=float("nan"), coef=1.0, clip=False)
         return result

@@ -208,6 +208,28 @@ int64_t or_reduce_prepare_run(const void* const* rep, int32_t n_rep, int32_t n_i
   return bad;
 }
 
+/*
+ * A2 check (check_for_nan_in_grad / check_for_large_grads): the Megatron
+ * distributed-package page, section 2.4 (the bucket groups' check_grads
+ * method looks at every bucket's gradients for NaN, Inf and unusually large
+ * values before the communication) and the options table of section 3.2.
+ * The pages give no threshold for "large"; the reading taken is the largest
+ * magnitude, which a caller compares with its own threshold.  Over a run of
+ * one replica's gradients as stored (grad dtype gdt, indices index0 ..
+ * index0 + len - 1): returns NaN when the run holds a NaN, else the largest
+ * |g| (+inf when it holds an infinity), 0 for an empty run.
+ */
+double or_grad_amax_run(const void* rep, int32_t gdt, int64_t index0, int64_t len) {
+  double m = 0.0;
+  for (int64_t j = 0; j < len; ++j) {
+    double x = (double)or_widen(rep, gdt, index0 + j);
+    if (x != x) return NAN;
+    if (x < 0) x = -x;
+    if (x > m) m = x;
+  }
+  return m;
+}
+
 /* A4: sum of squares of a run of main grads, in fp64, in index order. */
 double or_sumsq_run(const float* main_grad, int64_t len) {
   double s = 0.0;

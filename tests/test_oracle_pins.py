@@ -449,6 +449,107 @@ def test_inf_anywhere_in_params_skips_but_padding_does_not():
             assert res["found_inf"] == bool(owned[bi][w]), (bi, w)
 
 
+# --------------------------------------------------------------------------
+# A2 check: largest |g| per replica and bucket before the reduction
+
+
+def test_grad_amax_run_hand_values():
+    """Values fixed by the IEEE / bfloat16 formats: the largest magnitude,
+    +inf over any finite value, NaN over everything, 0 for nothing read."""
+    f = lambda xs: np.array(xs, np.float32)
+    u = lambda xs: np.array(xs, np.uint16)
+    amax = oracle.grad_amax_run
+    assert amax(f([1.0, -3.5, 2.0, 0.0]), F32, 0, 4) == 3.5
+    assert amax(f([-0.0, 0.0]), F32, 0, 2) == 0.0
+    assert amax(f([9.0]), F32, 0, 0) == 0.0
+    assert amax(f([100.0, 1.0, 2.0, -7.0, 50.0]), F32, 1, 3) == 7.0  # index0 and length
+    assert amax(f([1.0, np.inf]), F32, 0, 2) == math.inf
+    assert amax(f([-np.inf, 5.0]), F32, 0, 2) == math.inf
+    assert math.isnan(amax(f([np.nan, np.inf, 1.0]), F32, 0, 3))
+    assert math.isnan(amax(f([1.0, -np.nan]), F32, 0, 2))
+    assert amax(f([3.4028235e38, -1.0]), F32, 0, 2) == 3.4028234663852886e38
+    # bf16: 0xC0A0 = -5, 0x3F80 = 1, 0x0001 = 2^-133 (smallest subnormal)
+    assert amax(u([0x3F80, 0xC0A0]), BF16, 0, 2) == 5.0
+    assert amax(u([0x0001, 0x8000]), BF16, 0, 2) == 2.0 ** -133
+    assert amax(u([0xFF80, 0x3F80]), BF16, 0, 2) == math.inf
+    assert math.isnan(amax(u([0x7FC0, 0x7F80]), BF16, 0, 2))
+    # fp16: 0xBC00 = -1, 0x4500 = 5, 0x7BFF = 65504, 0x7C00 / 0xFC00 = +-inf, 0x7E00 NaN
+    assert amax(u([0xBC00, 0x4500]), F16, 0, 2) == 5.0
+    assert amax(u([0x7BFF, 0xFBFF]), F16, 0, 2) == 65504.0
+    assert amax(u([0x0001]), F16, 0, 1) == 2.0 ** -24
+    assert amax(u([0xFC00, 0x0000]), F16, 0, 2) == math.inf
+    assert math.isnan(amax(u([0x7C00, 0x7E00]), F16, 0, 2))
+
+
+def test_grad_check_constant_replicas_fill_every_read_bucket():
+    """Replica q holding the constant -(q + 1) everywhere: every bucket the
+    step reads shows q + 1 for replica q; a bucket holding none of the
+    selected rank's elements shows 0."""
+    params = [dict(numel=n, dtype=d)
+              for n, d in [(700, BF16), (5, F32), (1300, BF16), (33, F32), (90, BF16), (450, BF16)]]
+    m = oracle.ShardMap(params, 4, 400, True)
+    empty_seen = False
+    for ranks in ([0, 1, 2, 3], [2], [3]):
+        grads, st, pb = [], [], []
+        for bi, buf in enumerate(m.buffers):
+            grads.append([np.full(buf.numel, -(q + 1.0), np.float32) for q in range(4)])
+            n_local = len(ranks) * m.shard_numel(bi)
+            st.append({"exp_avg": np.zeros(n_local, np.float32), "exp_avg_sq": np.zeros(n_local, np.float32),
+                       **({"master": np.zeros(n_local, np.float32)} if buf.param_dtype != F32 else {})})
+            pb.append(np.zeros(buf.numel, np.uint16 if buf.param_dtype != F32 else np.float32))
+        res = oracle.step(m, ranks, grads, st, pb, W.HP, 1, check_grads=True)
+        amax = res["grad_amax"]
+        total = sum(len(b.buckets) for b in m.buffers)
+        assert amax.shape == (4, total) and total == 4
+        col = 0
+        for bi, buf in enumerate(m.buffers):
+            for b, bucket in enumerate(buf.buckets):
+                read = any(m.rank_views(bi, b, r) for r in ranks)
+                empty_seen |= not read
+                for q in range(4):
+                    assert amax[q, col] == ((q + 1.0) if read else 0.0), (ranks, bi, b, q)
+                col += 1
+    assert empty_seen  # rank 3's slice of the fp32 bucket is all padding
+
+def test_grad_check_locates_each_planted_value():
+    """Brute force over a tiny two-buffer map with padding: a large value
+    planted at one element of one replica shows up at exactly (that replica,
+    the element's bucket) when the element belongs to a param of a selected
+    rank's shard, and nowhere when it sits in padding or in another rank's
+    shard.  The element's bucket is found here from the bucket offsets."""
+    params = [dict(numel=n, dtype=d) for n, d in [(70, BF16), (5, F32), (130, BF16), (33, F32)]]
+    m = oracle.ShardMap(params, 4, 100, True)
+    base = 0.25
+    offsets = [0]
+    for buf in m.buffers:
+        offsets.append(offsets[-1] + len(buf.buckets))
+    for ranks in ([0, 1, 2, 3], [1]):
+        for bi, buf in enumerate(m.buffers):
+            owned = np.zeros(buf.numel, bool)
+            for pid in buf.params:
+                s0, e0, _ = buf.index[pid]
+                owned[s0:e0] = True
+            for w in range(0, buf.numel, 3):
+                b = next(k for k, bk in enumerate(buf.buckets) if bk.offset <= w < bk.offset + bk.numel)
+                slice_rank = (w - buf.buckets[b].offset) // (buf.buckets[b].numel // 4)
+                seen = bool(owned[w]) and slice_rank in ranks
+                q = w % 4
+                grads = [[np.full(bb.numel, base, np.float32) for _ in range(4)] for bb in m.buffers]
+                grads[bi][q][w] = -1.0e3
+                st = [{"exp_avg": np.zeros(len(ranks) * m.shard_numel(i), np.float32),
+                       "exp_avg_sq": np.zeros(len(ranks) * m.shard_numel(i), np.float32),
+                       **({"master": np.zeros(len(ranks) * m.shard_numel(i), np.float32)}
+                          if bb.param_dtype != F32 else {})} for i, bb in enumerate(m.buffers)]
+                pb = [np.zeros(bb.numel, np.uint16 if bb.param_dtype != F32 else np.float32) for bb in m.buffers]
+                amax = oracle.step(m, ranks, grads, st, pb, W.HP, 1, check_grads=True)["grad_amax"]
+                hit = np.argwhere(amax == 1.0e3)
+                if seen:
+                    assert hit.tolist() == [[q, offsets[bi] + b]], (ranks, bi, w)
+                else:
+                    assert len(hit) == 0, (ranks, bi, w)
+                assert set(np.unique(amax[amax != 1.0e3])) <= {0.0, base}
+
+
 def test_stream_sumsq_equals_array_path():
     n_rep = 8
     keys = [synth.key(3, synth.STREAM_GRAD, 1, k) for k in range(n_rep)]
