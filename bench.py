@@ -57,6 +57,8 @@ def parse_args(argv=None):
     p.add_argument("--layers", type=int, default=None,
                    help="override the layer count (a smaller case of the same kernels)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--check-grads", action="store_true",
+                   help="turn on the pre-reduction grad check (largest |g| per replica and bucket)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--graph", action="store_true",
@@ -285,6 +287,18 @@ def measured_peak_hbm():
         return 6800.0, "fallback"
 
 
+K1_SOURCES = ("kernels.cuh", "k1.cuh", "k1_f32.cu")
+
+
+def k1_source_sha256():
+    """sha256 over the sources of the fp32 reduce/prepare kernel, in order."""
+    h = hashlib.sha256()
+    for f in K1_SOURCES:
+        with open(os.path.join(ROOT, "mixed_precision_adam_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def recorded_traffic(elements_k1):
     """DRAM traffic of the reduce/prepare pass from the committed ncu summary,
     scaled to this launch's elements; None when the kernel source changed
@@ -294,8 +308,7 @@ def recorded_traffic(elements_k1):
         rec = json.load(open(path))
     except (OSError, ValueError):
         return None
-    src = open(os.path.join(ROOT, "mixed_precision_adam_gb300", "csrc", "dopt_cuda.cu"), "rb").read()
-    if hashlib.sha256(src).hexdigest() != rec.get("source_sha256"):
+    if k1_source_sha256() != rec.get("source_sha256"):
         return None
     return rec["dram_bytes_per_element"] * elements_k1
 
@@ -443,6 +456,9 @@ def run_ours(args):
     wl = Workload(cfg)
     log(f"[bench] rank {rank}: {wl.elements} elements per step, workspace {wl.ws_bytes} B")
     sargs = wl.args()
+    if args.check_grads:
+        amax = torch.zeros((wl.n_rep, D.dopt_total_buckets(wl.pm)), dtype=torch.float32, device="cuda")
+        sargs.set_grad_check(amax)
     for _ in range(args.warmup):
         wl.step(sargs)
     torch.cuda.synchronize()
@@ -540,7 +556,8 @@ def run_ours(args):
                    "replicas": wl.n_rep,
                    "l2": "no flush needed: inputs larger than L2 (the replica grads alone are "
                          f"{wl.elements * wl.n_rep * 4 / 1e9:.1f} GB per step)",
-                   "parallelism": "replicas only: each GPU runs its own emulated DP instance"},
+                   "parallelism": "replicas only: each GPU runs its own emulated DP instance",
+                   "grad_check": bool(args.check_grads)},
         "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s",
                      "frac": k1_gbs / peak, "traffic": traffic, "kernel": "k1_reduce_prepare",

@@ -167,6 +167,12 @@ int dopt_param_index(const dopt_shard_map* map, int32_t param, int32_t* buffer,
  */
 int dopt_rank_shards(const dopt_shard_map* map, int32_t buffer, int32_t rank,
                      dopt_param_shard* out, int32_t cap, int32_t* count);
+/* The number of buckets over all buffers (< 0 on a null map), and the
+ * number of bucket `bucket` of `buffer` in that count (buffers in order,
+ * buckets in order within a buffer; < 0 when out of range).  These index
+ * the grad check table of dopt_step_args.grad_amax. */
+int32_t dopt_total_buckets(const dopt_shard_map* map);
+int32_t dopt_bucket_number(const dopt_shard_map* map, int32_t buffer, int32_t bucket);
 
 /* ---------------------------------------------------------------------------
  * Device entry points.  `rank` is a rank or DOPT_ALL_RANKS; the workspace
@@ -299,6 +305,26 @@ typedef struct {
    * after a warm-up step. */
   int64_t* d_step;
   const double* d_lr;
+  /* Optional check of every replica's gradients before their reduction
+   * (check_for_nan_in_grad / check_for_large_grads: the check_grads method
+   * of the bucket groups, distributed-package page sections 2.4 and 3.2,
+   * which looks at each bucket's gradients for NaN, Inf and unusually large
+   * values before the communication).  NULL: no check.  Else a device array
+   * of n_replicas x dopt_total_buckets(map) floats, replica-major, 4-byte
+   * aligned: the reduce pass of the step sets grad_amax[k * total + j] to
+   * the largest |g| among the elements of replica k in bucket j (buckets
+   * numbered across buffers in buffer order, dopt_bucket_number) that the
+   * step reads -- the selected rank's shard of each bucket, or every rank's
+   * with DOPT_ALL_RANKS -- taken as stored in the grad dtype, before any
+   * prescale, unscale or scale_gradients.  The value is NaN when one of
+   * those grads is NaN, +inf when one is infinite (and none is NaN), and 0
+   * for a bucket the step reads nothing of.  The step clears the slots it
+   * sets first (dopt_step_reduce_buckets clears only its buckets' slots).
+   * The check changes nothing else: the caller compares the values with its
+   * own threshold for "unusually large" (the pages give none), and a
+   * non-finite grad already skips the step through found_inf.  Costs no
+   * extra memory traffic (the replica grads are read once either way). */
+  float* grad_amax;
 } dopt_step_args;
 
 /* Statistics of the last step, kept at the start of its workspace:

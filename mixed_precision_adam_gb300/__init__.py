@@ -72,7 +72,7 @@ class dopt_step_args(ctypes.Structure):
                 ("max_norm", _D), ("remote_sumsq", _D), ("hp", dopt_adamw_hparams),
                 ("workspace", _P), ("workspace_bytes", _SZ), ("stream", _P),
                 ("stage_events", ctypes.POINTER(_P)), ("grad_scale", _F), ("reserved", _I32),
-                ("d_step", _P), ("d_lr", _P)]
+                ("d_step", _P), ("d_lr", _P), ("grad_amax", _P)]
 
 
 class dopt_step_stats(ctypes.Structure):
@@ -100,6 +100,8 @@ _c = {
     "dopt_shard_map_free": _proto("dopt_shard_map_free", None, _P),
     "dopt_num_buffers": _proto("dopt_num_buffers", _I32, _P),
     "dopt_dp_size": _proto("dopt_dp_size", _I32, _P),
+    "dopt_total_buckets": _proto("dopt_total_buckets", _I32, _P),
+    "dopt_bucket_number": _proto("dopt_bucket_number", _I32, _P, _I32, _I32),
     "dopt_buffer_info_get": _proto("dopt_buffer_info_get", ctypes.c_int, _P, _I32,
                                    ctypes.POINTER(dopt_buffer_info)),
     "dopt_bucket_info_get": _proto("dopt_bucket_info_get", ctypes.c_int, _P, _I32, _I32,
@@ -217,6 +219,14 @@ def dopt_num_buffers(m):
 
 def dopt_dp_size(m):
     return _check(_c["dopt_dp_size"](m))
+
+
+def dopt_total_buckets(m):
+    return _check(_c["dopt_total_buckets"](m))
+
+
+def dopt_bucket_number(m, buffer, bucket):
+    return _check(_c["dopt_bucket_number"](m, buffer, bucket))
 
 
 def _struct_dict(s):
@@ -352,6 +362,13 @@ class StepArgs:
         learning rate) instead of the host step number."""
         self.c.d_step = _ptr(d_step)
         self.c.d_lr = _ptr(d_lr)
+
+    def set_grad_check(self, grad_amax):
+        """Turns on the pre-reduction grad check: grad_amax is a device
+        float32 array of n_replicas x dopt_total_buckets(map) (or None to
+        turn it off)."""
+        self._grad_amax = grad_amax
+        self.c.grad_amax = _ptr(grad_amax)
 
     def set_step(self, step, lr=None):
         self.c.hp.step = int(step)

@@ -1,8 +1,9 @@
 """Builds the in-tree CUDA library lib/libdopt.so for sm_103a.
 
-Two translation units (host shard map in C++, kernels and device entry
-points in CUDA) are compiled in parallel and linked into one shared library
-with the CUDA runtime linked statically.  Run this file as a script
+Six translation units (the host shard map in C++; the device entry points
+and the finalize kernel; the reduce/prepare kernels for each of the three
+grad dtypes; the AdamW kernel) are compiled in parallel and linked into one
+shared library with the CUDA runtime linked statically.  Run this file as a script
 (python mixed_precision_adam_gb300/build.py) or call build().
 """
 
@@ -18,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
-SOURCES = ["shard_map.cpp", "dopt_cuda.cu"]
+SOURCES = ["shard_map.cpp", "dopt_cuda.cu", "k1_f32.cu", "k1_bf16.cu", "k1_f16.cu", "k3.cu"]
 
 
 def _deps():

@@ -1,0 +1,847 @@
+// k1.cuh -- K1, the reduce/prepare pass: the emulated reduce-scatter of N
+// replica grads into the fp32 main grad, fused with prepare_grads (unscale,
+// non-finite detection, zero count), the partial sums of squares of the
+// grad norm and, optionally, the check of every replica's grads before the
+// reduction.  Included once per grad dtype (k1_f32.cu, k1_bf16.cu,
+// k1_f16.cu), each instantiating launch_k1_for<its dtype>.
+//
+// Three kernels, chosen per launch:
+//   k1_reduce_prepare      any replica count, instances, average_in_collective
+//   k1_reduce_prepare_n    prescale-and-sum with 1, 2, 4 or 8 replicas per
+//                          instance and one or two instances (compile time)
+//   k1_reduce_prepare_tma  the single-instance fp32 case with the replica
+//                          tiles staged in shared memory by bulk copies
+// All three compute the same values in the same order.
+#pragma once
+
+#include <type_traits>
+
+#include "kernels.cuh"
+
+namespace dopt {
+
+// ------------------------------------------------------- grad encodings --
+
+// Loads of kVec grad elements are held in their raw encoding (float4 for
+// fp32, two packed 16-bit pairs for bf16/fp16) until the reduction widens
+// them, so a 16-bit grad keeps half the registers of an fp32 one and a
+// thread can keep twice as many 16-bit accesses in flight.
+//
+// The grad check keeps a running maximum of |g| as integer bits: for a
+// non-negative float the order of its bit pattern is the order of its
+// value, +inf lies above every finite value and NaN above +inf, so the
+// maximum of the bits of |g| is the largest magnitude, or +inf when there
+// is an infinity, or a NaN when there is a NaN.  A thread's running maximum
+// is one 32-bit word: the fp32 bits for fp32 grads, two 16-bit halves for
+// bf16/fp16 (maximised half by half, as the packed loads hold them).
+template <typename T>
+struct GradT;
+template <>
+struct GradT<float> {
+  using Raw = float4;
+  static constexpr int kUnroll = 1;  // multiplier of kUnroll1 for this type
+  static __device__ __forceinline__ Raw load4(const void* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    return j == 0 ? r.x : j == 1 ? r.y : j == 2 ? r.z : r.w;
+  }
+  static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
+    return __ldcs(static_cast<const float*>(p) + i);
+  }
+  static __device__ __forceinline__ void widen4(const void* p, int64_t i, float* x) {
+    float4 v = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+  static __device__ __forceinline__ float round_to(float s) { return s; }
+  // grad check
+  static __device__ __forceinline__ uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
+  static __device__ __forceinline__ uint32_t abs4(const Raw& r) {
+    return max(max(abs_bits(r.x), abs_bits(r.y)), max(abs_bits(r.z), abs_bits(r.w)));
+  }
+  static __device__ __forceinline__ uint32_t abs1(const void* p, int64_t i) {
+    return abs_bits(static_cast<const float*>(p)[i]);
+  }
+  static __device__ __forceinline__ uint32_t amax(uint32_t a, uint32_t b) { return max(a, b); }
+  static __device__ __forceinline__ uint32_t f32_bits(uint32_t a) { return a; }
+};
+template <>
+struct GradT<__nv_bfloat16> {
+  using Raw = uint2;
+  static constexpr int kUnroll = 2;
+  static __device__ __forceinline__ Raw load4(const void* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    const unsigned w = j < 2 ? r.x : r.y;
+    return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+  static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
+    unsigned short b = __ldcs(static_cast<const unsigned short*>(p) + i);
+    return __uint_as_float((unsigned)b << 16);
+  }
+  static __device__ __forceinline__ void widen4(const void* p, int64_t i, float* x) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  }
+  static __device__ __forceinline__ float round_to(float s) {
+    return __bfloat162float(__float2bfloat16_rn(s));
+  }
+  // grad check: halves of |g| bits; bf16 is the top half of the same fp32
+  static __device__ __forceinline__ uint32_t abs4(const Raw& r) {
+    return __vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu);
+  }
+  static __device__ __forceinline__ uint32_t abs1(const void* p, int64_t i) {
+    return static_cast<const unsigned short*>(p)[i] & 0x7FFFu;
+  }
+  static __device__ __forceinline__ uint32_t amax(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+  static __device__ __forceinline__ uint32_t f32_bits(uint32_t a) {
+    return max(a & 0xFFFFu, a >> 16) << 16;
+  }
+};
+template <>
+struct GradT<__half> {
+  using Raw = uint2;
+  static constexpr int kUnroll = 2;
+  static __device__ __forceinline__ Raw load4(const void* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+  }
+  static __device__ __forceinline__ float at(const Raw& r, int j) {
+    const unsigned w = j < 2 ? r.x : r.y;
+    return __half2float(__ushort_as_half((unsigned short)((j & 1) ? (w >> 16) : (w & 0xFFFFu))));
+  }
+  static __device__ __forceinline__ float widen1(const void* p, int64_t i) {
+    unsigned short b = __ldcs(static_cast<const unsigned short*>(p) + i);
+    return __half2float(__ushort_as_half(b));
+  }
+  static __device__ __forceinline__ void widen4(const void* p, int64_t i, float* x) {
+    uint2 v = __ldcs(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(p) + i));
+    x[0] = __half2float(__ushort_as_half((unsigned short)(v.x & 0xFFFFu)));
+    x[1] = __half2float(__ushort_as_half((unsigned short)(v.x >> 16)));
+    x[2] = __half2float(__ushort_as_half((unsigned short)(v.y & 0xFFFFu)));
+    x[3] = __half2float(__ushort_as_half((unsigned short)(v.y >> 16)));
+  }
+  static __device__ __forceinline__ float round_to(float s) {
+    return __half2float(__float2half_rn(s));
+  }
+  // grad check: halves of |g| bits, widened to fp32 bits once at the end
+  // (the widening keeps the order, +inf and NaN)
+  static __device__ __forceinline__ uint32_t abs4(const Raw& r) {
+    return __vmaxu2(r.x & 0x7FFF7FFFu, r.y & 0x7FFF7FFFu);
+  }
+  static __device__ __forceinline__ uint32_t abs1(const void* p, int64_t i) {
+    return static_cast<const unsigned short*>(p)[i] & 0x7FFFu;
+  }
+  static __device__ __forceinline__ uint32_t amax(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+  static __device__ __forceinline__ uint32_t f32_bits(uint32_t a) {
+    const unsigned short h = (unsigned short)max(a & 0xFFFFu, a >> 16);
+    return __float_as_uint(__half2float(__ushort_as_half(h)));
+  }
+};
+
+// Merges a warp's per-lane maxima of replica k in one bucket into
+// amax[k * stride + bucket] (fp32 bits of |g|; an atomic max, so the
+// result does not depend on the order of the CTAs).  Called by whole warps.
+template <typename GT>
+__device__ __forceinline__ void amax_flush(uint32_t bits, const K1Params& p, int k, int bucket) {
+  const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, GradT<GT>::f32_bits(bits));
+  if ((threadIdx.x & 31) == 0 && v != 0u) atomicMax(p.amax + (size_t)k * p.amax_stride + bucket, v);
+}
+
+// ------------------------------------------------------------ reduction --
+
+// Reduction of one element over the replicas, in replica order, starting
+// from the first term; rounded to the grad dtype after each instance's sum
+// and again after the inter-instance sum.
+struct ReduceState {
+  float s, total;
+};
+
+// Where replica k sits in the reduction: its index inside its instance,
+// whether it opens / closes the instance's sum and whether its instance is
+// the first one.  The same for every element, so computed once per replica.
+struct ReplicaPos {
+  bool opens, closes, first_inst;
+};
+
+__device__ __forceinline__ ReplicaPos replica_pos(int k, int dpi) {
+  const int q = k % dpi;
+  return ReplicaPos{q == 0, q == dpi - 1, k < dpi};
+}
+
+template <typename GT>
+__device__ __forceinline__ void reduce_term(ReduceState& st, float x, ReplicaPos rp,
+                                            const K1Params& p) {
+  float term = p.average ? x : __fmul_rn(x, p.pre);
+  st.s = rp.opens ? term : __fadd_rn(st.s, term);
+  if (rp.closes) {
+    float s = p.average ? __fmul_rn(st.s, p.inv_dpi) : st.s;
+    s = GradT<GT>::round_to(s);
+    st.total = rp.first_inst ? s : __fadd_rn(st.total, s);
+  }
+}
+
+// The reduced grad in the grad dtype, times the scale_gradients factor
+// (rounded to the grad dtype again; skipped for a factor of 1).
+template <typename GT>
+__device__ __forceinline__ float post_scaled(float red, float post_scale) {
+  return post_scale == 1.0f ? red : GradT<GT>::round_to(__fmul_rn(red, post_scale));
+}
+
+template <typename GT>
+__device__ __forceinline__ float reduce_finish(const ReduceState& st, const K1Params& p) {
+  float total = st.total;
+  if (p.n_inst > 1) {
+    if (p.average) total = __fmul_rn(total, p.inv_ninst);
+    total = GradT<GT>::round_to(total);
+  }
+  return __fmul_rn(post_scaled<GT>(total, p.post_scale), p.inv_scale);
+}
+
+// ---------------------------------------------------------- norm partials --
+
+// Sum of squares of a thread's main grads, accurate to about fp64 while
+// computing in fp32: each square is split exactly into p + pe (FMA) and added
+// with the error-free TwoSum, the errors gathered in c (the Dot2 scheme of
+// Ogita, Rump & Oishi, "Accurate sum and dot product", SIAM J. Sci. Comput.
+// 2005).  Squares of |x| >= 2^62 would overflow fp32 and go to an fp64
+// accumulator instead, and the fp32 pair moves to fp64 before it could
+// overflow; both rare paths are out-of-line calls, so no fp64 instruction
+// is issued per element (GB300's fp64 rate is a small fraction of fp32's).
+// A non-finite main grad makes the sum non-finite, and finite main grads
+// cannot overflow it, so the non-finite check of prepare_grads is read off
+// the sum.
+static __device__ __noinline__ double sumsq_wide(double d, float a, float b, float c, float e) {
+  return d + (double)a * (double)a + (double)b * (double)b + (double)c * (double)c +
+         (double)e * (double)e;
+}
+static __device__ __noinline__ double sumsq_flush(double d, float s, float c) {
+  return d + ((double)s + (double)c);
+}
+
+struct SumSq {
+  float s = 0.f, c = 0.f;
+  double d = 0.0;
+  int zeros = 0;  // main grads equal to zero (count_zeros)
+  __device__ __forceinline__ void dot2(float x) {
+    float p = __fmul_rn(x, x);
+    float pe = fmaf(x, x, -p);
+    float t = __fadd_rn(s, p);
+    float bp = __fsub_rn(t, s);
+    float e = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(e, pe));
+  }
+  __device__ __forceinline__ void add4(const float* x) {
+    zeros += (x[0] == 0.f) + (x[1] == 0.f) + (x[2] == 0.f) + (x[3] == 0.f);
+    float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    if (mx >= 0x1p62f) {
+      d = sumsq_wide(d, x[0], x[1], x[2], x[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dot2(x[j]);
+    }
+  }
+  __device__ __forceinline__ void add1(float x) {
+    zeros += (x == 0.f);
+    if (fabsf(x) >= 0x1p62f) d = sumsq_wide(d, x, 0.f, 0.f, 0.f);
+    else dot2(x);
+  }
+  // once per tile: keeps |s| below 2^100 (NaN also takes this path)
+  __device__ __forceinline__ void maybe_flush() {
+    if (!(fabsf(s) <= 0x1p100f)) {
+      d = sumsq_flush(d, s, c);
+      s = c = 0.f;
+    }
+  }
+  __device__ __forceinline__ double value() const { return d + ((double)s + (double)c); }
+};
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Writes this CTA's partial (sum of squares, non-finite flag) and zeroes the
+// slots of its region that this launch leaves unused, so the finalize pass
+// can always sum whole regions.
+__device__ __forceinline__ void write_partial(const SumSq& acc, Partial* partials) {
+  __shared__ double s_sum[kThreads / 32];
+  __shared__ int s_zero[kThreads / 32];
+  double v = warp_sum(acc.value());
+  int z = acc.zeros;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+  if (threadIdx.x % 32 == 0) {
+    s_sum[threadIdx.x / 32] = v;
+    s_zero[threadIdx.x / 32] = z;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    int zt = 0;
+    for (int i = 0; i < kThreads / 32; ++i) {
+      tot += s_sum[i];
+      zt += s_zero[i];
+    }
+    partials[blockIdx.x] = Partial{tot, isfinite(tot) ? 0 : 1, zt};
+    for (int i = gridDim.x + blockIdx.x; i < kMaxGrid; i += gridDim.x)
+      partials[i] = Partial{0.0, 0, 0};
+  }
+}
+
+// ------------------------------------------------------------------- K1 --
+
+// General reduction: any replica count, instances, average_in_collective.
+// With CHECK, each warp folds its per-replica maxima of a tile into shared
+// memory (the replica count is known only at run time), and the CTA merges
+// them into the global table whenever its tiles move to another bucket.
+template <typename GT, bool FULL, bool STATS, bool CHECK>
+__global__ void __launch_bounds__(kThreads, DOPT_K1_MIN_BLOCKS)
+k1_reduce_prepare(const __grid_constant__ K1Params p) {
+  __shared__ uint32_t s_amax[DOPT_MAX_REPLICAS];
+  const int dpi = p.n_rep / p.n_inst;
+  SumSq acc;
+  int si = 0, cur_bucket = -1;
+  if constexpr (CHECK) {
+    for (int k = threadIdx.x; k < DOPT_MAX_REPLICAS; k += kThreads) s_amax[k] = 0u;
+    __syncthreads();
+  }
+  // CTA-wide: merge the shared maxima into the bucket's slots and clear them
+  auto flush_bucket = [&](int bucket) {
+    __syncthreads();
+    if (threadIdx.x < p.n_rep) {
+      const uint32_t v = s_amax[threadIdx.x];
+      if (v) atomicMax(p.amax + (size_t)threadIdx.x * p.amax_stride + bucket, v);
+      s_amax[threadIdx.x] = 0u;
+    }
+    __syncthreads();
+  };
+  for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
+    si = seek(p.tab, si, t);
+    const Seg& sg = p.tab.seg[si];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTile1;
+    const int n = (int)min((int64_t)kTile1, (int64_t)sg.len - off);
+    const int64_t l0 = sg.local + off;
+    const int64_t r0 = FULL ? sg.world + off : l0;
+    const bool aligned = seg_aligned(sg.local, sg.world);
+    if constexpr (CHECK) {
+      if (sg.bucket != cur_bucket) {
+        if (cur_bucket >= 0) flush_bucket(cur_bucket);
+        cur_bucket = sg.bucket;
+      }
+    }
+
+    ReduceState st[kUnroll1][kVec];
+    bool vec_ok[kUnroll1];
+#pragma unroll
+    for (int u = 0; u < kUnroll1; ++u) vec_ok[u] = aligned && ((u * kThreads + threadIdx.x) * kVec + kVec <= n);
+
+    // kBatch replicas x kUnroll1 accesses of kVec elements in flight
+    for (int k0 = 0; k0 < p.n_rep; k0 += kBatch) {
+      float x[kBatch][kUnroll1][kVec];
+#pragma unroll
+      for (int kk = 0; kk < kBatch; ++kk) {
+        if (k0 + kk < p.n_rep) {
+#pragma unroll
+          for (int u = 0; u < kUnroll1; ++u) {
+            const int e = (u * kThreads + threadIdx.x) * kVec;
+            if (vec_ok[u]) GradT<GT>::widen4(p.rep[k0 + kk], r0 + e, x[kk][u]);
+          }
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < kBatch; ++kk) {
+        if (k0 + kk < p.n_rep) {
+          const ReplicaPos rp = replica_pos(k0 + kk, dpi);
+          uint32_t mx = 0u;
+#pragma unroll
+          for (int u = 0; u < kUnroll1; ++u) {
+            if (vec_ok[u]) {
+#pragma unroll
+              for (int j = 0; j < kVec; ++j) {
+                reduce_term<GT>(st[u][j], x[kk][u][j], rp, p);
+                if (CHECK) mx = max(mx, GradT<float>::abs_bits(x[kk][u][j]));
+              }
+            }
+          }
+          if (CHECK) {
+            mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+            if ((threadIdx.x & 31) == 0 && mx) atomicMax(&s_amax[k0 + kk], mx);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll1; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (vec_ok[u]) {
+        float m[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) m[j] = reduce_finish<GT>(st[u][j], p);
+        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        if (STATS) acc.add4(m);
+      } else if (e < n) {
+        // scalar path: the ragged end of a run, or a run whose starts are
+        // not 8-element aligned
+        const int cnt = min(kVec, n - e);
+        for (int j = 0; j < cnt; ++j) {
+          ReduceState s1;
+          s1.s = 0.f;
+          s1.total = 0.f;
+          for (int k = 0; k < p.n_rep; ++k) {
+            const float xk = GradT<GT>::widen1(p.rep[k], r0 + e + j);
+            reduce_term<GT>(s1, xk, replica_pos(k, dpi), p);
+            if (CHECK) {
+              const uint32_t b = GradT<float>::abs_bits(xk);
+              if (b) atomicMax(&s_amax[k], b);
+            }
+          }
+          float m = reduce_finish<GT>(s1, p);
+          p.main_grad[l0 + e + j] = m;
+          if (STATS) acc.add1(m);
+        }
+      }
+    }
+    if (STATS) acc.maybe_flush();
+  }
+  if constexpr (CHECK) {
+    if (cur_bucket >= 0) flush_bucket(cur_bucket);
+  }
+  if (STATS) write_partial(acc, p.partials);
+}
+
+// The common reductions: prescale by 1/N and sum (average_in_collective =
+// false), NINST instances of DPI replicas each, both known at compile time.
+// Same arithmetic as the general kernel, in the same order (each instance's
+// replicas summed in order and rounded to the grad dtype, then the instance
+// sums in order, rounded again when there is more than one), without its
+// per-element selects.  Loads of one instance are in flight together.  With
+// CHECK every thread keeps a running maximum per replica in registers and
+// each warp merges it into the global table when its tiles move to another
+// bucket.
+template <typename GT, bool FULL, bool STATS, bool CHECK, int DPI, int NINST>
+__global__ void __launch_bounds__(kThreads, DOPT_K1_MIN_BLOCKS)
+k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
+  constexpr int U = kUnroll1 * GradT<GT>::kUnroll;  // accesses per thread per tile
+  constexpr int TILE = kThreads * kVec * U;
+  SumSq acc;
+  int si = 0, cur_bucket = -1;
+  uint32_t amx[NINST][DPI];  // unused (and dropped by the compiler) without CHECK
+#pragma unroll
+  for (int j = 0; j < NINST; ++j)
+#pragma unroll
+    for (int k = 0; k < DPI; ++k) amx[j][k] = 0u;
+  auto flush_bucket = [&](int bucket) {
+#pragma unroll
+    for (int j = 0; j < NINST; ++j)
+#pragma unroll
+      for (int k = 0; k < DPI; ++k) {
+        amax_flush<GT>(amx[j][k], p, j * DPI + k, bucket);
+        amx[j][k] = 0u;
+      }
+  };
+  const float pre = p.pre, inv_scale = p.inv_scale;
+  for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
+    si = seek(p.tab, si, t);
+    const Seg& sg = p.tab.seg[si];
+    const int64_t off = (int64_t)(t - sg.tile0) * TILE;
+    const int n = (int)min((int64_t)TILE, (int64_t)sg.len - off);
+    const int64_t l0 = sg.local + off;
+    const int64_t r0 = FULL ? sg.world + off : l0;
+    const bool aligned = seg_aligned(sg.local, sg.world);
+    if constexpr (CHECK) {
+      if (sg.bucket != cur_bucket) {
+        if (cur_bucket >= 0) flush_bucket(cur_bucket);
+        cur_bucket = sg.bucket;
+      }
+    }
+
+    bool vec_ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) vec_ok[u] = aligned && (u * kThreads + threadIdx.x) * kVec + kVec <= n;
+    float total[U][kVec];
+#pragma unroll 1
+    for (int j = 0; j < NINST; ++j) {  // one instance's loads live at a time
+      typename GradT<GT>::Raw x[DPI][U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = (u * kThreads + threadIdx.x) * kVec;
+        if (vec_ok[u]) {
+#pragma unroll
+          for (int k = 0; k < DPI; ++k) x[k][u] = GradT<GT>::load4(p.rep[j * DPI + k], r0 + e);
+        }
+      }
+      if (CHECK) {
+        // j is a run-time index: select the instance's registers by compare
+#pragma unroll
+        for (int jj = 0; jj < NINST; ++jj) {
+          if (jj == j) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              if (vec_ok[u]) {
+#pragma unroll
+                for (int k = 0; k < DPI; ++k) amx[jj][k] = GradT<GT>::amax(amx[jj][k], GradT<GT>::abs4(x[k][u]));
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          float sum = __fmul_rn(GradT<GT>::at(x[0][u], q), pre);
+#pragma unroll
+          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::at(x[k][u], q), pre));
+          sum = GradT<GT>::round_to(sum);
+          total[u][q] = (j == 0) ? sum : __fadd_rn(total[u][q], sum);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (vec_ok[u]) {
+        float m[kVec];
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          float tt = NINST > 1 ? GradT<GT>::round_to(total[u][q]) : total[u][q];
+          m[q] = __fmul_rn(post_scaled<GT>(tt, p.post_scale), inv_scale);
+        }
+        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        if (STATS) acc.add4(m);
+      } else if (e < n) {
+        const int cnt = min(kVec, n - e);
+        for (int q = 0; q < cnt; ++q) {
+          float tt = 0.f;
+#pragma unroll
+          for (int j = 0; j < NINST; ++j) {
+            float sum = 0.f;
+#pragma unroll
+            for (int k = 0; k < DPI; ++k) {
+              const int64_t i = r0 + e + q;
+              const float term = __fmul_rn(GradT<GT>::widen1(p.rep[j * DPI + k], i), pre);
+              sum = k == 0 ? term : __fadd_rn(sum, term);
+              if (CHECK) amx[j][k] = GradT<GT>::amax(amx[j][k], GradT<GT>::abs1(p.rep[j * DPI + k], i));
+            }
+            sum = GradT<GT>::round_to(sum);
+            tt = (j == 0) ? sum : __fadd_rn(tt, sum);
+          }
+          if (NINST > 1) tt = GradT<GT>::round_to(tt);
+          float m = __fmul_rn(post_scaled<GT>(tt, p.post_scale), inv_scale);
+          p.main_grad[l0 + e + q] = m;
+          if (STATS) acc.add1(m);
+        }
+      }
+    }
+    if (STATS) acc.maybe_flush();
+  }
+  if constexpr (CHECK) {
+    if (cur_bucket >= 0) flush_bucket(cur_bucket);
+  }
+  if (STATS) write_partial(acc, p.partials);
+}
+
+// ---------------------------------------------------------- K1 with TMA --
+//
+// The single-instance reduction with every replica tile staged through
+// shared memory by the bulk-copy engine (cp.async.bulk, one 1-D copy per
+// replica per tile, completion counted in bytes on a per-stage mbarrier).
+// A ring of DOPT_TMA_STAGES stages keeps up to stages x replicas x tile bytes
+// in flight per SM independently of registers; thread 0 issues, every thread
+// consumes.  Every wait is bounded: a CTA that gives up (decided uniformly)
+// sets the error flag, marks its partial non-finite so the step is skipped,
+// waits (bounded) for its copies still in flight and leaves.  Used for
+// fp32 replicas when every run of the launch is 8-element aligned.
+
+constexpr unsigned long long kWaitNs = 1000000000ull;  // give up a wait after 1 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Polls an mbarrier phase for at most kWaitNs nanoseconds.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+#if DOPT_TMA_EVICT_FIRST
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"((unsigned long long)__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+#else
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"((unsigned long long)__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+#endif
+}
+
+template <typename GT>
+struct GradBits {
+  using T = typename std::conditional<std::is_same<GT, float>::value, float, unsigned short>::type;
+};
+
+template <typename GT, int DPI>
+__host__ __device__ constexpr size_t tma_smem_bytes() {
+  return (size_t)DOPT_TMA_STAGES * DPI * kTmaTile * sizeof(typename GradBits<GT>::T) +
+         DOPT_TMA_STAGES * sizeof(uint64_t);
+}
+
+template <typename GT, bool FULL, bool STATS, bool CHECK, int DPI>
+__global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __grid_constant__ K1Params p) {
+  using E = typename GradBits<GT>::T;
+  constexpr int S = DOPT_TMA_STAGES;
+  constexpr int VALIGN = 16 / sizeof(E);  // elements per 16 bytes: bulk sizes are multiples of it
+  extern __shared__ __align__(128) unsigned char smem[];
+  E* tiles = reinterpret_cast<E*>(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * DPI * kTmaTile * sizeof(E));
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int G = gridDim.x;
+  const int my = p.tab.n_tiles > (int)blockIdx.x ? (p.tab.n_tiles - (int)blockIdx.x + G - 1) / G : 0;
+  int si_issue = 0;
+  // thread 0: start the copies of this CTA's i-th tile into stage i % S
+  auto issue = [&](int i) {
+    const int t = blockIdx.x + i * G;
+    si_issue = seek(p.tab, si_issue, t);
+    const Seg& sg = p.tab.seg[si_issue];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTmaTile;
+    const int n = (int)min((int64_t)kTmaTile, (int64_t)sg.len - off);
+    const int nv = n & ~(VALIGN - 1);
+    const int64_t r0 = FULL ? sg.world + off : sg.local + off;
+    const int stage = i % S;
+    mbar_arrive_expect_tx(&bars[stage], (unsigned)(nv * sizeof(E)) * DPI);
+    if (nv > 0 && !(blockIdx.x == 0 && i == p.starve_tile)) {
+#pragma unroll
+      for (int k = 0; k < DPI; ++k)
+        bulk_load(tiles + ((size_t)stage * DPI + k) * kTmaTile, static_cast<const E*>(p.rep[k]) + r0,
+                  (unsigned)(nv * sizeof(E)), &bars[stage]);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < min(S, my); ++i) issue(i);
+
+  SumSq acc;
+  int si = 0, cur_bucket = -1;
+  uint32_t amx[DPI];  // unused (and dropped by the compiler) without CHECK
+#pragma unroll
+  for (int k = 0; k < DPI; ++k) amx[k] = 0u;
+  auto flush_bucket = [&](int bucket) {
+#pragma unroll
+    for (int k = 0; k < DPI; ++k) {
+      amax_flush<GT>(amx[k], p, k, bucket);
+      amx[k] = 0u;
+    }
+  };
+  bool failed = false;
+  const float pre = p.pre, inv_scale = p.inv_scale;
+  int i = 0;
+  for (; i < my; ++i) {
+    const int stage = i % S;
+    const bool ok = mbar_wait_bounded(&bars[stage], (unsigned)((i / S) & 1));
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    const int t = blockIdx.x + i * G;
+    si = seek(p.tab, si, t);
+    const Seg& sg = p.tab.seg[si];
+    const int64_t off = (int64_t)(t - sg.tile0) * kTmaTile;
+    const int n = (int)min((int64_t)kTmaTile, (int64_t)sg.len - off);
+    const int nv = n & ~(VALIGN - 1);
+    const int64_t l0 = sg.local + off;
+    const int64_t r0 = FULL ? sg.world + off : l0;
+    const E* st = tiles + (size_t)stage * DPI * kTmaTile;
+    if constexpr (CHECK) {
+      if (sg.bucket != cur_bucket) {
+        if (cur_bucket >= 0) flush_bucket(cur_bucket);
+        cur_bucket = sg.bucket;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kTmaTile / (kThreads * kVec); ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (e + kVec <= nv) {
+        float m[kVec];
+        typename GradT<GT>::Raw x[DPI];
+#pragma unroll
+        for (int k = 0; k < DPI; ++k)
+          x[k] = *reinterpret_cast<const typename GradT<GT>::Raw*>(st + (size_t)k * kTmaTile + e);
+        if (CHECK) {
+#pragma unroll
+          for (int k = 0; k < DPI; ++k) amx[k] = GradT<GT>::amax(amx[k], GradT<GT>::abs4(x[k]));
+        }
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          float sum = __fmul_rn(GradT<GT>::at(x[0], q), pre);
+#pragma unroll
+          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::at(x[k], q), pre));
+          m[q] = __fmul_rn(post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale), inv_scale);
+        }
+        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        if (STATS) acc.add4(m);
+      } else if (e < n) {
+        // the last few elements of a run: not in the staged copy
+        const int cnt = min(kVec, n - e);
+        for (int q = 0; q < cnt; ++q) {
+          float sum = 0.f;
+#pragma unroll
+          for (int k = 0; k < DPI; ++k) {
+            const float term = __fmul_rn(GradT<GT>::widen1(p.rep[k], r0 + e + q), pre);
+            sum = k == 0 ? term : __fadd_rn(sum, term);
+            if (CHECK) amx[k] = GradT<GT>::amax(amx[k], GradT<GT>::abs1(p.rep[k], r0 + e + q));
+          }
+          float m = __fmul_rn(post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale), inv_scale);
+          p.main_grad[l0 + e + q] = m;
+          if (STATS) acc.add1(m);
+        }
+      }
+    }
+    if (STATS) acc.maybe_flush();
+    __syncthreads();  // every thread is done with this stage
+    if (threadIdx.x == 0 && i + S < my) issue(i + S);
+  }
+  if (failed) {
+    if (threadIdx.x == 0) {
+      *p.error_flag = kErrorMagic;
+      // let the copies already issued land before the shared memory goes away
+      for (int j = i; j < min(i + S, my); ++j) mbar_wait_bounded(&bars[j % S], (unsigned)((j / S) & 1));
+    }
+    __syncthreads();
+    acc.s = __int_as_float(0x7FC00000);  // a NaN partial skips the step
+  }
+  if constexpr (CHECK) {
+    if (cur_bucket >= 0) flush_bucket(cur_bucket);
+  }
+  if (STATS) write_partial(acc, p.partials);
+}
+
+// ------------------------------------------------------------ launchers --
+
+template <typename K>
+int launch_plain(K kern, const K1Params& kp, cudaStream_t s, const char* what) {
+  int grid = 0;
+  int st = grid_for(kern, kp.tab.n_tiles, &grid);
+  if (st) return st;
+  kern<<<grid, kThreads, 0, s>>>(kp);
+  return check_launch(what);
+}
+
+template <typename GT, bool FULL, bool STATS, bool CHECK, int DPI>
+int launch_tma(K1Params& kp, cudaStream_t s) {
+  auto kern = k1_reduce_prepare_tma<GT, FULL, STATS, CHECK, DPI>;
+  const size_t smem = tma_smem_bytes<GT, DPI>();
+  // the dynamic shared-memory limit is raised once per device (a later call,
+  // e.g. inside a stream capture, then issues nothing but the launch)
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (!bit || !(attr_set.load() & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+      return fail(DOPT_E_CUDA, std::string("k1 tma smem attribute: ") + cudaGetErrorString(e));
+    attr_set.fetch_or(bit);
+  }
+  int grid = 0;
+  int st = grid_for(kern, kp.tab.n_tiles, &grid, smem);
+  if (st) return st;
+  kern<<<grid, kThreads, smem, s>>>(kp);
+  return check_launch("k1_reduce_prepare_tma launch");
+}
+
+// The specialised kernels cover prescale-and-sum with one instance of 1, 2,
+// 4 or 8 replicas, or two instances of 4 or 8; fp32 replicas in a single
+// instance whose runs are all 8-element aligned are staged by TMA (16-bit
+// replicas stream faster through registers: packed loads, four accesses per
+// thread).  Everything else runs the general kernel.
+template <typename GT, bool FULL, bool STATS, bool CHECK>
+int launch_k1_sel(K1Params& kp, const K1Launch& l, cudaStream_t s) {
+  const int dpi = kp.n_rep / kp.n_inst;
+  const bool special = !kp.average && ((kp.n_inst == 1 && (dpi == 1 || dpi == 2 || dpi == 4 || dpi == 8)) ||
+                                       (kp.n_inst == 2 && (dpi == 4 || dpi == 8)));
+  bool all_aligned = true;
+  for (int k = 0; k < l.count; ++k) all_aligned &= seg_aligned(l.runs[k].local, l.runs[k].world);
+  constexpr bool kTmaKind = DOPT_K1_TMA && STATS && std::is_same<GT, float>::value;
+  const bool tma = kTmaKind && kp.error_flag && special && kp.n_inst == 1 && all_aligned;
+  const int tile = tma ? kTmaTile : special ? kThreads * kVec * kUnroll1 * GradT<GT>::kUnroll : kTile1;
+  fill_table(kp.tab, l.runs, l.count, tile, l.bucket_base);
+  if constexpr (kTmaKind) {
+    if (tma) {
+      switch (dpi) {
+        case 1: return launch_tma<GT, FULL, STATS, CHECK, 1>(kp, s);
+        case 2: return launch_tma<GT, FULL, STATS, CHECK, 2>(kp, s);
+        case 4: return launch_tma<GT, FULL, STATS, CHECK, 4>(kp, s);
+        default: return launch_tma<GT, FULL, STATS, CHECK, 8>(kp, s);
+      }
+    }
+  }
+  const char* what = "k1_reduce_prepare_n launch";
+  if (special && kp.n_inst == 1) {
+    switch (dpi) {
+      case 1: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 1, 1>, kp, s, what);
+      case 2: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 2, 1>, kp, s, what);
+      case 4: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 4, 1>, kp, s, what);
+      default: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 8, 1>, kp, s, what);
+    }
+  }
+  if (special) {
+    if (dpi == 4) return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 4, 2>, kp, s, what);
+    return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 8, 2>, kp, s, what);
+  }
+  return launch_plain(k1_reduce_prepare<GT, FULL, STATS, CHECK>, kp, s, "k1_reduce_prepare launch");
+}
+
+// The grad check rides on the statistics pass only (the fused and
+// bucket-staged steps); the plain reduction has no check.
+template <typename GT>
+int launch_k1_for(K1Params& kp, const K1Launch& l, cudaStream_t s) {
+  if (l.check && !l.stats) return fail(DOPT_E_INVALID, "the grad check needs the statistics pass");
+  if (!l.stats)
+    return l.full ? launch_k1_sel<GT, true, false, false>(kp, l, s) : launch_k1_sel<GT, false, false, false>(kp, l, s);
+  if (l.check)
+    return l.full ? launch_k1_sel<GT, true, true, true>(kp, l, s) : launch_k1_sel<GT, false, true, true>(kp, l, s);
+  return l.full ? launch_k1_sel<GT, true, true, false>(kp, l, s) : launch_k1_sel<GT, false, true, false>(kp, l, s);
+}
+
+}  // namespace dopt

@@ -1,0 +1,9 @@
+// k1_f16.cu -- K1 reduce/prepare kernels for fp16 replica grads (one grad
+// dtype per translation unit, so the three compile in parallel).
+#include "k1.cuh"
+
+namespace dopt {
+
+int launch_k1_f16(K1Params& kp, const K1Launch& l, cudaStream_t s) { return launch_k1_for<__half>(kp, l, s); }
+
+}  // namespace dopt

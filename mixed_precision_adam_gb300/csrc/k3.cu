@@ -1,0 +1,185 @@
+// k3.cu -- K3, the AdamW pass: reads the fp32 main grad, master weight, m
+// and v of every shard element once, applies the clip coefficient and the
+// AdamW update (torch semantics, fp32), writes master, m and v back and
+// casts the new master into the bf16/fp16 param buffer at the element's
+// buffer offset (the stand-in for the param all-gather).  An fp32 param
+// buffer is its own master and is stepped in place.  A step the finalize
+// pass marked as skipped writes nothing.
+#include "kernels.cuh"
+
+namespace dopt {
+
+template <typename PT>
+struct ParamT;
+template <>
+struct ParamT<__nv_bfloat16> {
+  static constexpr bool kInPlace = false;
+  static __device__ __forceinline__ void store4(void* p, int64_t i, const float* x) {
+    unsigned short h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __bfloat16_as_ushort(__float2bfloat16_rn(x[j]));
+    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i),
+           make_uint2((unsigned)h[0] | ((unsigned)h[1] << 16), (unsigned)h[2] | ((unsigned)h[3] << 16)));
+  }
+  static __device__ __forceinline__ void store1(void* p, int64_t i, float x) {
+    static_cast<unsigned short*>(p)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  }
+};
+template <>
+struct ParamT<__half> {
+  static constexpr bool kInPlace = false;
+  static __device__ __forceinline__ void store4(void* p, int64_t i, const float* x) {
+    unsigned short h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = __half_as_ushort(__float2half_rn(x[j]));
+    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i),
+           make_uint2((unsigned)h[0] | ((unsigned)h[1] << 16), (unsigned)h[2] | ((unsigned)h[3] << 16)));
+  }
+  static __device__ __forceinline__ void store1(void* p, int64_t i, float x) {
+    static_cast<unsigned short*>(p)[i] = __half_as_ushort(__float2half_rn(x));
+  }
+};
+template <>
+struct ParamT<float> {
+  static constexpr bool kInPlace = true;  // the fp32 param buffer is the master
+  static __device__ __forceinline__ void store4(void*, int64_t, const float*) {}
+  static __device__ __forceinline__ void store1(void*, int64_t, float) {}
+};
+
+// The decoupled weight-decay factor (float)(1 - lr*wd*wd_mult), formed in
+// fp64; out of line so no fp64 instruction is issued per element -- it runs
+// once per run change.
+static __device__ __noinline__ float decay_of(double lr_wd, double wd_mult) {
+  return (float)(1.0 - lr_wd * wd_mult);
+}
+
+struct StepScalars {
+  float step_size, bc2_sqrt;
+  double lr_wd;
+};
+
+__device__ __forceinline__ StepScalars step_scalars(const K3Params& p) {
+  if (p.dev) return StepScalars{p.dev->step_size, p.dev->bc2_sqrt, p.dev->lr_wd};
+  return StepScalars{p.step_size, p.bc2_sqrt, p.lr_wd};
+}
+
+// One element of AdamW (torch semantics: decay the weight, update m and v,
+// divide the bias-corrected sqrt(v) + eps into m, step), each operation
+// rounded once in fp32.
+__device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, const StepScalars& ss,
+                                       float& w, float& m, float& v) {
+  float pp = __fmul_rn(w, decay);
+  float mm = __fadd_rn(__fmul_rn(p.b1, m), __fmul_rn(p.omb1, g));
+  float vv = __fadd_rn(__fmul_rn(p.b2, v), __fmul_rn(__fmul_rn(p.omb2, g), g));
+  float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(vv), ss.bc2_sqrt), p.eps);
+  pp = __fsub_rn(pp, __fmul_rn(ss.step_size, __fdiv_rn(mm, denom)));
+  w = pp;
+  m = mm;
+  v = vv;
+}
+
+// The AdamW pass with the loads of a thread's next tile issued before the
+// current tile is computed and stored, so the memory pipe stays busy while
+// the thread does arithmetic (software pipelining across tiles).
+struct K3Tile {
+  float4 g[kUnroll3], w[kUnroll3], m[kUnroll3], v[kUnroll3];
+  int64_t l0, w0, m0;
+  int n;
+  float decay;
+  bool aligned;
+};
+
+template <typename PT>
+__device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, int& si, K3Tile& T,
+                                        int& decay_si, float& decay, double lr_wd) {
+  si = seek(p.tab, si, t);
+  const Seg& sg = p.tab.seg[si];
+  if (si != decay_si) {
+    decay = decay_of(lr_wd, sg.wd_mult);
+    decay_si = si;
+  }
+  const int64_t off = (int64_t)(t - sg.tile0) * kTile3;
+  T.n = (int)min((int64_t)kTile3, (int64_t)sg.len - off);
+  T.l0 = sg.local + off;
+  T.w0 = sg.world + off;
+  T.m0 = ParamT<PT>::kInPlace ? T.w0 : T.l0;
+  T.aligned = seg_aligned(sg.local, sg.world);
+  T.decay = decay;
+#pragma unroll
+  for (int u = 0; u < kUnroll3; ++u) {
+    const int e = (u * kThreads + threadIdx.x) * kVec;
+    if (T.aligned && e + kVec <= T.n) {
+      T.g[u] = __ldcs(reinterpret_cast<const float4*>(p.main_grad + T.l0 + e));
+      T.w[u] = __ldcs(reinterpret_cast<const float4*>(wbase + T.m0 + e));
+      T.m[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg + T.l0 + e));
+      T.v[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg_sq + T.l0 + e));
+    }
+  }
+}
+
+template <typename PT>
+__global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(const __grid_constant__ K3Params p) {
+  if (*p.found_inf) return;  // skipped step: nothing is written
+  const float c = *p.coef;
+  const StepScalars ss = step_scalars(p);
+  float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
+  int si = 0, decay_si = -1;
+  float decay = 1.f;
+  int t = blockIdx.x;
+  if (t >= p.tab.n_tiles) return;
+  K3Tile cur;
+  k3_load<PT>(p, wbase, t, si, cur, decay_si, decay, ss.lr_wd);
+  for (; t < p.tab.n_tiles; t += gridDim.x) {
+    K3Tile nxt;
+    const bool more = t + (int)gridDim.x < p.tab.n_tiles;
+    if (more) k3_load<PT>(p, wbase, t + gridDim.x, si, nxt, decay_si, decay, ss.lr_wd);
+#pragma unroll
+    for (int u = 0; u < kUnroll3; ++u) {
+      const int e = (u * kThreads + threadIdx.x) * kVec;
+      if (cur.aligned && e + kVec <= cur.n) {
+        float g[kVec] = {cur.g[u].x, cur.g[u].y, cur.g[u].z, cur.g[u].w};
+        float w[kVec] = {cur.w[u].x, cur.w[u].y, cur.w[u].z, cur.w[u].w};
+        float m[kVec] = {cur.m[u].x, cur.m[u].y, cur.m[u].z, cur.m[u].w};
+        float v[kVec] = {cur.v[u].x, cur.v[u].y, cur.v[u].z, cur.v[u].w};
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[j], c), cur.decay, p, ss, w[j], m[j], v[j]);
+        __stcs(reinterpret_cast<float4*>(wbase + cur.m0 + e), make_float4(w[0], w[1], w[2], w[3]));
+        __stcs(reinterpret_cast<float4*>(p.exp_avg + cur.l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + cur.l0 + e), make_float4(v[0], v[1], v[2], v[3]));
+        ParamT<PT>::store4(p.param, cur.w0 + e, w);
+      } else if (e < cur.n) {
+        const int cnt = min(kVec, cur.n - e);
+        for (int j = 0; j < cnt; ++j) {
+          float ww = wbase[cur.m0 + e + j], mm = p.exp_avg[cur.l0 + e + j], vv = p.exp_avg_sq[cur.l0 + e + j];
+          adamw1(__fmul_rn(p.main_grad[cur.l0 + e + j], c), cur.decay, p, ss, ww, mm, vv);
+          wbase[cur.m0 + e + j] = ww;
+          p.exp_avg[cur.l0 + e + j] = mm;
+          p.exp_avg_sq[cur.l0 + e + j] = vv;
+          ParamT<PT>::store1(p.param, cur.w0 + e + j, ww);
+        }
+      }
+    }
+    if (more) cur = nxt;
+  }
+}
+
+template <typename PT>
+int launch_k3_t(K3Params& kp, cudaStream_t s) {
+  auto kern = k3_adamw_pipe<PT>;
+  int grid = 0;
+  int st = grid_for(kern, kp.tab.n_tiles, &grid);
+  if (st) return st;
+  kern<<<grid, kThreads, 0, s>>>(kp);
+  return check_launch("k3_adamw launch");
+}
+
+int launch_k3(int32_t param_dtype, K3Params& kp, const Run* runs, int count, cudaStream_t s) {
+  fill_table(kp.tab, runs, count, kTile3, -1);
+  switch (param_dtype) {
+    case DOPT_BF16: return launch_k3_t<__nv_bfloat16>(kp, s);
+    case DOPT_F16: return launch_k3_t<__half>(kp, s);
+    default: return launch_k3_t<float>(kp, s);
+  }
+}
+
+}  // namespace dopt

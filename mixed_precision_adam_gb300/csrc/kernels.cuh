@@ -1,0 +1,230 @@
+// kernels.cuh -- what the device kernels of the sharded mixed-precision Adam
+// step share: launch constants, the run table passed to every kernel, the
+// kernel-parameter blocks, the workspace layout, and the host-side launch
+// helpers.  Included by every CUDA translation unit of the library:
+//   k1_f32.cu, k1_bf16.cu, k1_f16.cu -- K1 reduce/prepare, one grad dtype each
+//   k3.cu                             -- K3 AdamW + cast back
+//   dopt_cuda.cu                      -- K2 finalize and the C entry points
+//
+// The step is three HBM-bound passes over the selected shard(s):
+//   K1 reduce_prepare : reads the N replica grads of every element, sums
+//                       them (emulated reduce-scatter), rounds to the grad
+//                       dtype, unscales, writes the fp32 main grad and keeps
+//                       per-CTA partials of the sum of squares and of the
+//                       non-finite flag.
+//   K2 finalize       : one CTA sums the partials in a fixed order and decides
+//                       norm, clip coefficient and skip on the device.
+//   K3 adamw          : reads main grad, master, m, v once, writes master, m,
+//                       v and the 16-bit param at its buffer offset once.
+// No tensor cores: nothing here is a contraction.  The work is described to
+// the kernels by a table of runs (contiguous in both the flat shard and the
+// buffer) passed by value as a __grid_constant__ kernel parameter, so a step
+// needs no host-to-device copy and no library-owned device memory.  Each run
+// is cut into tiles; CTAs take tiles round-robin.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <string>
+
+#include "dopt_internal.h"
+
+#ifndef DOPT_K1_UNROLL
+#define DOPT_K1_UNROLL 2
+#endif
+#ifndef DOPT_K3_UNROLL
+#define DOPT_K3_UNROLL 1
+#endif
+#ifndef DOPT_K1_TMA
+#define DOPT_K1_TMA 1  // 1: single-instance reduce stages replica tiles through shared memory with TMA
+#endif
+#ifndef DOPT_TMA_STAGES
+#define DOPT_TMA_STAGES 2
+#endif
+#ifndef DOPT_TMA_TILE
+#define DOPT_TMA_TILE 2048
+#endif
+#ifndef DOPT_TMA_EVICT_FIRST
+#define DOPT_TMA_EVICT_FIRST 1  // 1: the replica tiles are marked first to leave L2
+#endif
+#ifndef DOPT_K1_MIN_BLOCKS
+#define DOPT_K1_MIN_BLOCKS 2
+#endif
+#ifndef DOPT_K3_MIN_BLOCKS
+#define DOPT_K3_MIN_BLOCKS 4
+#endif
+
+namespace dopt {
+
+constexpr int kThreads = 256;              // threads per CTA
+constexpr int kVec = 4;                    // contiguous elements per thread access
+constexpr int kUnroll1 = DOPT_K1_UNROLL;   // K1 accesses per thread per tile
+constexpr int kUnroll3 = DOPT_K3_UNROLL;   // K3 accesses per thread per tile
+constexpr int kTile1 = kThreads * kVec * kUnroll1;  // K1 elements per tile
+constexpr int kTile3 = kThreads * kVec * kUnroll3;  // K3 elements per tile
+constexpr int kTmaTile = DOPT_TMA_TILE;    // elements per tile of the TMA-staged K1
+static_assert(kTmaTile % (kThreads * kVec) == 0, "TMA tile");
+constexpr int kMaxSeg = 960;               // runs per launch (kernel-parameter table)
+constexpr int kMaxGrid = 2048;             // partial slots per launch region
+constexpr int kBatch = 8;                  // replicas loaded together
+constexpr size_t kScalarBytes = 256;
+
+// A run whose flat-shard and buffer starts are both multiples of 8 elements
+// takes the vector paths.
+__host__ __device__ __forceinline__ bool seg_aligned(int64_t local, int64_t world) {
+  return ((local | world) & 7) == 0;
+}
+
+struct Seg {
+  int64_t local;   // first element in the flat shard arrays (rank slot included)
+  int64_t world;   // first element in the buffer
+  int32_t len;     // elements
+  int32_t tile0;   // first tile of this run in the launch
+  union {
+    double wd_mult;  // K3 tables: weight-decay multiplier of the run's param
+    int32_t bucket;  // K1 tables: the run's bucket, numbered across all buffers
+  };
+};
+static_assert(sizeof(Seg) == 32, "Seg layout");
+
+struct SegTable {
+  int32_t n_seg;
+  int32_t n_tiles;
+  Seg seg[kMaxSeg];
+};
+
+struct Partial {
+  double sumsq;
+  int32_t nonfinite;
+  int32_t zeros;  // main grads equal to zero
+};
+static_assert(sizeof(Partial) == 16, "Partial layout");
+
+// Device scalars of one step, at the start of the workspace: the public
+// dopt_step_stats layout.
+using Scalars = dopt_step_stats;
+static_assert(sizeof(Scalars) == 40, "dopt_step_stats layout");
+// Byte offset, inside the workspace's scalar area, of the word a reduce
+// kernel sets when it gives up waiting for its own copies; the finalize
+// pass reports it as dopt_step_stats.kernel_error and clears it.
+constexpr size_t kErrorFlagOffset = 128;
+// Byte offset of the step scalars the finalize pass computes when the step
+// number (and learning rate) live in device memory.
+constexpr size_t kDevStepOffset = 64;
+struct DevStep {
+  float step_size;  // (float)(lr / (1 - beta1^t))
+  float bc2_sqrt;   // (float)sqrt(1 - beta2^t)
+  double lr_wd;     // lr * weight_decay
+};
+constexpr int32_t kErrorMagic = 0x4B31544D;  // the flag's "set" value
+
+struct K1Params {
+  const void* rep[DOPT_MAX_REPLICAS];
+  float* main_grad;
+  Partial* partials;  // this launch's region of kMaxGrid slots (STATS only)
+  int32_t n_rep, n_inst;
+  float pre;        // (float)(1 / n_rep): prescale of average_in_collective = 0
+  float inv_dpi;    // (float)(1 / (n_rep / n_inst))
+  float inv_ninst;  // (float)(1 / n_inst)
+  float inv_scale;  // 1 / loss scale
+  int32_t average;
+  float post_scale; // scale_gradients factor on the reduced grad (1 = none)
+  int32_t* error_flag;  // set by a kernel that gave up waiting (TMA path)
+  int32_t starve_tile;  // test hook: CTA 0 never copies its tile of this index (-1: off)
+  int32_t pad;
+  // grad check (CHECK kernels only): amax[k * amax_stride + bucket] gathers
+  // the fp32 bits of replica k's largest |g| in that bucket (atomic max)
+  uint32_t* amax;
+  int64_t amax_stride;
+  SegTable tab;
+};
+
+struct K3Params {
+  const float* main_grad;
+  float* master;      // flat shard, or NULL when the param buffer is the master
+  float* exp_avg;
+  float* exp_avg_sq;
+  void* param;        // the whole param buffer
+  const float* coef;  // device scalar
+  const int32_t* found_inf;
+  const DevStep* dev;  // step scalars from the finalize pass, or NULL: use the fields below
+  double lr_wd;        // lr * weight_decay (host step)
+  float b1, b2, omb1, omb2, eps, step_size, bc2_sqrt;
+  int32_t pad;
+  SegTable tab;
+};
+
+static_assert(sizeof(K1Params) <= 32764 && sizeof(K3Params) <= 32764, "kernel parameter limit");
+
+// Advances the run cursor of a CTA to the run holding tile t (tiles visited
+// in increasing order, so the cursor only moves forward).
+__device__ __forceinline__ int seek(const SegTable& tab, int si, int t) {
+  while (si + 1 < tab.n_seg && tab.seg[si + 1].tile0 <= t) ++si;
+  return si;
+}
+
+// beta^t by binary powering in fp64 (host and device compute it the same way).
+__host__ __device__ __forceinline__ double pow_int(double b, int64_t t) {
+  double r = 1.0, x = b;
+  while (t > 0) {
+    if (t & 1) r *= x;
+    x *= x;
+    t >>= 1;
+  }
+  return r;
+}
+
+// ------------------------------------------------------- host-side launch --
+
+// SM count of the current device (cached per thread and device).
+int device_sms(int* sms);
+// Counts a launch and turns a launch error into a status.
+int check_launch(const char* what);
+
+// Grid of a tile-striding kernel: as many CTAs as fit on the GPU at once
+// (occupancy x SMs), at most one per tile and at most kMaxGrid.
+template <typename K>
+int grid_for(K kernel, int n_tiles, int* grid, size_t smem = 0) {
+  int sms = 0;
+  int st = device_sms(&sms);
+  if (st) return st;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+  if (e != cudaSuccess)
+    return fail(DOPT_E_CUDA, std::string("occupancy query: ") + cudaGetErrorString(e));
+  if (per_sm < 1) return fail(DOPT_E_CUDA, "occupancy query: the kernel does not fit on an SM");
+  *grid = std::max(1, std::min({per_sm * sms, kMaxGrid, std::max(1, n_tiles)}));
+  return DOPT_OK;
+}
+
+// Fills a launch's run table with runs[0, count) cut into tiles of
+// tile_elems; bucket_base >= 0 makes it a K1 table (each run records its
+// bucket as bucket_base + Run::bucket), otherwise a K3 table (each run
+// records its weight-decay multiplier).
+void fill_table(SegTable& tab, const Run* runs, int count, int tile_elems, int32_t bucket_base);
+
+// One K1 launch: a chunk of at most kMaxSeg runs and how to treat them.
+struct K1Launch {
+  const Run* runs;
+  int count;
+  int32_t bucket_base;  // number of the first bucket of the runs' buffer
+  bool full;            // replicas are whole grad buffers (else the flat shard)
+  bool stats;           // write the norm partials
+  bool check;           // gather the per-replica max |g| (needs stats)
+};
+
+// K1 over one launch, for one grad dtype (one translation unit each): picks
+// the kernel, fills kp.tab for that kernel's tile and launches it.  The
+// other fields of kp are filled by the caller.
+int launch_k1_f32(K1Params& kp, const K1Launch& l, cudaStream_t s);
+int launch_k1_bf16(K1Params& kp, const K1Launch& l, cudaStream_t s);
+int launch_k1_f16(K1Params& kp, const K1Launch& l, cudaStream_t s);
+// K3 over a chunk of runs for a param dtype; fills kp.tab.
+int launch_k3(int32_t param_dtype, K3Params& kp, const Run* runs, int count, cudaStream_t s);
+
+}  // namespace dopt

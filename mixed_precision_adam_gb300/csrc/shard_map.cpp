@@ -208,6 +208,22 @@ int32_t dopt_dp_size(const dopt_shard_map* m) {
   return m->dp;
 }
 
+int32_t dopt_total_buckets(const dopt_shard_map* m) {
+  if (!m) return dopt::fail(DOPT_E_INVALID, "dopt_total_buckets: NULL map");
+  int32_t n = 0;
+  for (const dopt::Buffer& buf : m->buffers) n += (int32_t)buf.buckets.size();
+  return n;
+}
+
+int32_t dopt_bucket_number(const dopt_shard_map* m, int32_t buffer, int32_t bucket) {
+  if (!m || buffer < 0 || buffer >= (int32_t)m->buffers.size() || bucket < 0 ||
+      bucket >= (int32_t)m->buffers[buffer].buckets.size())
+    return dopt::fail(DOPT_E_INVALID, "dopt_bucket_number: bad map, buffer or bucket");
+  int32_t n = 0;
+  for (int32_t b = 0; b < buffer; ++b) n += (int32_t)m->buffers[b].buckets.size();
+  return n + bucket;
+}
+
 int dopt_buffer_info_get(const dopt_shard_map* m, int32_t b, dopt_buffer_info* out) {
   if (!m || !out || b < 0 || b >= (int32_t)m->buffers.size())
     return dopt::fail(DOPT_E_INVALID, "dopt_buffer_info_get: bad map, buffer or out");

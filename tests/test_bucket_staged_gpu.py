@@ -17,45 +17,6 @@ if not torch.cuda.is_available():
 import gpu_harness as H  # noqa: E402
 
 
-def _staged_step(dc, reps, t, group, streams):
-    """Buckets reduced in backward order (bucket 0 first) on side streams,
-    each waiting on an event that marks its grads ready; finalize; updates in
-    forward order (last bucket first)."""
-    D = H.dopt()
-    hc = dc.hc
-    ws_bytes = D.dopt_workspace_bytes_bucketed(hc.pm, hc.rank_arg)
-    if getattr(dc, "bws", None) is None or dc.bws.numel() < ws_bytes:
-        dc.bws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    args = dc.step_args(reps, t)
-    args.c.workspace = dc.bws.data_ptr()
-    args.c.workspace_bytes = ws_bytes
-    main = torch.cuda.current_stream()
-    ready = []
-    for bi in range(len(hc.om.buffers)):
-        nbk = len(hc.om.buffers[bi].buckets)
-        for k0 in range(0, nbk, group):
-            ev = torch.cuda.Event()
-            ev.record(main)  # "the grads of these buckets are ready"
-            s = streams[(bi + k0) % len(streams)]
-            s.wait_event(ev)
-            args.set_stream(s)
-            D.dopt_step_reduce_buckets(args, bi, k0, min(group, nbk - k0))
-            done = torch.cuda.Event()
-            done.record(s)
-            ready.append(done)
-    for ev in ready:
-        main.wait_event(ev)
-    args.set_stream(main)
-    d_found = torch.zeros(1, dtype=torch.int32, device="cuda")
-    d_norm = torch.zeros(1, dtype=torch.float32, device="cuda")
-    D.dopt_step_finalize(args, d_found, d_norm)
-    for bi in range(len(hc.om.buffers)):
-        for k in reversed(range(len(hc.om.buffers[bi].buckets))):
-            D.dopt_step_update_buckets(args, bi, k, 1)
-    torch.cuda.synchronize()
-    return bool(d_found.item()), float(d_norm.item())
-
-
 @pytest.mark.parametrize("name,group", [("llama_7b_dp8_rank0", 1), ("gpt2_small_dp8", 2),
                                         ("llama_7b_dp16_2x8_1m", 3), ("llama_1p3b_fp16_dp8", 1)])
 def test_bucket_staged_equals_fused(name, group):
@@ -70,7 +31,7 @@ def test_bucket_staged_equals_fused(name, group):
         t = t_applied + 1
         f1, n1 = fused.step(grads, t)
         reps = [[staged._up(r) for r in g] for g in grads]
-        f2, n2 = _staged_step(staged, reps, t, group, streams)
+        f2, n2 = H.staged_step(staged, reps, t, group, streams)
         assert f1 == f2
         if not f1:
             assert n1 == n2
