@@ -2,7 +2,7 @@
 arrays) and the CUDA library (torch device tensors) -- runs optimizer steps
 on each, and compares the results element by element.
 
-Tolerances (from the benchmark spec of this path): shard map and
+Tolerances (the parity bar set for this path): shard map and
 found_inf bit-exact; fp32 master, m and v within 4 ulp or 1e-6 relative;
 16-bit params within 1 ulp of their type; grad norm within 1e-5 relative.
 The main grad (the reduced, unscaled fp32 gradient) follows the same fixed
