@@ -266,7 +266,7 @@ def encode_grad(gdt, value):
     v = np.float32(value)
     if gdt == F32:
         return v
-    return np.uint16(oracle.round_bf16(v) if gdt == BF16 else oracle.round_f16(v))
+    return (oracle.round_bf16(v) if gdt == BF16 else oracle.round_f16(v))[0]
 
 
 def plant(hc, grads, bi, k, w, value):
