@@ -114,17 +114,19 @@ def describe(cfg, n_elems):
 
 def algorithmic_bytes(D, pm, n_rep, ranks):
     """Per-stage algorithmic DRAM bytes of one step and the stepped element count.
-    K1 reads every replica element once and writes the fp32 main grad once;
-    K3 reads main grad, master, m, v once and writes master, m, v and (16-bit
-    buffers) the param once.  The fp32 buffer's master is its param buffer."""
+    K1 reads every replica element once and writes the main grad once (fp32,
+    or for 16-bit grads the reduced grad in the grad dtype); K3 reads that
+    main grad, master, m, v once and writes master, m, v and (16-bit buffers)
+    the param once.  The fp32 buffer's master is its param buffer."""
     k1 = k3 = elems = 0
     for b in range(D.dopt_num_buffers(pm)):
         info = D.dopt_buffer_info_get(pm, b)
         n = sum(s["gbuf_local"][1] - s["gbuf_local"][0]
                 for r in ranks for s in D.dopt_rank_shards(pm, b, r))
         elems += n
-        k1 += n * (n_rep * ELEM_BYTES[info["grad_dtype"]] + 4)
-        k3 += n * (16 + 12 + (ELEM_BYTES[info["param_dtype"]] if info["param_dtype"] != F32 else 0))
+        g = ELEM_BYTES[info["grad_dtype"]]  # the main grad between the passes takes g bytes too
+        k1 += n * (n_rep * g + g)
+        k3 += n * (g + 12 + 12 + (ELEM_BYTES[info["param_dtype"]] if info["param_dtype"] != F32 else 0))
     return k1, k3, elems
 
 

@@ -266,7 +266,9 @@ typedef struct {
   int32_t layout;                 /* dopt_layout of the replica grads          */
   int32_t average_in_collective;
   const void* const* const* replica_grads; /* [buffer][replica] device ptrs    */
-  float* const* main_grad;        /* [buffer] fp32 temporary                   */
+  float* const* main_grad;        /* [buffer] step temporary, 4 B x shard
+                                     numel (x ranks for DOPT_ALL_RANKS); see
+                                     below                                   */
   float* const* master;           /* [buffer]; NULL for fp32 buffers           */
   float* const* exp_avg;          /* [buffer]                                  */
   float* const* exp_avg_sq;       /* [buffer]                                  */
@@ -326,6 +328,18 @@ typedef struct {
    * extra memory traffic (the replica grads are read once either way). */
   float* grad_amax;
 } dopt_step_args;
+
+/* The main-grad buffers of dopt_step_args are scratch between the reduce
+ * pass and the AdamW pass of a fused or bucket-staged step.  For a buffer
+ * with fp32 grads they receive the fp32 main grads (the reduced grads times
+ * inv_loss_scale).  For a buffer with bf16/fp16 grads the reduced grads are
+ * values of the grad dtype, so the reduce pass stores them in that dtype, in
+ * the first half of the buffer (element i at 16-bit index i), and the AdamW
+ * pass forms the fp32 main grad fp32(g) * inv_loss_scale from them -- the
+ * same value, from half the bytes (the distrib_optimizer page's fp32 main
+ * grad copy, kept as its exact 16-bit source between the passes).  The
+ * separate entry points (dopt_grad_reduce_shard, dopt_prepare_grads,
+ * dopt_adam_step) always use fp32 main grads. */
 
 /* Statistics of the last step, kept at the start of its workspace:
  * the fp64 sum of squares (with the remote term), the reported norm (NaN

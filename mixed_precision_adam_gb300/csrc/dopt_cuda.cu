@@ -243,6 +243,7 @@ struct K1Job {
   uint32_t* amax = nullptr;  // grad check table, or NULL
   int64_t amax_stride = 0;   // buckets of all buffers
   int32_t bucket_base = 0;   // number of the buffer's first bucket
+  bool compact = false;      // 16-bit grads: keep the reduced grads in the grad dtype
 };
 
 // Launches K1 over every chunk of a run list; with stats, chunk i writes its
@@ -266,7 +267,7 @@ int run_k1_runs(const std::vector<Run>& runs, int region_first, const K1Job& j, 
     kp.post_scale = j.post_scale;
     kp.error_flag = j.ws ? reinterpret_cast<int32_t*>(static_cast<char*>(j.ws) + kErrorFlagOffset) : nullptr;
     kp.starve_tile = g_starve_tile.load(std::memory_order_relaxed);
-    kp.pad = 0;
+    kp.compact = j.compact && j.stats ? 1 : 0;
     kp.amax = j.amax;
     kp.amax_stride = j.amax_stride;
     const K1Launch l{runs.data() + c.first, c.count, j.bucket_base, j.full, j.stats, j.amax != nullptr};
@@ -308,6 +309,7 @@ K1Job step_job(const dopt_step_args* a, int32_t b) {
   j.amax = reinterpret_cast<uint32_t*>(a->grad_amax);
   j.amax_stride = bucket_number(m, (int32_t)m->buffers.size(), 0);
   j.bucket_base = bucket_number(m, b, 0);
+  j.compact = j.gdt != DOPT_F32;
   return j;
 }
 
@@ -370,21 +372,35 @@ int check_hparams(const dopt_adamw_hparams* hp, const char* fn) {
 }
 
 
-int run_k3_runs(const std::vector<Run>& runs, int32_t pdt, const float* main_grad, float* master,
-                float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
-                const float* d_coef, const int32_t* d_found, cudaStream_t s,
-                const DevStep* dev = nullptr) {
+// What a K3 pass does, apart from the runs it covers.
+struct K3Job {
+  int32_t param_dtype = DOPT_F32;
+  int32_t main_dtype = DOPT_F32;  // DOPT_F32, or the grad dtype for compact main grads
+  float inv_scale = 1.0f;         // compact main grads: main = widen(stored) * inv_scale
+  const float* main_grad = nullptr;
+  float* master = nullptr;
+  float* exp_avg = nullptr;
+  float* exp_avg_sq = nullptr;
+  void* param = nullptr;
+  const dopt_adamw_hparams* hp = nullptr;
+  const float* d_coef = nullptr;
+  const int32_t* d_found = nullptr;
+  const DevStep* dev = nullptr;   // device step scalars, or NULL: from hp
+};
+
+int run_k3_runs(const std::vector<Run>& runs, const K3Job& j, cudaStream_t s) {
+  const dopt_adamw_hparams* hp = j.hp;
   std::vector<Chunk> chunks = chunks_of(runs);
   for (const Chunk& c : chunks) {
     K3Params& kp = k3_scratch();
-    kp.main_grad = main_grad;
-    kp.master = master;
-    kp.exp_avg = exp_avg;
-    kp.exp_avg_sq = exp_avg_sq;
-    kp.param = param;
-    kp.coef = d_coef;
-    kp.found_inf = d_found;
-    kp.dev = dev;
+    kp.main_grad = j.main_grad;
+    kp.master = j.master;
+    kp.exp_avg = j.exp_avg;
+    kp.exp_avg_sq = j.exp_avg_sq;
+    kp.param = j.param;
+    kp.coef = j.d_coef;
+    kp.found_inf = j.d_found;
+    kp.dev = j.dev;
     kp.lr_wd = hp->lr * hp->weight_decay;
     kp.b1 = (float)hp->beta1;
     kp.b2 = (float)hp->beta2;
@@ -393,18 +409,32 @@ int run_k3_runs(const std::vector<Run>& runs, int32_t pdt, const float* main_gra
     kp.eps = (float)hp->eps;
     kp.step_size = (float)(hp->lr / (1.0 - pow_int(hp->beta1, hp->step)));
     kp.bc2_sqrt = (float)std::sqrt(1.0 - pow_int(hp->beta2, hp->step));
-    kp.pad = 0;
-    int st = launch_k3(pdt, kp, runs.data() + c.first, c.count, s);
+    kp.inv_scale = j.inv_scale;
+    int st = launch_k3(j.param_dtype, j.main_dtype, kp, runs.data() + c.first, c.count, s);
     if (st) return st;
   }
   return DOPT_OK;
 }
 
-int run_k3(dopt_shard_map* m, int32_t buffer, int32_t rank, const float* main_grad, float* master,
-           float* exp_avg, float* exp_avg_sq, void* param, const dopt_adamw_hparams* hp,
-           const float* d_coef, const int32_t* d_found, cudaStream_t s, const DevStep* dev = nullptr) {
-  return run_k3_runs(dopt::runs_for(m, buffer, rank), m->buffers[buffer].param_dtype, main_grad, master,
-                     exp_avg, exp_avg_sq, param, hp, d_coef, d_found, s, dev);
+// The K3 job of buffer b of a fused or bucket-staged step: a 16-bit grad
+// buffer's main grads arrive in their compact form (see step_job).
+K3Job step_job3(const dopt_step_args* a, int32_t b) {
+  const dopt_shard_map* m = a->map;
+  Scalars* sc = scalars_ptr(a->workspace);
+  K3Job j;
+  j.param_dtype = m->buffers[b].param_dtype;
+  j.main_dtype = m->buffers[b].grad_dtype;
+  j.inv_scale = a->inv_loss_scale;
+  j.main_grad = a->main_grad[b];
+  j.master = a->master[b];
+  j.exp_avg = a->exp_avg[b];
+  j.exp_avg_sq = a->exp_avg_sq[b];
+  j.param = a->param_buffer[b];
+  j.hp = &a->hp;
+  j.d_coef = &sc->clip_coef;
+  j.d_found = &sc->found_inf;
+  j.dev = a->d_step ? dev_step_ptr(a->workspace) : nullptr;
+  return j;
 }
 
 // ---- bucket-staged step: one partial region per (buffer, bucket, chunk) --
@@ -632,8 +662,17 @@ int dopt_adam_step(const dopt_shard_map* map, int32_t buffer, int32_t rank, cons
   if (!main_grad || !d_clip_coef || !d_found_inf)
     return dopt::fail(DOPT_E_INVALID, "dopt_adam_step: NULL main_grad, clip coef or found_inf");
   if (!aligned16(main_grad)) return dopt::fail(DOPT_E_ALIGN, "dopt_adam_step: main_grad not aligned");
-  return run_k3(m, buffer, rank, main_grad, master, exp_avg, exp_avg_sq, param_buffer, hp, d_clip_coef,
-                d_found_inf, (cudaStream_t)stream);
+  K3Job j;
+  j.param_dtype = m->buffers[buffer].param_dtype;
+  j.main_grad = main_grad;
+  j.master = master;
+  j.exp_avg = exp_avg;
+  j.exp_avg_sq = exp_avg_sq;
+  j.param = param_buffer;
+  j.hp = hp;
+  j.d_coef = d_clip_coef;
+  j.d_found = d_found_inf;
+  return run_k3_runs(runs_for(m, buffer, rank), j, (cudaStream_t)stream);
 }
 
 int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm) {
@@ -648,16 +687,12 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
     if ((st = run_k1(m, b, a->rank, step_job(a, b), s))) return st;
   }
   if ((st = record_stage(a, 1, s))) return st;
-  Scalars* sc = scalars_ptr(a->workspace);
   if ((st = run_k2(m, a->rank, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm, d_norm,
                    nullptr, d_found_inf, s, a)))
     return st;
   if ((st = record_stage(a, 2, s))) return st;
-  const DevStep* dev = a->d_step ? dev_step_ptr(a->workspace) : nullptr;
   for (int32_t b = 0; b < nb; ++b) {
-    st = run_k3(m, b, a->rank, a->main_grad[b], a->master[b], a->exp_avg[b], a->exp_avg_sq[b],
-                a->param_buffer[b], &a->hp, &sc->clip_coef, &sc->found_inf, s, dev);
-    if (st) return st;
+    if ((st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s))) return st;
   }
   return record_stage(a, 3, s);
 }
@@ -708,11 +743,7 @@ int dopt_step_update_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
   std::vector<dopt::Run> runs;
   for (int32_t k = bucket_first; k < bucket_first + bucket_count; ++k)
     runs.insert(runs.end(), by[k].begin(), by[k].end());
-  Scalars* sc = scalars_ptr(a->workspace);
-  return run_k3_runs(runs, m->buffers[buffer].param_dtype, a->main_grad[buffer], a->master[buffer],
-                     a->exp_avg[buffer], a->exp_avg_sq[buffer], a->param_buffer[buffer], &a->hp, &sc->clip_coef,
-                     &sc->found_inf, (cudaStream_t)a->stream,
-                     a->d_step ? dev_step_ptr(a->workspace) : nullptr);
+  return run_k3_runs(runs, step_job3(a, buffer), (cudaStream_t)a->stream);
 }
 
 namespace {

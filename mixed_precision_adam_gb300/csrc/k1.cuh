@@ -54,6 +54,9 @@ struct GradT<float> {
     x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
   }
   static __device__ __forceinline__ float round_to(float s) { return s; }
+  static constexpr bool kCompact = false;  // the reduced grad is the fp32 main grad itself
+  static __device__ __forceinline__ void store4c(void*, int64_t, const float*) {}
+  static __device__ __forceinline__ void store1c(void*, int64_t, float) {}
   // grad check
   static __device__ __forceinline__ uint32_t abs_bits(float x) { return __float_as_uint(x) & 0x7FFFFFFFu; }
   static __device__ __forceinline__ uint32_t abs4(const Raw& r) {
@@ -87,6 +90,16 @@ struct GradT<__nv_bfloat16> {
   }
   static __device__ __forceinline__ float round_to(float s) {
     return __bfloat162float(__float2bfloat16_rn(s));
+  }
+  // compact store of reduced grads that are bf16 values already (exact)
+  static constexpr bool kCompact = true;
+  static __device__ __forceinline__ void store4c(void* p, int64_t i, const float* r) {
+    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i),
+           make_uint2((__float_as_uint(r[0]) >> 16) | (__float_as_uint(r[1]) & 0xFFFF0000u),
+                      (__float_as_uint(r[2]) >> 16) | (__float_as_uint(r[3]) & 0xFFFF0000u)));
+  }
+  static __device__ __forceinline__ void store1c(void* p, int64_t i, float r) {
+    static_cast<unsigned short*>(p)[i] = (unsigned short)(__float_as_uint(r) >> 16);
   }
   // grad check: halves of |g| bits; bf16 is the top half of the same fp32
   static __device__ __forceinline__ uint32_t abs4(const Raw& r) {
@@ -124,6 +137,16 @@ struct GradT<__half> {
   }
   static __device__ __forceinline__ float round_to(float s) {
     return __half2float(__float2half_rn(s));
+  }
+  // compact store of reduced grads that are fp16 values already (exact)
+  static constexpr bool kCompact = true;
+  static __device__ __forceinline__ void store4c(void* p, int64_t i, const float* r) {
+    const unsigned a = __half_as_ushort(__float2half_rn(r[0])), b = __half_as_ushort(__float2half_rn(r[1]));
+    const unsigned c = __half_as_ushort(__float2half_rn(r[2])), d = __half_as_ushort(__float2half_rn(r[3]));
+    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i), make_uint2(a | (b << 16), c | (d << 16)));
+  }
+  static __device__ __forceinline__ void store1c(void* p, int64_t i, float r) {
+    static_cast<unsigned short*>(p)[i] = __half_as_ushort(__float2half_rn(r));
   }
   // grad check: halves of |g| bits, widened to fp32 bits once at the end
   // (the widening keeps the order, +inf and NaN)
@@ -189,14 +212,47 @@ __device__ __forceinline__ float post_scaled(float red, float post_scale) {
   return post_scale == 1.0f ? red : GradT<GT>::round_to(__fmul_rn(red, post_scale));
 }
 
+// The reduced grad of an element in the grad dtype, after scale_gradients
+// (before the unscale that makes it the fp32 main grad).
 template <typename GT>
-__device__ __forceinline__ float reduce_finish(const ReduceState& st, const K1Params& p) {
+__device__ __forceinline__ float reduce_value(const ReduceState& st, const K1Params& p) {
   float total = st.total;
   if (p.n_inst > 1) {
     if (p.average) total = __fmul_rn(total, p.inv_ninst);
     total = GradT<GT>::round_to(total);
   }
-  return __fmul_rn(post_scaled<GT>(total, p.post_scale), p.inv_scale);
+  return post_scaled<GT>(total, p.post_scale);
+}
+
+// Turns kVec reduced grads v (grad-dtype values) of main-grad index i into
+// fp32 main grads in place (v * inv_scale) and stores them, or, in the
+// compact form, stores the reduced grads themselves in the grad dtype first
+// (half the bytes; the AdamW pass forms the same main grads from them).
+template <typename GT, bool STATS>
+__device__ __forceinline__ void finish_store4(const K1Params& p, int64_t i, float* v) {
+  if constexpr (STATS && GradT<GT>::kCompact) {
+    if (p.compact) {
+      GradT<GT>::store4c(p.main_grad, i, v);
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) v[j] = __fmul_rn(v[j], p.inv_scale);
+      return;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) v[j] = __fmul_rn(v[j], p.inv_scale);
+  __stcs(reinterpret_cast<float4*>(p.main_grad + i), make_float4(v[0], v[1], v[2], v[3]));
+}
+template <typename GT, bool STATS>
+__device__ __forceinline__ float finish_store1(const K1Params& p, int64_t i, float r) {
+  const float m = __fmul_rn(r, p.inv_scale);
+  if constexpr (STATS && GradT<GT>::kCompact) {
+    if (p.compact) {
+      GradT<GT>::store1c(p.main_grad, i, r);
+      return m;
+    }
+  }
+  p.main_grad[i] = m;
+  return m;
 }
 
 // ---------------------------------------------------------- norm partials --
@@ -339,11 +395,13 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
 #pragma unroll
     for (int u = 0; u < kUnroll1; ++u) vec_ok[u] = aligned && ((u * kThreads + threadIdx.x) * kVec + kVec <= n);
 
-    // kBatch replicas x kUnroll1 accesses of kVec elements in flight
-    for (int k0 = 0; k0 < p.n_rep; k0 += kBatch) {
-      float x[kBatch][kUnroll1][kVec];
+    // B replicas x kUnroll1 accesses of kVec elements in flight (half as
+    // many with the check, whose maxima take registers too)
+    constexpr int B = CHECK ? kBatch / 2 : kBatch;
+    for (int k0 = 0; k0 < p.n_rep; k0 += B) {
+      float x[B][kUnroll1][kVec];
 #pragma unroll
-      for (int kk = 0; kk < kBatch; ++kk) {
+      for (int kk = 0; kk < B; ++kk) {
         if (k0 + kk < p.n_rep) {
 #pragma unroll
           for (int u = 0; u < kUnroll1; ++u) {
@@ -353,7 +411,7 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
         }
       }
 #pragma unroll
-      for (int kk = 0; kk < kBatch; ++kk) {
+      for (int kk = 0; kk < B; ++kk) {
         if (k0 + kk < p.n_rep) {
           const ReplicaPos rp = replica_pos(k0 + kk, dpi);
           uint32_t mx = 0u;
@@ -380,8 +438,8 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
       if (vec_ok[u]) {
         float m[kVec];
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) m[j] = reduce_finish<GT>(st[u][j], p);
-        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        for (int j = 0; j < kVec; ++j) m[j] = reduce_value<GT>(st[u][j], p);
+        finish_store4<GT, STATS>(p, l0 + e, m);
         if (STATS) acc.add4(m);
       } else if (e < n) {
         // scalar path: the ragged end of a run, or a run whose starts are
@@ -399,8 +457,7 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
               if (b) atomicMax(&s_amax[k], b);
             }
           }
-          float m = reduce_finish<GT>(s1, p);
-          p.main_grad[l0 + e + j] = m;
+          const float m = finish_store1<GT, STATS>(p, l0 + e + j, reduce_value<GT>(s1, p));
           if (STATS) acc.add1(m);
         }
       }
@@ -509,9 +566,9 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
 #pragma unroll
         for (int q = 0; q < kVec; ++q) {
           float tt = NINST > 1 ? GradT<GT>::round_to(total[u][q]) : total[u][q];
-          m[q] = __fmul_rn(post_scaled<GT>(tt, p.post_scale), inv_scale);
+          m[q] = post_scaled<GT>(tt, p.post_scale);
         }
-        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        finish_store4<GT, STATS>(p, l0 + e, m);
         if (STATS) acc.add4(m);
       } else if (e < n) {
         const int cnt = min(kVec, n - e);
@@ -531,8 +588,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
             tt = (j == 0) ? sum : __fadd_rn(tt, sum);
           }
           if (NINST > 1) tt = GradT<GT>::round_to(tt);
-          float m = __fmul_rn(post_scaled<GT>(tt, p.post_scale), inv_scale);
-          p.main_grad[l0 + e + q] = m;
+          const float m = finish_store1<GT, STATS>(p, l0 + e + q, post_scaled<GT>(tt, p.post_scale));
           if (STATS) acc.add1(m);
         }
       }
@@ -715,9 +771,9 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
           float sum = __fmul_rn(GradT<GT>::at(x[0], q), pre);
 #pragma unroll
           for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::at(x[k], q), pre));
-          m[q] = __fmul_rn(post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale), inv_scale);
+          m[q] = post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale);
         }
-        __stcs(reinterpret_cast<float4*>(p.main_grad + l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        finish_store4<GT, STATS>(p, l0 + e, m);
         if (STATS) acc.add4(m);
       } else if (e < n) {
         // the last few elements of a run: not in the staged copy
@@ -730,8 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
             sum = k == 0 ? term : __fadd_rn(sum, term);
             if (CHECK) amx[k] = GradT<GT>::amax(amx[k], GradT<GT>::abs1(p.rep[k], r0 + e + q));
           }
-          float m = __fmul_rn(post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale), inv_scale);
-          p.main_grad[l0 + e + q] = m;
+          const float m = finish_store1<GT, STATS>(p, l0 + e + q, post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale));
           if (STATS) acc.add1(m);
         }
       }

@@ -46,6 +46,60 @@ struct ParamT<float> {
   static __device__ __forceinline__ void store1(void*, int64_t, float) {}
 };
 
+// How the main grads reach K3: fp32 main grads, or (16-bit grad buffers in
+// the fused and bucket-staged steps) the reduced grads in the grad dtype,
+// from which main = fp32(stored) * inv_scale is formed exactly as K1 formed
+// it -- the same fp32 value, from half the bytes.
+template <typename MG>
+struct MainT;
+template <>
+struct MainT<float> {
+  using Raw = float4;
+  static __device__ __forceinline__ Raw load4(const float* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const float4*>(p + i));
+  }
+  static __device__ __forceinline__ void widen4(const Raw& r, float, float* g) {
+    g[0] = r.x; g[1] = r.y; g[2] = r.z; g[3] = r.w;
+  }
+  static __device__ __forceinline__ float load1(const float* p, int64_t i, float) { return p[i]; }
+};
+template <>
+struct MainT<__nv_bfloat16> {
+  using Raw = uint2;
+  static __device__ __forceinline__ Raw load4(const float* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(p) + i));
+  }
+  static __device__ __forceinline__ void widen4(const Raw& r, float inv_scale, float* g) {
+    g[0] = __fmul_rn(__uint_as_float(r.x << 16), inv_scale);
+    g[1] = __fmul_rn(__uint_as_float(r.x & 0xFFFF0000u), inv_scale);
+    g[2] = __fmul_rn(__uint_as_float(r.y << 16), inv_scale);
+    g[3] = __fmul_rn(__uint_as_float(r.y & 0xFFFF0000u), inv_scale);
+  }
+  static __device__ __forceinline__ float load1(const float* p, int64_t i, float inv_scale) {
+    const unsigned short b = reinterpret_cast<const unsigned short*>(p)[i];
+    return __fmul_rn(__uint_as_float((unsigned)b << 16), inv_scale);
+  }
+};
+template <>
+struct MainT<__half> {
+  using Raw = uint2;
+  static __device__ __forceinline__ Raw load4(const float* p, int64_t i) {
+    return __ldcs(reinterpret_cast<const uint2*>(reinterpret_cast<const unsigned short*>(p) + i));
+  }
+  static __device__ __forceinline__ float h(unsigned bits) {
+    return __half2float(__ushort_as_half((unsigned short)bits));
+  }
+  static __device__ __forceinline__ void widen4(const Raw& r, float inv_scale, float* g) {
+    g[0] = __fmul_rn(h(r.x & 0xFFFFu), inv_scale);
+    g[1] = __fmul_rn(h(r.x >> 16), inv_scale);
+    g[2] = __fmul_rn(h(r.y & 0xFFFFu), inv_scale);
+    g[3] = __fmul_rn(h(r.y >> 16), inv_scale);
+  }
+  static __device__ __forceinline__ float load1(const float* p, int64_t i, float inv_scale) {
+    return __fmul_rn(h(reinterpret_cast<const unsigned short*>(p)[i]), inv_scale);
+  }
+};
+
 // The decoupled weight-decay factor (float)(1 - lr*wd*wd_mult), formed in
 // fp64; out of line so no fp64 instruction is issued per element -- it runs
 // once per run change.
@@ -81,16 +135,18 @@ __device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, 
 // The AdamW pass with the loads of a thread's next tile issued before the
 // current tile is computed and stored, so the memory pipe stays busy while
 // the thread does arithmetic (software pipelining across tiles).
+template <typename MG>
 struct K3Tile {
-  float4 g[kUnroll3], w[kUnroll3], m[kUnroll3], v[kUnroll3];
+  typename MainT<MG>::Raw g[kUnroll3];
+  float4 w[kUnroll3], m[kUnroll3], v[kUnroll3];
   int64_t l0, w0, m0;
   int n;
   float decay;
   bool aligned;
 };
 
-template <typename PT>
-__device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, int& si, K3Tile& T,
+template <typename PT, typename MG>
+__device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, int& si, K3Tile<MG>& T,
                                         int& decay_si, float& decay, double lr_wd) {
   si = seek(p.tab, si, t);
   const Seg& sg = p.tab.seg[si];
@@ -109,7 +165,7 @@ __device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, 
   for (int u = 0; u < kUnroll3; ++u) {
     const int e = (u * kThreads + threadIdx.x) * kVec;
     if (T.aligned && e + kVec <= T.n) {
-      T.g[u] = __ldcs(reinterpret_cast<const float4*>(p.main_grad + T.l0 + e));
+      T.g[u] = MainT<MG>::load4(p.main_grad, T.l0 + e);
       T.w[u] = __ldcs(reinterpret_cast<const float4*>(wbase + T.m0 + e));
       T.m[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg + T.l0 + e));
       T.v[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg_sq + T.l0 + e));
@@ -117,7 +173,7 @@ __device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, 
   }
 }
 
-template <typename PT>
+template <typename PT, typename MG>
 __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(const __grid_constant__ K3Params p) {
   if (*p.found_inf) return;  // skipped step: nothing is written
   const float c = *p.coef;
@@ -127,17 +183,18 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
   float decay = 1.f;
   int t = blockIdx.x;
   if (t >= p.tab.n_tiles) return;
-  K3Tile cur;
-  k3_load<PT>(p, wbase, t, si, cur, decay_si, decay, ss.lr_wd);
+  K3Tile<MG> cur;
+  k3_load<PT, MG>(p, wbase, t, si, cur, decay_si, decay, ss.lr_wd);
   for (; t < p.tab.n_tiles; t += gridDim.x) {
-    K3Tile nxt;
+    K3Tile<MG> nxt;
     const bool more = t + (int)gridDim.x < p.tab.n_tiles;
-    if (more) k3_load<PT>(p, wbase, t + gridDim.x, si, nxt, decay_si, decay, ss.lr_wd);
+    if (more) k3_load<PT, MG>(p, wbase, t + gridDim.x, si, nxt, decay_si, decay, ss.lr_wd);
 #pragma unroll
     for (int u = 0; u < kUnroll3; ++u) {
       const int e = (u * kThreads + threadIdx.x) * kVec;
       if (cur.aligned && e + kVec <= cur.n) {
-        float g[kVec] = {cur.g[u].x, cur.g[u].y, cur.g[u].z, cur.g[u].w};
+        float g[kVec];
+        MainT<MG>::widen4(cur.g[u], p.inv_scale, g);
         float w[kVec] = {cur.w[u].x, cur.w[u].y, cur.w[u].z, cur.w[u].w};
         float m[kVec] = {cur.m[u].x, cur.m[u].y, cur.m[u].z, cur.m[u].w};
         float v[kVec] = {cur.v[u].x, cur.v[u].y, cur.v[u].z, cur.v[u].w};
@@ -151,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
         const int cnt = min(kVec, cur.n - e);
         for (int j = 0; j < cnt; ++j) {
           float ww = wbase[cur.m0 + e + j], mm = p.exp_avg[cur.l0 + e + j], vv = p.exp_avg_sq[cur.l0 + e + j];
-          adamw1(__fmul_rn(p.main_grad[cur.l0 + e + j], c), cur.decay, p, ss, ww, mm, vv);
+          adamw1(__fmul_rn(MainT<MG>::load1(p.main_grad, cur.l0 + e + j, p.inv_scale), c), cur.decay, p, ss,
+                 ww, mm, vv);
           wbase[cur.m0 + e + j] = ww;
           p.exp_avg[cur.l0 + e + j] = mm;
           p.exp_avg_sq[cur.l0 + e + j] = vv;
@@ -163,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
   }
 }
 
-template <typename PT>
+template <typename PT, typename MG>
 int launch_k3_t(K3Params& kp, cudaStream_t s) {
-  auto kern = k3_adamw_pipe<PT>;
+  auto kern = k3_adamw_pipe<PT, MG>;
   int grid = 0;
   int st = grid_for(kern, kp.tab.n_tiles, &grid);
   if (st) return st;
@@ -173,12 +231,21 @@ int launch_k3_t(K3Params& kp, cudaStream_t s) {
   return check_launch("k3_adamw launch");
 }
 
-int launch_k3(int32_t param_dtype, K3Params& kp, const Run* runs, int count, cudaStream_t s) {
+// Param and grad dtypes pair up as the buffers allow: a 16-bit param buffer
+// has grads in its own dtype or in fp32, an fp32 param buffer fp32 grads.
+int launch_k3(int32_t param_dtype, int32_t main_dtype, K3Params& kp, const Run* runs, int count,
+              cudaStream_t s) {
   fill_table(kp.tab, runs, count, kTile3, -1);
+  const bool compact = main_dtype != DOPT_F32;
+  if (compact && main_dtype != param_dtype)
+    return fail(DOPT_E_INVALID, "compact main grads need the grad dtype of the param buffer");
   switch (param_dtype) {
-    case DOPT_BF16: return launch_k3_t<__nv_bfloat16>(kp, s);
-    case DOPT_F16: return launch_k3_t<__half>(kp, s);
-    default: return launch_k3_t<float>(kp, s);
+    case DOPT_BF16:
+      return compact ? launch_k3_t<__nv_bfloat16, __nv_bfloat16>(kp, s) : launch_k3_t<__nv_bfloat16, float>(kp, s);
+    case DOPT_F16:
+      return compact ? launch_k3_t<__half, __half>(kp, s) : launch_k3_t<__half, float>(kp, s);
+    default:
+      return launch_k3_t<float, float>(kp, s);
   }
 }
 

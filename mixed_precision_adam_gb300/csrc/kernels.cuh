@@ -136,7 +136,8 @@ struct K1Params {
   float post_scale; // scale_gradients factor on the reduced grad (1 = none)
   int32_t* error_flag;  // set by a kernel that gave up waiting (TMA path)
   int32_t starve_tile;  // test hook: CTA 0 never copies its tile of this index (-1: off)
-  int32_t pad;
+  int32_t compact;      // 16-bit grads, statistics pass: store the reduced grads in the
+                        // grad dtype instead of the fp32 main grads (see store_main4)
   // grad check (CHECK kernels only): amax[k * amax_stride + bucket] gathers
   // the fp32 bits of replica k's largest |g| in that bucket (atomic max)
   uint32_t* amax;
@@ -155,7 +156,7 @@ struct K3Params {
   const DevStep* dev;  // step scalars from the finalize pass, or NULL: use the fields below
   double lr_wd;        // lr * weight_decay (host step)
   float b1, b2, omb1, omb2, eps, step_size, bc2_sqrt;
-  int32_t pad;
+  float inv_scale;     // compact main grads: main = widen(stored) * inv_scale
   SegTable tab;
 };
 
@@ -224,7 +225,10 @@ struct K1Launch {
 int launch_k1_f32(K1Params& kp, const K1Launch& l, cudaStream_t s);
 int launch_k1_bf16(K1Params& kp, const K1Launch& l, cudaStream_t s);
 int launch_k1_f16(K1Params& kp, const K1Launch& l, cudaStream_t s);
-// K3 over a chunk of runs for a param dtype; fills kp.tab.
-int launch_k3(int32_t param_dtype, K3Params& kp, const Run* runs, int count, cudaStream_t s);
+// K3 over a chunk of runs for a param dtype; fills kp.tab.  main_dtype is
+// DOPT_F32 for fp32 main grads, or the grad dtype (bf16/fp16) when K1 left
+// the reduced grads in their compact form.
+int launch_k3(int32_t param_dtype, int32_t main_dtype, K3Params& kp, const Run* runs, int count,
+              cudaStream_t s);
 
 }  // namespace dopt

@@ -358,6 +358,22 @@ def run_check(cfg, plants_per_step, staged_group=None):
     return ok, report
 
 
+def decode_main(raw, gdt, inv_scale, n):
+    """The fp32 main grads held in a main-grad buffer after a fused or
+    bucket-staged step: for an fp32 grad buffer the buffer itself; for a
+    bf16/fp16 grad buffer the first n 16-bit words hold the reduced grads in
+    the grad dtype, and main = fp32(word) * inv_scale, one fp32 rounding."""
+    raw = np.asarray(raw)
+    if gdt == F32:
+        return raw[:n]
+    bits = raw.view(np.uint16)[:n]
+    if gdt == BF16:
+        vals = (bits.astype(np.uint32) << 16).view(np.float32)
+    else:
+        vals = bits.view(np.float16).astype(np.float32)
+    return vals * np.float32(inv_scale)
+
+
 def ulp16(a, b):
     """Distance in ulps between 16-bit float bit patterns (bf16 or fp16)."""
     def key(x):
@@ -376,10 +392,12 @@ def state_close(got, want, before):
             np.abs(got.astype(np.float64) - want.astype(np.float64)) <= 1e-6 * scale)
 
 
-def compare_step(hc, dc, ores, found, norm, before, report):
+def compare_step(hc, dc, ores, found, norm, before, report, compact=True):
     """Compares the device state after a step with the oracle's.  `before`
-    holds the oracle's state before the step.  Appends findings to report
-    and returns True when every check passes."""
+    holds the oracle's state before the step; compact: the step was fused or
+    bucket-staged, so 16-bit grad buffers left their main grads in compact
+    form (decode_main).  Appends findings to report and returns True when
+    every check passes."""
     ok = True
     if bool(found) != bool(ores["found_inf"]):
         report.append(f"found_inf device={found} oracle={ores['found_inf']}")
@@ -398,7 +416,11 @@ def compare_step(hc, dc, ores, found, norm, before, report):
         mask = hc.piece_mask(bi)
         st = hc.state[bi]
         om_ = ores["main"][bi]
-        if not amax_equal(mains[bi][mask], om_[mask]):
+        got_main = mains[bi]
+        if compact:
+            got_main = decode_main(got_main, buf.grad_dtype, np.float32(1.0 / hc.cfg["loss_scale"]),
+                                   len(got_main))
+        if not amax_equal(got_main[mask], om_[mask]):
             report.append(f"buffer {bi}: main grad differs")
             ok = False
         checks = [("exp_avg", exp_avg[bi], st["exp_avg"], before[bi]["exp_avg"]),
@@ -450,7 +472,7 @@ def run_parity(cfg, steps=None, separate=False):
         before = snapshot(hc)
         ores = hc.oracle_step(grads, t)
         found, norm = dc.step_separate(grads, t) if separate else dc.step(grads, t)
-        good = compare_step(hc, dc, ores, found, norm, before, report)
+        good = compare_step(hc, dc, ores, found, norm, before, report, compact=not separate)
         report.append(f"step {t_step} (t={t}): found_inf={found} norm={norm:.9g} "
                       f"oracle={ores['norm']:.9g} coef={ores['coef']:.9g} ok={good}")
         ok &= good
@@ -653,7 +675,13 @@ class FullCase:
         for bi, s in st.items():
             lo = torch.tensor([x[2] for x in s["sel"]], dtype=torch.int64, device="cuda")
             w = torch.tensor([x[3] for x in s["sel"]], dtype=torch.int64, device="cuda")
-            g = {"main": self.main[bi][lo].cpu().numpy(), "exp_avg": self.m[bi][lo].cpu().numpy(),
+            buf = self.om.buffers[bi]
+            if buf.grad_dtype == F32:
+                main = self.main[bi][lo].cpu().numpy()
+            else:  # compact main grads (decode_main)
+                main = decode_main(self.main[bi].view(torch.int16)[lo].cpu().numpy(), buf.grad_dtype,
+                                   np.float32(1.0 / self.cfg["loss_scale"]), len(s["sel"]))
+            g = {"main": main, "exp_avg": self.m[bi][lo].cpu().numpy(),
                  "exp_avg_sq": self.v[bi][lo].cpu().numpy()}
             p = self.params[bi][w].cpu().numpy()
             g["param"] = p.view(np.uint16) if p.dtype == np.int16 else p
