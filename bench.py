@@ -360,19 +360,39 @@ class OracleSample:
         self.h = oracle.Hparams(**cfg["hp"])
         self.t = 0
 
-    def step(self):
+    def _reduce(self, lo, hi):
         c, L = self.ctypes, self.L
-        bad = L.or_reduce_prepare_run(self.arr, self.n_rep, self.cfg["n_inst"], self.gdt, 0, 0,
-                                      self.elements, c.c_float(1.0), c.c_float(self.inv_scale),
-                                      self.main.ctypes.data)
-        sumsq = L.or_sumsq_run(self.main.ctypes.data, self.elements)
+        bad = L.or_reduce_prepare_run(self.arr, self.n_rep, self.cfg["n_inst"], self.gdt, 0, lo,
+                                      hi - lo, c.c_float(1.0), c.c_float(self.inv_scale),
+                                      self.main.ctypes.data + 4 * lo)
+        return bad, L.or_sumsq_run(self.main.ctypes.data + 4 * lo, hi - lo)
+
+    def _adamw(self, lo, hi, coef, clip):
+        c = self.ctypes
+        self.L.or_adamw_run(self.main.ctypes.data + 4 * lo, hi - lo, coef, clip,
+                            self.master.ctypes.data + 4 * lo, self.m.ctypes.data + 4 * lo,
+                            self.v.ctypes.data + 4 * lo, c.byref(self.h), 1.0, self.t,
+                            self.out.ctypes.data + self.out.itemsize * lo, self.pdt)
+
+    def step(self, pool=None, threads=1):
+        """One oracle step over the sample: on one thread, or on `threads`
+        fixed chunks run by a thread pool (the C oracle runs without the
+        GIL), the chunks' sums of squares added in chunk order."""
+        c = self.ctypes
+        step = -(-self.elements // threads)
+        chunks = [(lo, min(self.elements, lo + step)) for lo in range(0, self.elements, step)]
+        run = (lambda f, args: [f(*a) for a in args]) if pool is None else \
+            (lambda f, args: list(pool.map(lambda a: f(*a), args)))
+        parts = run(self._reduce, chunks)
+        bad = sum(p[0] for p in parts)
+        sumsq = 0.0
+        for p in parts:
+            sumsq += p[1]
         norm, coef = c.c_double(), c.c_double()
-        clip = L.or_clip_coef(sumsq, self.cfg["max_norm"], c.byref(norm), c.byref(coef))
+        clip = self.L.or_clip_coef(sumsq, self.cfg["max_norm"], c.byref(norm), c.byref(coef))
         if bad == 0:
             self.t += 1
-            L.or_adamw_run(self.main.ctypes.data, self.elements, coef.value, clip,
-                           self.master.ctypes.data, self.m.ctypes.data, self.v.ctypes.data,
-                           c.byref(self.h), 1.0, self.t, self.out.ctypes.data, self.pdt)
+            run(self._adamw, [(lo, hi, coef.value, clip) for lo, hi in chunks])
 
     def describe(self):
         names = {F32: "fp32", BF16: "bf16", F16: "fp16"}
@@ -381,20 +401,44 @@ class OracleSample:
                 f"{names[self.gdt]} replicas")
 
 
-def cpu_baseline(cfg, seconds_target=12.0, max_passes=40):
-    """The oracle timed on the host over a bounded sample: repeated full
-    oracle steps on CPU_SAMPLE_ELEMENTS elements, at least seconds_target
-    seconds (at most max_passes steps)."""
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(sample, seconds_target, max_passes, threads):
+    """Repeated full oracle steps on the sample for at least seconds_target
+    seconds (at most max_passes): (passes, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+    pool = ThreadPoolExecutor(threads) if threads > 1 else None
+    try:
+        passes, t0 = 0, time.perf_counter()
+        while True:
+            sample.step(pool, threads)
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= seconds_target or passes >= max_passes:
+                return passes, el
+    finally:
+        if pool is not None:
+            pool.shutdown()
+
+
+def cpu_baseline(cfg, seconds_target=8.0, max_passes=40):
+    """The oracle timed on the host over a bounded sample of
+    CPU_SAMPLE_ELEMENTS elements: on every host core (fixed chunks, one per
+    core, the norm's partial sums added in chunk order) -- the reported value
+    -- and on one thread."""
     sample = OracleSample(cfg, CPU_SAMPLE_ELEMENTS)
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        sample.step()
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= seconds_target or passes >= max_passes:
-            break
-    return {"value": sample.elements * passes / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{sample.describe()}: {passes} full oracle steps in {el:.1f} s, one thread"}
+    cores = host_cores()
+    p1, e1 = time_oracle(sample, seconds_target, max_passes, 1)
+    pn, en = time_oracle(sample, seconds_target / 2, max_passes * cores, cores)
+    return {"value": sample.elements * pn / en, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{sample.describe()}: {pn} full oracle steps in {en:.1f} s on {cores} threads "
+                      f"(one chunk per thread); one thread: {p1} steps in {e1:.1f} s",
+            "value_one_thread": sample.elements * p1 / e1}
 
 
 REFERENCE_BUDGET_ELEMENTS = 600_000_000  # ~1 minute of oracle work per run
@@ -408,20 +452,26 @@ def run_reference(args):
     per_step = REFERENCE_BUDGET_ELEMENTS // max(1, args.steps + args.warmup)
     per_step = max(1 << 20, min(CPU_SAMPLE_ELEMENTS, per_step))
     sample = OracleSample(cfg, per_step)
+    cores = host_cores()
+    from concurrent.futures import ThreadPoolExecutor
+    pool = ThreadPoolExecutor(cores) if cores > 1 else None
     for _ in range(args.warmup):
-        sample.step()
+        sample.step(pool, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        sample.step()
+        sample.step(pool, cores)
     el = time.perf_counter() - t0
+    if pool is not None:
+        pool.shutdown()
     value = sample.elements * args.steps / el
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "impl": "reference",
             "config": {"workload": f"{cfg['name']}, a bounded sample per step (see cpu_baseline)"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"each step: {sample.describe()}, one thread"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: {sample.describe()}, {cores} threads "
+                                       "(one fixed chunk each)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
