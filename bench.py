@@ -289,7 +289,7 @@ def measured_peak_hbm():
         return 6800.0, "fallback"
 
 
-K1_SOURCES = ("kernels.cuh", "k1.cuh", "k1_f32.cu")
+K1_SOURCES = ("kernels.cuh", "tma.cuh", "k1.cuh", "k1_f32.cu")
 
 
 def k1_source_sha256():

@@ -353,11 +353,8 @@ typedef struct {
   int32_t found_inf;
   int32_t clipped;
   int64_t num_zeros;
-  int32_t kernel_error; /* 1: the reduce pass gave up waiting for its own data
-                           copies; the step was skipped (found_inf set).
-                           2: the AdamW pass gave up waiting; the step was
-                           applied in part.  Both are bounded waits on copies
-                           that always complete on a working GPU. */
+  int32_t kernel_error; /* nonzero: a kernel gave up waiting for its own data
+                           copies; the step was skipped (found_inf set) */
   int32_t reserved;
 } dopt_step_stats;
 
@@ -490,16 +487,13 @@ int dopt_loss_scaler_init(dopt_loss_scaler* s, double initial_scale, double grow
                           double min_scale);
 int dopt_loss_scaler_update(dopt_loss_scaler* s, int32_t found_inf);
 
-/* Test hook for the bounded waits of the TMA-staged passes: while set to
- * tile >= 0 for pass 1 (reduce/prepare) or pass 3 (AdamW), CTA 0 of every
- * TMA-staged launch of that pass announces its tile of that (CTA-local)
- * index but never copies it, so its wait runs out after about a second.
- * Pass 1: the step reports kernel_error 1, returns DOPT_E_CUDA from
- * dopt_step and is skipped.  Pass 3: kernel_error 2, DOPT_E_CUDA, and the
- * step is applied in part.  Either way the CUDA context stays usable.
- * tile -1 turns the pass's hook off (the default).  Not for production use.
- * Errors: DOPT_E_INVALID for another pass or tile < -1. */
-int dopt_debug_starve_copy(int32_t pass, int32_t tile);
+/* Test hook for the bounded waits of the TMA-staged reduce pass: while set
+ * to tile >= 0, CTA 0 of every such launch announces its tile of that
+ * (CTA-local) index but never copies it, so its wait runs out after about a
+ * second; the step then reports kernel_error, returns DOPT_E_CUDA from
+ * dopt_step and is skipped, and the CUDA context stays usable.  -1 turns the
+ * hook off (the default).  Not for production use. */
+int dopt_debug_starve_copy(int32_t tile);
 
 /* Number of kernels this library has launched in this process (all
  * devices, all threads); a caller can difference it around a region. */

@@ -140,7 +140,7 @@ _c = {
     "dopt_loss_scaler_update": _proto("dopt_loss_scaler_update", ctypes.c_int,
                                       ctypes.POINTER(dopt_loss_scaler), _I32),
     "dopt_kernel_launches": _proto("dopt_kernel_launches", ctypes.c_uint64),
-    "dopt_debug_starve_copy": _proto("dopt_debug_starve_copy", ctypes.c_int, _I32, _I32),
+    "dopt_debug_starve_copy": _proto("dopt_debug_starve_copy", ctypes.c_int, _I32),
     "dopt_read_step_stats": _proto("dopt_read_step_stats", ctypes.c_int, _P,
                                    ctypes.POINTER(dopt_step_stats), _P),
     "dopt_last_error": _proto("dopt_last_error", ctypes.c_char_p),
@@ -424,8 +424,8 @@ def dopt_read_step_stats(workspace, stream=None):
     return _struct_dict(st)
 
 
-def dopt_debug_starve_copy(pass_, tile):
-    _check(_c["dopt_debug_starve_copy"](pass_, tile))
+def dopt_debug_starve_copy(tile):
+    _check(_c["dopt_debug_starve_copy"](tile))
 
 
 def dopt_kernel_launches():

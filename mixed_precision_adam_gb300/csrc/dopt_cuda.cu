@@ -155,8 +155,7 @@ namespace {
 using namespace dopt;
 
 thread_local std::vector<char> t_param_scratch;  // kernel-parameter staging
-std::atomic<int32_t> g_starve_tile{-1};           // test hooks, see dopt_debug_starve_copy
-std::atomic<int32_t> g_starve_tile3{-1};
+std::atomic<int32_t> g_starve_tile{-1};           // test hook, see dopt_debug_starve_copy
 
 // The run table of one launch: runs [first, first + count) of a rank
 // selection, with per-run decay for K3.
@@ -387,7 +386,6 @@ struct K3Job {
   const float* d_coef = nullptr;
   const int32_t* d_found = nullptr;
   const DevStep* dev = nullptr;   // device step scalars, or NULL: from hp
-  int32_t* error = nullptr;       // where a TMA-staged pass reports a failed wait (NULL: no TMA)
 };
 
 int run_k3_runs(const std::vector<Run>& runs, const K3Job& j, cudaStream_t s) {
@@ -412,8 +410,6 @@ int run_k3_runs(const std::vector<Run>& runs, const K3Job& j, cudaStream_t s) {
     kp.step_size = (float)(hp->lr / (1.0 - pow_int(hp->beta1, hp->step)));
     kp.bc2_sqrt = (float)std::sqrt(1.0 - pow_int(hp->beta2, hp->step));
     kp.inv_scale = j.inv_scale;
-    kp.error = j.error;
-    kp.starve_tile = g_starve_tile3.load(std::memory_order_relaxed);
     int st = launch_k3(j.param_dtype, j.main_dtype, kp, runs.data() + c.first, c.count, s);
     if (st) return st;
   }
@@ -438,7 +434,6 @@ K3Job step_job3(const dopt_step_args* a, int32_t b) {
   j.d_coef = &sc->clip_coef;
   j.d_found = &sc->found_inf;
   j.dev = a->d_step ? dev_step_ptr(a->workspace) : nullptr;
-  j.error = &sc->kernel_error;
   return j;
 }
 
@@ -568,10 +563,9 @@ extern "C" {
 
 uint64_t dopt_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int dopt_debug_starve_copy(int32_t pass, int32_t tile) {
+int dopt_debug_starve_copy(int32_t tile) {
   if (tile < -1) return fail(DOPT_E_INVALID, "dopt_debug_starve_copy: tile < -1");
-  if (pass != 1 && pass != 3) return fail(DOPT_E_INVALID, "dopt_debug_starve_copy: pass must be 1 or 3");
-  (pass == 1 ? g_starve_tile : g_starve_tile3).store(tile, std::memory_order_relaxed);
+  g_starve_tile.store(tile, std::memory_order_relaxed);
   return DOPT_OK;
 }
 
@@ -804,11 +798,8 @@ int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_
   if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
   if (found_inf_out) *found_inf_out = host.found_inf;
   if (grad_norm_out) *grad_norm_out = host.grad_norm;
-  if (host.kernel_error == 1)
-    return fail(DOPT_E_CUDA, "dopt_step: a kernel gave up waiting for its own data copies; the step was skipped");
   if (host.kernel_error)
-    return fail(DOPT_E_CUDA,
-                "dopt_step: the AdamW pass gave up waiting for its own data copies; the step was applied in part");
+    return fail(DOPT_E_CUDA, "dopt_step: a kernel gave up waiting for its own data copies; the step was skipped");
   return DOPT_OK;
 }
 

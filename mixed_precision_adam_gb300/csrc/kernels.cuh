@@ -52,15 +52,6 @@
 #ifndef DOPT_TMA_EVICT_FIRST
 #define DOPT_TMA_EVICT_FIRST 1  // 1: the replica tiles are marked first to leave L2
 #endif
-#ifndef DOPT_K3_TMA
-#define DOPT_K3_TMA 1  // 1: the AdamW pass stages its four input streams through shared memory with TMA
-#endif
-#ifndef DOPT_K3_TMA_TILE
-#define DOPT_K3_TMA_TILE 2048
-#endif
-#ifndef DOPT_K3_TMA_STAGES
-#define DOPT_K3_TMA_STAGES 2
-#endif
 #ifndef DOPT_K1_MIN_BLOCKS
 #define DOPT_K1_MIN_BLOCKS 2
 #endif
@@ -163,12 +154,9 @@ struct K3Params {
   const float* coef;  // device scalar
   const int32_t* found_inf;
   const DevStep* dev;  // step scalars from the finalize pass, or NULL: use the fields below
-  int32_t* error;      // TMA-staged pass: set to 2 when it gives up waiting (NULL: no TMA)
   double lr_wd;        // lr * weight_decay (host step)
   float b1, b2, omb1, omb2, eps, step_size, bc2_sqrt;
   float inv_scale;     // compact main grads: main = widen(stored) * inv_scale
-  int32_t starve_tile; // test hook: CTA 0 never copies its tile of this index (-1: off)
-  int32_t pad;
   SegTable tab;
 };
 

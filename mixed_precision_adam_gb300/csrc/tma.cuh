@@ -1,4 +1,4 @@
-// tma.cuh -- the bulk-copy (TMA) staging both streaming passes use:
+// tma.cuh -- bulk-copy (TMA) staging for the streaming passes:
 // mbarrier waits bounded by the global timer, 1-D bulk copies from global
 // to shared memory with an L2 evict-first hint, and the once-per-device
 // raise of a kernel's dynamic shared-memory limit.
@@ -48,7 +48,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   }
 }
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-#if DOPT_TMA_EVICT_FIRST
+  if constexpr (DOPT_TMA_EVICT_FIRST) {
   uint64_t policy;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
   asm volatile(
@@ -56,13 +56,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
           smem_addr(dst)),
       "l"((unsigned long long)__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
-#else
+  } else {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_addr(dst)),
       "l"((unsigned long long)__cvta_generic_to_global(src)), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
-#endif
+  }
 }
 
 // Raises a kernel's dynamic shared-memory limit once per device (a later

@@ -196,14 +196,10 @@ def test_dynamic_loss_scaler_through_a_skipped_step():
     assert scaler.scale == 65536.0  # two clean steps after the backoff: growth
 
 
-@pytest.mark.parametrize("pass_", [1, 3])
-def test_bounded_wait_runs_out_and_reports(pass_):
-    """A tile whose copy is never issued (test hook): the TMA-staged pass
-    gives up after its bounded wait and the step reports a kernel error --
-    the reduce pass (1): the step is skipped and the state untouched; the
-    AdamW pass (3): the step is applied in part (the starved CTA's tiles keep
-    their old values).  The context stays usable and the next step is
-    correct."""
+def test_bounded_wait_runs_out_and_reports():
+    """A tile whose copy is never issued (test hook): the TMA-staged reduce
+    gives up after its bounded wait, the step is skipped and reported as a
+    kernel error, the state is untouched, and the next step is correct."""
     D = H.dopt()
     params = [dict(numel=300_000, dtype=1), dict(numel=4096, dtype=1)]
     cfg = _tiny(params, 2, bucket_size=None, steps=2)
@@ -211,28 +207,20 @@ def test_bounded_wait_runs_out_and_reports(pass_):
     dc = H.DeviceCase(hc)
     grads = hc.grads(1)
     before = dc.download()
-    D.dopt_debug_starve_copy(pass_, 0)
+    D.dopt_debug_starve_copy(0)
     try:
         with pytest.raises(D.DoptError) as e:
             dc.step(grads, 1)
     finally:
-        D.dopt_debug_starve_copy(pass_, -1)
+        D.dopt_debug_starve_copy(-1)
+    assert e.value.status == D.E_CUDA and "gave up waiting" in str(e.value)
     stats = D.dopt_read_step_stats(dc.ws)
+    assert stats["kernel_error"] == 1 and stats["found_inf"] == 1
     after = dc.download()
-    assert e.value.status == D.E_CUDA
-    if pass_ == 1:
-        assert "skipped" in str(e.value)
-        assert stats["kernel_error"] == 1 and stats["found_inf"] == 1
-        for b_list, a_list in zip(before[:4], after[:4]):
-            for b, a in zip(b_list, a_list):
-                if b is not None:
-                    assert b.tobytes() == a.tobytes()
-    else:
-        assert "applied in part" in str(e.value)
-        assert stats["kernel_error"] == 2 and stats["found_inf"] == 0
-        m0, m1 = before[3][0], after[3][0]  # exp_avg_sq of the bf16 buffer
-        assert (m0 != m1).any() and (m0 == m1).any()
-        dc = H.DeviceCase(hc)  # the partial step is not the oracle's: start again
+    for b_list, a_list in zip(before[:4], after[:4]):
+        for b, a in zip(b_list, a_list):
+            if b is not None:
+                assert b.tobytes() == a.tobytes()
     # the context is usable and the next step matches the oracle
     report = []
     snap = H.snapshot(hc)
