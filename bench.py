@@ -41,6 +41,7 @@ DEFAULT_WORKLOAD = "llama_7b_dp8_rank0"
 CPU_SAMPLE_ELEMENTS = 32 * 2**20
 F32, BF16, F16 = 0, 1, 2
 ELEM_BYTES = {F32: 4, BF16: 2, F16: 2}
+STATS_BYTES = 40  # sizeof(dopt_step_stats): the step's results read back to the host
 
 
 def log(*a):
@@ -570,52 +571,51 @@ def run_ours(args):
                 else:
                     hb.append(hb[k % len(hb)])
             host_reps.append(hb)
-        # two sets of device replica buffers: the copies of step i + 1's
-        # replicas run on a copy stream while step i runs on the main stream
-        dev_sets = [wl.reps, [[torch.empty_like(d) for d in db] for db in wl.reps]]
-        arg_sets = [sargs, wl.args(reps=dev_sets[1])]
+        # the C-ABI step with host replicas: the library copies each bucket's
+        # replica slices on its copy stream and reduces the bucket as soon as
+        # they land (dopt_step_from_host); it needs the bucket-staged workspace
+        ws_b = D.dopt_workspace_bytes_bucketed(wl.pm, wl.rank)
+        ws_staged = torch.empty(ws_b, dtype=torch.uint8, device="cuda")
+        eargs = wl.args()
+        eargs.c.workspace, eargs.c.workspace_bytes = ws_staged.data_ptr(), ws_b
         if args.check_grads:
-            arg_sets[1].set_grad_check(amax)
-        copy_stream = torch.cuda.Stream()
-        ready = [torch.cuda.Event(), torch.cuda.Event()]
+            eargs.set_grad_check(amax)
+        # bytes the library copies per step: every replica's part of each
+        # bucket that the step reads
+        h2d = 0
+        for b in range(D.dopt_num_buffers(wl.pm)):
+            info = D.dopt_buffer_info_get(wl.pm, b)
+            for k in range(info["n_buckets"]):
+                bk = D.dopt_bucket_info_get(wl.pm, b, k)
+                n = bk["numel"] if (wl.full and wl.all_ranks) else bk["shard_numel"]
+                h2d += n * ELEM_BYTES[info["grad_dtype"]] * wl.n_rep
+        eargs.set_step(wl.t_applied + 1)  # one untimed step (creates the copy stream)
+        if not D.dopt_step_from_host(eargs, host_reps)[0]:
+            wl.t_applied += 1
         torch.cuda.synchronize()
         distinct = len({id(h) for hb in host_reps for h in hb})
-        h2d = sum(per_rep)
         n_e2e = max(1, min(args.e2e_steps, args.steps))
-        main_stream = torch.cuda.current_stream()
-
-        def issue_copies(i):
-            # set i % 2 is free: the step that last read it has returned
-            # (dopt_step waits for its stream)
-            with torch.cuda.stream(copy_stream):
-                for hb, db in zip(host_reps, dev_sets[i % 2]):
-                    for h, d in zip(hb, db):
-                        d.copy_(h, non_blocking=True)
-                ready[i % 2].record(copy_stream)
-
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
         e0.record()
-        copy_stream.wait_stream(main_stream)
-        issue_copies(0)
-        for i in range(n_e2e):
-            if i + 1 < n_e2e:
-                issue_copies(i + 1)
-            main_stream.wait_event(ready[i % 2])
-            wl.step(arg_sets[i % 2])
+        for _ in range(n_e2e):
+            eargs.set_step(wl.t_applied + 1)
+            found, _ = D.dopt_step_from_host(eargs, host_reps)
+            if not found:
+                wl.t_applied += 1
         e1.record()
         torch.cuda.synchronize()
         wall = (time.perf_counter() - t0) * 1e3
         barrier(world)
         e2e_value, _ = aggregate(max(e0.elapsed_time(e1), wall), wl.elements, n_e2e, world)
-        del dev_sets, arg_sets
-        note = ("replica grads copied from pinned host memory each step (double-buffered: "
-                "step i + 1's copies overlap step i)")
+        del ws_staged
+        note = ("replica grads copied from pinned host memory each step by dopt_step_from_host, "
+                "bucket by bucket, each bucket reduced as soon as its copies land")
         if distinct < len(per_rep):
             note += f" ({distinct} distinct host buffers for {len(per_rep)} replicas: host memory bound)"
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": 32, "steps": n_e2e, "note": note}
+               "d2h_bytes_per_step": STATS_BYTES, "steps": n_e2e, "note": note}
         del host_reps
 
     if rank != 0:

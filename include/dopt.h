@@ -412,6 +412,34 @@ int dopt_step_update_buckets(const dopt_step_args* args, int32_t buffer, int32_t
                              int32_t bucket_count);
 
 /*
+ * One step whose replica gradients start in host memory (no counterpart in
+ * the pages, which start from grads already on the GPU: this is the front
+ * end for grads that arrive from the host, and the path the end-to-end
+ * benchmark times).  For every bucket of every buffer, in order, the
+ * library copies the part of each replica the step reads -- the selected
+ * rank's slice of the bucket (every rank's with DOPT_ALL_RANKS) in the full
+ * layout, the bucket's part of the flat shard in the shard-only layout --
+ * from host_replica_grads into the device replica buffers of args on
+ * copy_stream, and reduces the bucket on args->stream as soon as its copies
+ * have landed (dopt_step_reduce_buckets), so the reduce pass runs under the
+ * transfer; then it finalizes, updates every bucket, waits for args->stream
+ * and returns *found_inf_out and *grad_norm_out like dopt_step.
+ *   host_replica_grads -- [buffer][replica] host pointers, same layout and
+ *                   dtype as args->replica_grads; page-locked (pinned)
+ *                   memory for asynchronous copies (pageable memory works,
+ *                   with copies that do not overlap).
+ *   copy_stream   -- a stream other than args->stream (NULL: the library's
+ *                   own non-blocking stream for the current device).  It
+ *                   first waits for the work already on args->stream.
+ * The workspace must be the bucket-staged one (dopt_workspace_bytes_bucketed).
+ * The device replica buffers are overwritten; the call returns only after
+ * the step has finished, so the next call may reuse every buffer.
+ * Errors: as dopt_step; DOPT_E_INVALID for NULL host pointers.
+ */
+int dopt_step_from_host(const dopt_step_args* args, const void* const* const* host_replica_grads,
+                        dopt_stream copy_stream, int32_t* found_inf_out, float* grad_norm_out);
+
+/*
  * dopt_step_noalloc -- the fused step of dopt_step for callers that cannot
  * allocate device memory.  No page describes this entry point; it exists for
  * the library's users, not for the method.

@@ -125,6 +125,8 @@ _c = {
                               _P, _P),
     "dopt_step_noalloc": _proto("dopt_step_noalloc", ctypes.c_int, ctypes.POINTER(dopt_step_args),
                                 ctypes.POINTER(_I32), ctypes.POINTER(_F)),
+    "dopt_step_from_host": _proto("dopt_step_from_host", ctypes.c_int, ctypes.POINTER(dopt_step_args),
+                                  _P, _P, ctypes.POINTER(_I32), ctypes.POINTER(_F)),
     "dopt_workspace_bytes_bucketed": _proto("dopt_workspace_bytes_bucketed", _SZ, _P, _I32),
     "dopt_step_reduce_buckets": _proto("dopt_step_reduce_buckets", ctypes.c_int,
                                        ctypes.POINTER(dopt_step_args), _I32, _I32, _I32),
@@ -168,6 +170,8 @@ def _ptr(x):
         return None
     if hasattr(x, "data_ptr"):
         return x.data_ptr()
+    if hasattr(x, "__array_interface__"):  # numpy array (host memory)
+        return x.__array_interface__["data"][0]
     return int(x)
 
 
@@ -391,6 +395,20 @@ def dopt_step_noalloc(args):
     workspace (args' workspace is ignored); returns (found_inf, grad_norm)."""
     f, n = _I32(), _F()
     _check(_c["dopt_step_noalloc"](ctypes.byref(args.c), ctypes.byref(f), ctypes.byref(n)))
+    return bool(f.value), n.value
+
+
+def dopt_step_from_host(args, host_replica_grads, copy_stream=None):
+    """One step whose replica grads start in host memory: host_replica_grads
+    is a list per buffer of host arrays (pinned torch tensors or numpy
+    arrays) laid out like args' device replicas, which the library fills
+    bucket by bucket while it reduces; args needs the bucket-staged
+    workspace.  Returns (found_inf, grad_norm)."""
+    rows = [_ptr_array(reps) for reps in host_replica_grads]
+    table = (ctypes.POINTER(_P) * len(rows))(*[ctypes.cast(r, ctypes.POINTER(_P)) for r in rows])
+    f, n = _I32(), _F()
+    _check(_c["dopt_step_from_host"](ctypes.byref(args.c), ctypes.cast(table, _P), _stream(copy_stream),
+                                     ctypes.byref(f), ctypes.byref(n)))
     return bool(f.value), n.value
 
 

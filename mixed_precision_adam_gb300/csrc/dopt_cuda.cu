@@ -788,19 +788,119 @@ int dopt_step_noalloc(const dopt_step_args* a, int32_t* found_inf_out, float* gr
   return dopt_step(&with_scratch, found_inf_out, grad_norm_out);
 }
 
-int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {
-  int st = dopt_step_async(a, nullptr, nullptr);
-  if (st) return st;
+namespace {
+// Per thread and device: the copy stream of dopt_step_from_host when the
+// caller gives none, and the event that orders its copies with the step.
+struct HostCopyResources {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t ready = nullptr;
+};
+thread_local HostCopyResources t_host_copy[kMaxDevices];
+
+int host_copy_resources(HostCopyResources** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(DOPT_E_INVALID, "device index out of range");
+  HostCopyResources& r = t_host_copy[dev];
+  if (!r.stream) {
+    e = cudaStreamCreateWithFlags(&r.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r.ready, cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("copy stream: ") + cudaGetErrorString(e));
+  }
+  *out = &r;
+  return DOPT_OK;
+}
+
+// Reads the step scalars back and turns them into the results of a
+// synchronous step.
+int finish_sync_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out, const char* fn) {
   Scalars host{};
   cudaStream_t s = (cudaStream_t)a->stream;
   cudaError_t e = cudaMemcpyAsync(&host, a->workspace, sizeof(Scalars), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return dopt::fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
   if (found_inf_out) *found_inf_out = host.found_inf;
   if (grad_norm_out) *grad_norm_out = host.grad_norm;
   if (host.kernel_error)
-    return fail(DOPT_E_CUDA, "dopt_step: a kernel gave up waiting for its own data copies; the step was skipped");
+    return fail(DOPT_E_CUDA,
+                std::string(fn) + ": a kernel gave up waiting for its own data copies; the step was skipped");
   return DOPT_OK;
+}
+}  // namespace
+
+int dopt_step_from_host(const dopt_step_args* a, const void* const* const* host_replica_grads,
+                        dopt_stream copy_stream, int32_t* found_inf_out, float* grad_norm_out) {
+  const char* fn = "dopt_step_from_host";
+  int st = check_step_args(a, true, fn);
+  if (st) return st;
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  const int32_t nb = (int32_t)m->buffers.size();
+  const int32_t n_rep = m->dp * a->n_instances;
+  if (!host_replica_grads) return fail(DOPT_E_INVALID, std::string(fn) + ": NULL host replica array");
+  for (int32_t b = 0; b < nb; ++b) {
+    if (!host_replica_grads[b]) return fail(DOPT_E_INVALID, std::string(fn) + ": NULL host replica array");
+    for (int32_t k = 0; k < n_rep; ++k)
+      if (!host_replica_grads[b][k]) return fail(DOPT_E_INVALID, std::string(fn) + ": NULL host replica pointer");
+  }
+  HostCopyResources* res = nullptr;
+  if ((st = host_copy_resources(&res))) return st;
+  cudaStream_t s = (cudaStream_t)a->stream;
+  cudaStream_t cs = copy_stream ? (cudaStream_t)copy_stream : res->stream;
+  if (cs == s) return fail(DOPT_E_INVALID, std::string(fn) + ": copy_stream must differ from args->stream");
+  auto cuda_ok = [&](cudaError_t e, const char* what) {
+    return e == cudaSuccess ? DOPT_OK : fail(DOPT_E_CUDA, std::string(fn) + ": " + what + ": " + cudaGetErrorString(e));
+  };
+  // the copies overwrite the device replicas: after the work already queued
+  if ((st = cuda_ok(cudaEventRecord(res->ready, s), "event record"))) return st;
+  if ((st = cuda_ok(cudaStreamWaitEvent(cs, res->ready, 0), "stream wait"))) return st;
+  if ((st = clear_amax(a, 0, bucket_number(m, nb, 0), s))) return st;
+  const bool full = a->layout == DOPT_LAYOUT_FULL_BUFFER;
+  int region = 0;  // bucketed workspace: regions in (buffer, bucket, chunk) order
+  for (int32_t b = 0; b < nb; ++b) {
+    const Buffer& buf = m->buffers[b];
+    const size_t esz = buf.grad_dtype == DOPT_F32 ? 4 : 2;
+    const std::vector<std::vector<Run>> by = runs_by_bucket(m, b, a->rank);
+    const K1Job j = step_job(a, b);
+    for (int32_t k = 0; k < (int32_t)buf.buckets.size(); ++k) {
+      const Bucket& bk = buf.buckets[k];
+      const int64_t slice = bk.numel / m->dp;
+      int64_t first, count;  // elements of every replica the bucket's reduce reads
+      if (!full) {
+        first = bk.shard_base;
+        count = slice;
+      } else if (a->rank == DOPT_ALL_RANKS) {
+        first = bk.offset;
+        count = bk.numel;
+      } else {
+        first = bk.offset + (int64_t)a->rank * slice;
+        count = slice;
+      }
+      for (int32_t r = 0; r < n_rep && count > 0; ++r) {
+        char* dst = static_cast<char*>(const_cast<void*>(a->replica_grads[b][r])) + first * esz;
+        const char* src = static_cast<const char*>(host_replica_grads[b][r]) + first * esz;
+        if ((st = cuda_ok(cudaMemcpyAsync(dst, src, (size_t)count * esz, cudaMemcpyHostToDevice, cs),
+                          "host-to-device copy")))
+          return st;
+      }
+      if ((st = cuda_ok(cudaEventRecord(res->ready, cs), "event record"))) return st;
+      if ((st = cuda_ok(cudaStreamWaitEvent(s, res->ready, 0), "stream wait"))) return st;
+      if ((st = run_k1_runs(by[k], region, j, s))) return st;
+      region += (int)chunks_of(by[k]).size();
+    }
+  }
+  if ((st = run_k2_slots(region * kMaxGrid, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm,
+                         nullptr, nullptr, nullptr, s, a)))
+    return st;
+  for (int32_t b = 0; b < nb; ++b)
+    if ((st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s))) return st;
+  return finish_sync_step(a, found_inf_out, grad_norm_out, fn);
+}
+
+int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {
+  int st = dopt_step_async(a, nullptr, nullptr);
+  if (st) return st;
+  return finish_sync_step(a, found_inf_out, grad_norm_out, "dopt_step");
 }
 
 }  // extern "C"
