@@ -108,9 +108,12 @@ def test_argument_errors():
     ws_bytes = D.dopt_workspace_bytes_bucketed(hc.pm, hc.rank_arg)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     args.c.workspace, args.c.workspace_bytes = ws.data_ptr(), ws_bytes
+    side = torch.cuda.Stream()  # a copy stream equal to the step's stream is refused
+    args.set_stream(side)
     with pytest.raises(D.DoptError) as e:
-        D.dopt_step_from_host(args, host, copy_stream=torch.cuda.current_stream())
+        D.dopt_step_from_host(args, host, copy_stream=side)
     assert e.value.status == D.E_INVALID
+    args.set_stream(torch.cuda.current_stream())
     bad = [list(h) for h in host]
     bad[0][1] = None
     with pytest.raises(D.DoptError) as e:
