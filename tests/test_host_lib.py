@@ -39,6 +39,11 @@ def _compare_maps(params, dp, bucket_size, grad_fp32, busbw):
     om = oracle.ShardMap(params, dp, None if bucket_size < 0 else bucket_size, grad_fp32, busbw)
     pm = dopt.dopt_build_shard_map(params, dp, bucket_size, grad_fp32, busbw)
     assert dopt.dopt_num_buffers(pm) == len(om.buffers)
+    # the grad-check table index: buckets numbered across buffers in order
+    assert dopt.dopt_total_buckets(pm) == sum(len(b.buckets) for b in om.buffers)
+    for bi, ob in enumerate(om.buffers):
+        for k in range(len(ob.buckets)):
+            assert dopt.dopt_bucket_number(pm, bi, k) == oracle.bucket_number(om, bi, k)
     for bi, ob in enumerate(om.buffers):
         info = dopt.dopt_buffer_info_get(pm, bi)
         assert (info["param_dtype"], info["grad_dtype"], info["numel"], info["numel_unpadded"],
@@ -200,3 +205,10 @@ def test_bad_arguments_return_status():
     with pytest.raises(dopt.DoptError) as e:
         dopt.dopt_adam_step(mf, 0, 0, 16, 16, 16, 16, 16, W.HP, 1, 16, 16)
     assert e.value.status == dopt.E_INVALID  # fp32 buffer: master must be NULL
+
+    # bucket numbering outside the map
+    m = dopt.dopt_build_shard_map([dict(numel=100, dtype=1)], 2, -1, True, False)
+    for buffer, bucket in [(-1, 0), (1, 0), (0, 1), (0, -1)]:
+        with pytest.raises(dopt.DoptError) as e:
+            dopt.dopt_bucket_number(m, buffer, bucket)
+        assert e.value.status == dopt.E_INVALID
