@@ -501,7 +501,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
         amx[j][k] = 0u;
       }
   };
-  const float pre = p.pre, inv_scale = p.inv_scale;
+  const float pre = p.pre;
   for (int t = blockIdx.x; t < p.tab.n_tiles; t += gridDim.x) {
     si = seek(p.tab, si, t);
     const Seg& sg = p.tab.seg[si];
@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
     }
   };
   bool failed = false;
-  const float pre = p.pre, inv_scale = p.inv_scale;
+  const float pre = p.pre;
   int i = 0;
   for (; i < my; ++i) {
     const int stage = i % S;

@@ -140,24 +140,48 @@ class HostCase:
 class DeviceCase:
     """The same inputs on the GPU, stepped through the library's C ABI."""
 
+    # Every device buffer sits between two guard regions of GUARD_BYTES
+    # filled with a canary pattern; check_guards() finds any write outside a
+    # buffer (the pool has no memory checker, so the tests look themselves).
+    GUARD_BYTES = 256
+    CANARY = 0xA5
+
     def __init__(self, hc):
         import torch
         D = dopt()
         self.hc = hc
         self.torch = torch
-        dev = torch.device("cuda")
+        self.guarded = []
         self.params = [self._up(p) for p in hc.params]
         self.master = [self._up(st["master"]) if "master" in st else None for st in hc.state]
         self.exp_avg = [self._up(st["exp_avg"]) for st in hc.state]
         self.exp_avg_sq = [self._up(st["exp_avg_sq"]) for st in hc.state]
-        self.main = [torch.zeros(len(st["exp_avg"]), dtype=torch.float32, device=dev)
-                     for st in hc.state]
+        self.main = [self._alloc(len(st["exp_avg"]), torch.float32).zero_() for st in hc.state]
         self.ws_bytes = D.dopt_workspace_bytes(hc.pm, hc.rank_arg)
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.ws = self._alloc(self.ws_bytes, torch.uint8)
+
+    def _alloc(self, n, dtype):
+        """A device tensor of n elements between two canary-filled guards."""
+        torch = self.torch
+        es = torch.empty(0, dtype=dtype).element_size()
+        g = self.GUARD_BYTES
+        raw = torch.full((2 * g + n * es,), self.CANARY, dtype=torch.uint8, device="cuda")
+        self.guarded.append((raw, n * es))
+        return raw[g:g + n * es].view(dtype)
 
     def _up(self, a):
-        t = self.torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a.copy())
-        return t.cuda()
+        src = self.torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a.copy())
+        t = self._alloc(src.numel(), src.dtype)
+        t.copy_(src)
+        return t
+
+    def check_guards(self):
+        """True when no guard byte of any buffer has changed."""
+        g = self.GUARD_BYTES
+        for raw, nbytes in self.guarded:
+            if not (bool((raw[:g] == self.CANARY).all()) and bool((raw[g + nbytes:] == self.CANARY).all())):
+                return False
+        return True
 
     def step_args(self, reps, t, stream=None):
         D = dopt()
@@ -334,7 +358,7 @@ def run_check(cfg, plants_per_step, staged_group=None):
                            inv_scale=float(np.float32(1.0 / cfg["loss_scale"])),
                            max_norm=cfg["max_norm"], layout=cfg["layout"], n_inst=cfg["n_inst"],
                            average=cfg["average"], check_grads=True)
-        amax = torch_.full((hc.n_rep, total), 12345.0, dtype=torch_.float32, device="cuda")
+        amax = dc._alloc(hc.n_rep * total, torch_.float32).view(hc.n_rep, total).fill_(12345.0)
         reps = [[dc._up(r) for r in g] for g in grads]
         if staged_group:
             found, norm = staged_step(dc, reps, t, staged_group, streams, grad_amax=amax)
@@ -399,6 +423,9 @@ def compare_step(hc, dc, ores, found, norm, before, report, compact=True):
     form (decode_main).  Appends findings to report and returns True when
     every check passes."""
     ok = True
+    if hasattr(dc, "check_guards") and not dc.check_guards():
+        report.append("a write landed outside a device buffer (guard bytes changed)")
+        ok = False
     if bool(found) != bool(ores["found_inf"]):
         report.append(f"found_inf device={found} oracle={ores['found_inf']}")
         return False
