@@ -515,6 +515,45 @@ int dopt_loss_scaler_init(dopt_loss_scaler* s, double initial_scale, double grow
                           double min_scale);
 int dopt_loss_scaler_update(dopt_loss_scaler* s, int32_t found_inf);
 
+/* ---------------------------------------------------------------------------
+ * Reshardable optimizer state.  The distrib_optimizer page lists "fully
+ * reshardable" checkpoint formats, which do not depend on the internal
+ * buffer layout (no layout is printed).  Reading: state in model space.  The
+ * model space of a buffer holds its params in the order they were given to
+ * dopt_build_shard_map, each as one contiguous range of numel elements;
+ * it does not depend on the DP size, the bucket size or the padding.  A
+ * state saved in model space at one DP size loads at any other.
+ */
+typedef enum {
+  DOPT_STATE_FLAT_SHARD = 0,   /* fp32 master / exp_avg / exp_avg_sq of the
+                                  step: the rank's flat shard (all ranks'
+                                  slots, rank-major, for DOPT_ALL_RANKS) */
+  DOPT_STATE_PARAM_BUFFER = 1  /* the whole param buffer, in the param dtype
+                                  (for an fp32 buffer: its master) */
+} dopt_state_layout;
+
+/* Elements of `buffer`'s model space: the sum of its params' numel (< 0 on
+ * a bad map or buffer). */
+int64_t dopt_model_numel(const dopt_shard_map* map, int32_t buffer);
+
+/*
+ * Copies the elements that `rank` owns (every rank's with DOPT_ALL_RANKS)
+ * of one state tensor of `buffer` between its step layout and model space:
+ * to_model writes model[model index] = state[layout index], from_model the
+ * reverse; other elements of the destination are not touched (padding, and
+ * params or pieces of other ranks).  Elements are fp32 for
+ * DOPT_STATE_FLAT_SHARD and the param dtype for DOPT_STATE_PARAM_BUFFER.
+ * Either pointer may be device or host memory (one cudaMemcpyAsync per
+ * param piece, cudaMemcpyDefault, on `stream`; pageable host memory makes
+ * the copies synchronous).  A checkpoint gathers all ranks' pieces; a
+ * restore scatters each rank's own.  Errors: DOPT_E_INVALID (bad map,
+ * buffer, rank or layout, NULL pointer), DOPT_E_CUDA.
+ */
+int dopt_state_to_model(const dopt_shard_map* map, int32_t buffer, int32_t rank, int32_t layout,
+                        const void* state, void* model, dopt_stream stream);
+int dopt_state_from_model(const dopt_shard_map* map, int32_t buffer, int32_t rank, int32_t layout,
+                          const void* model, void* state, dopt_stream stream);
+
 /* Test hook for the bounded waits of the TMA-staged reduce pass: while set
  * to tile >= 0, CTA 0 of every such launch announces its tile of that
  * (CTA-local) index but never copies it, so its wait runs out after about a

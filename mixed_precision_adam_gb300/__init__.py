@@ -125,6 +125,9 @@ _c = {
                               _P, _P),
     "dopt_step_noalloc": _proto("dopt_step_noalloc", ctypes.c_int, ctypes.POINTER(dopt_step_args),
                                 ctypes.POINTER(_I32), ctypes.POINTER(_F)),
+    "dopt_model_numel": _proto("dopt_model_numel", _I64, _P, _I32),
+    "dopt_state_to_model": _proto("dopt_state_to_model", ctypes.c_int, _P, _I32, _I32, _I32, _P, _P, _P),
+    "dopt_state_from_model": _proto("dopt_state_from_model", ctypes.c_int, _P, _I32, _I32, _I32, _P, _P, _P),
     "dopt_step_from_host": _proto("dopt_step_from_host", ctypes.c_int, ctypes.POINTER(dopt_step_args),
                                   _P, _P, ctypes.POINTER(_I32), ctypes.POINTER(_F)),
     "dopt_workspace_bytes_bucketed": _proto("dopt_workspace_bytes_bucketed", _SZ, _P, _I32),
@@ -396,6 +399,24 @@ def dopt_step_noalloc(args):
     f, n = _I32(), _F()
     _check(_c["dopt_step_noalloc"](ctypes.byref(args.c), ctypes.byref(f), ctypes.byref(n)))
     return bool(f.value), n.value
+
+
+STATE_FLAT_SHARD, STATE_PARAM_BUFFER = 0, 1
+
+
+def dopt_model_numel(m, buffer):
+    return _check(_c["dopt_model_numel"](m, buffer))
+
+
+def dopt_state_to_model(m, buffer, rank, layout, state, model, stream=None):
+    """Copies the pieces rank (or ALL_RANKS) owns of a state tensor into
+    model space (buffer params in model order); device or host arrays."""
+    _check(_c["dopt_state_to_model"](m, buffer, rank, layout, _ptr(state), _ptr(model), _stream(stream)))
+
+
+def dopt_state_from_model(m, buffer, rank, layout, model, state, stream=None):
+    """The reverse of dopt_state_to_model."""
+    _check(_c["dopt_state_from_model"](m, buffer, rank, layout, _ptr(model), _ptr(state), _stream(stream)))
 
 
 def dopt_step_from_host(args, host_replica_grads, copy_stream=None):

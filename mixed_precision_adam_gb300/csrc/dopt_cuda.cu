@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "kernels.cuh"
@@ -895,6 +896,81 @@ int dopt_step_from_host(const dopt_step_args* a, const void* const* const* host_
   for (int32_t b = 0; b < nb; ++b)
     if ((st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s))) return st;
   return finish_sync_step(a, found_inf_out, grad_norm_out, fn);
+}
+
+namespace {
+// One param piece of a rank's shard: where it sits in the state layout and
+// in model space (elements), and its length.
+struct StatePiece {
+  int64_t state, model, len;
+};
+
+// The pieces of `rank` (every rank's for DOPT_ALL_RANKS) in `buffer`, with
+// their model-space offsets (the buffer's params in model order).
+std::vector<StatePiece> state_pieces(const dopt_shard_map* m, int32_t b, int32_t rank, int32_t layout) {
+  const Buffer& buf = m->buffers[b];
+  std::unordered_map<int32_t, int64_t> model_start;
+  int64_t acc = 0;
+  for (int32_t pid : buf.params) {
+    model_start[pid] = acc;
+    acc += m->params[pid].numel;
+  }
+  const int64_t S = buf.numel / m->dp;
+  const int32_t first = rank == DOPT_ALL_RANKS ? 0 : rank;
+  const int32_t last = rank == DOPT_ALL_RANKS ? m->dp - 1 : rank;
+  std::vector<StatePiece> out;
+  for (int32_t r = first; r <= last; ++r) {
+    for (const Bucket& bk : buf.buckets) {
+      const int64_t slice = bk.numel / m->dp;
+      const int64_t w0 = bk.offset + (int64_t)r * slice, w1 = w0 + slice;
+      for (int32_t pid : bk.params) {
+        const Param& p = m->params[pid];
+        const int64_t lo = std::max(p.start, w0), hi = std::min(p.end, w1);
+        if (hi <= lo) continue;
+        const int64_t state = layout == DOPT_STATE_FLAT_SHARD ? (int64_t)(r - first) * S + bk.shard_base + (lo - w0)
+                                                               : lo;
+        out.push_back(StatePiece{state, model_start[pid] + (lo - p.start), hi - lo});
+      }
+    }
+  }
+  return out;
+}
+
+int state_copy(const dopt_shard_map* map, int32_t b, int32_t rank, int32_t layout, const void* src, void* dst,
+               dopt_stream stream, bool to_model, const char* fn) {
+  int st = check_map_buffer_rank(map, b, rank, fn);
+  if (st) return st;
+  if (layout != DOPT_STATE_FLAT_SHARD && layout != DOPT_STATE_PARAM_BUFFER)
+    return fail(DOPT_E_INVALID, std::string(fn) + ": unknown state layout");
+  if (!src || !dst) return fail(DOPT_E_INVALID, std::string(fn) + ": NULL pointer");
+  const int32_t pdt = map->buffers[b].param_dtype;
+  const size_t es = layout == DOPT_STATE_FLAT_SHARD || pdt == DOPT_F32 ? 4 : 2;
+  for (const StatePiece& pc : state_pieces(map, b, rank, layout)) {
+    const int64_t from = to_model ? pc.state : pc.model, to = to_model ? pc.model : pc.state;
+    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dst) + to * es, static_cast<const char*>(src) + from * es,
+                                    (size_t)pc.len * es, cudaMemcpyDefault, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+  }
+  return DOPT_OK;
+}
+}  // namespace
+
+int64_t dopt_model_numel(const dopt_shard_map* map, int32_t buffer) {
+  if (!map || buffer < 0 || buffer >= (int32_t)map->buffers.size())
+    return fail(DOPT_E_INVALID, "dopt_model_numel: bad map or buffer");
+  int64_t n = 0;
+  for (int32_t pid : map->buffers[buffer].params) n += map->params[pid].numel;
+  return n;
+}
+
+int dopt_state_to_model(const dopt_shard_map* map, int32_t buffer, int32_t rank, int32_t layout,
+                        const void* state, void* model, dopt_stream stream) {
+  return state_copy(map, buffer, rank, layout, state, model, stream, true, "dopt_state_to_model");
+}
+
+int dopt_state_from_model(const dopt_shard_map* map, int32_t buffer, int32_t rank, int32_t layout,
+                          const void* model, void* state, dopt_stream stream) {
+  return state_copy(map, buffer, rank, layout, model, state, stream, false, "dopt_state_from_model");
 }
 
 int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {

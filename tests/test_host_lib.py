@@ -8,6 +8,7 @@ import os
 import random
 import re
 
+import numpy as np
 import pytest
 
 import oracle
@@ -206,6 +207,17 @@ def test_bad_arguments_return_status():
         dopt.dopt_adam_step(mf, 0, 0, 16, 16, 16, 16, 16, W.HP, 1, 16, 16)
     assert e.value.status == dopt.E_INVALID  # fp32 buffer: master must be NULL
 
+    # model-space state copies: bad buffer, rank, layout or pointer fail
+    # before any device work
+    pm2 = dopt.dopt_build_shard_map([dict(numel=100, dtype=1), dict(numel=7, dtype=0)], 2, -1, True, False)
+    assert [dopt.dopt_model_numel(pm2, b) for b in range(2)] == [100, 7]
+    arr = np.zeros(256, np.float32)
+    for args in [(2, 0, 0, arr, arr), (0, 2, 0, arr, arr), (0, -2, 0, arr, arr), (0, 0, 5, arr, arr),
+                 (0, 0, 0, None, arr), (0, 0, 0, arr, None)]:
+        for fn in (dopt.dopt_state_to_model, dopt.dopt_state_from_model):
+            with pytest.raises(dopt.DoptError) as e:
+                fn(pm2, *args)
+            assert e.value.status == dopt.E_INVALID
     # bucket numbering outside the map
     m = dopt.dopt_build_shard_map([dict(numel=100, dtype=1)], 2, -1, True, False)
     for buffer, bucket in [(-1, 0), (1, 0), (0, 1), (0, -1)]:
