@@ -36,26 +36,42 @@ struct K2Step {
   DevStep* out;
 };
 
-__global__ void __launch_bounds__(kThreads)
+constexpr int kFinThreads = 512;  // the finalize pass is one CTA
+
+__global__ void __launch_bounds__(kFinThreads)
 k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
             int remote_found_inf, double max_norm, Scalars* __restrict__ sc,
             float* d_norm, float* d_coef, int32_t* d_found, int32_t* err_flag, K2Step step) {
-  __shared__ double s_sum[kThreads];
-  __shared__ int s_bad[kThreads];
-  __shared__ long long s_zero[kThreads];
-  double v = 0.0;
+  __shared__ double s_sum[kFinThreads];
+  __shared__ int s_bad[kFinThreads];
+  __shared__ long long s_zero[kFinThreads];
+  // each thread sums its slots (stride kFinThreads) in four independent
+  // chains, so four loads are in flight; chains and threads are then added
+  // in a fixed order: the result does not depend on timing
+  double v[4] = {0.0, 0.0, 0.0, 0.0};
   int b = 0;
   long long z = 0;
-  for (int i = threadIdx.x; i < n_slots; i += kThreads) {
-    v += parts[i].sumsq;
-    b |= parts[i].nonfinite;
-    z += parts[i].zeros;
+  int i = threadIdx.x;
+  for (; i + 3 * kFinThreads < n_slots; i += 4 * kFinThreads) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const Partial pq = parts[i + q * kFinThreads];
+      v[q] += pq.sumsq;
+      b |= pq.nonfinite;
+      z += pq.zeros;
+    }
   }
-  s_sum[threadIdx.x] = v;
+  for (; i < n_slots; i += kFinThreads) {
+    const Partial pq = parts[i];
+    v[0] += pq.sumsq;
+    b |= pq.nonfinite;
+    z += pq.zeros;
+  }
+  s_sum[threadIdx.x] = (v[0] + v[1]) + (v[2] + v[3]);
   s_bad[threadIdx.x] = b;
   s_zero[threadIdx.x] = z;
   __syncthreads();
-  for (int w = kThreads / 2; w > 0; w >>= 1) {
+  for (int w = kFinThreads / 2; w > 0; w >>= 1) {
     if (threadIdx.x < w) {
       s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
       s_bad[threadIdx.x] |= s_bad[threadIdx.x + w];
@@ -349,7 +365,7 @@ int run_k2_slots(int n_slots, void* ws, double remote_sumsq, int32_t remote_foun
     step.beta1 = a->hp.beta1;
     step.beta2 = a->hp.beta2;
   }
-  k2_finalize<<<1, kThreads, 0, s>>>(region_ptr(ws, 0), n_slots, remote_sumsq, remote_found ? 1 : 0,
+  k2_finalize<<<1, kFinThreads, 0, s>>>(region_ptr(ws, 0), n_slots, remote_sumsq, remote_found ? 1 : 0,
                                      max_norm, scalars_ptr(ws), d_norm, d_coef, d_found,
                                      reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset),
                                      step);
