@@ -26,93 +26,11 @@ namespace dopt {
 
 // ------------------------------------------------------------------- K2 --
 
-// The step number and learning rate of a step whose counter lives in device
-// memory: the finalize pass reads them, computes the step scalars for the
-// next step number and advances the counter only when the step is applied.
-struct K2Step {
-  int64_t* d_step;      // NULL: the host supplied the step scalars
-  const double* d_lr;   // NULL: lr below
-  double lr, wd, beta1, beta2;
-  DevStep* out;
-};
-
 constexpr int kFinThreads = 512;  // the finalize pass is one CTA
 
 __global__ void __launch_bounds__(kFinThreads)
-k2_finalize(const Partial* __restrict__ parts, int n_slots, double remote_sumsq,
-            int remote_found_inf, double max_norm, Scalars* __restrict__ sc,
-            float* d_norm, float* d_coef, int32_t* d_found, int32_t* err_flag, K2Step step) {
-  __shared__ double s_sum[kFinThreads];
-  __shared__ int s_bad[kFinThreads];
-  __shared__ long long s_zero[kFinThreads];
-  // each thread sums its slots (stride kFinThreads) in four independent
-  // chains, so four loads are in flight; chains and threads are then added
-  // in a fixed order: the result does not depend on timing
-  double v[4] = {0.0, 0.0, 0.0, 0.0};
-  int b = 0;
-  long long z = 0;
-  int i = threadIdx.x;
-  for (; i + 3 * kFinThreads < n_slots; i += 4 * kFinThreads) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const Partial pq = parts[i + q * kFinThreads];
-      v[q] += pq.sumsq;
-      b |= pq.nonfinite;
-      z += pq.zeros;
-    }
-  }
-  for (; i < n_slots; i += kFinThreads) {
-    const Partial pq = parts[i];
-    v[0] += pq.sumsq;
-    b |= pq.nonfinite;
-    z += pq.zeros;
-  }
-  s_sum[threadIdx.x] = (v[0] + v[1]) + (v[2] + v[3]);
-  s_bad[threadIdx.x] = b;
-  s_zero[threadIdx.x] = z;
-  __syncthreads();
-  for (int w = kFinThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
-      s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
-      s_bad[threadIdx.x] |= s_bad[threadIdx.x + w];
-      s_zero[threadIdx.x] += s_zero[threadIdx.x + w];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    const int kernel_error = *err_flag == kErrorMagic ? 1 : 0;
-    *err_flag = 0;
-    const double sumsq = s_sum[0] + remote_sumsq;
-    const int found = (s_bad[0] || remote_found_inf || kernel_error) ? 1 : 0;
-    const double norm = sqrt(sumsq);
-    double coef = 1.0;
-    int clip = 0;
-    if (max_norm > 0.0) {
-      coef = max_norm / (norm + 1.0e-6);
-      clip = coef < 1.0;
-    }
-    const float coef_f = clip ? (float)coef : 1.0f;
-    const float norm_f = found ? __int_as_float(0x7FC00000) : (float)norm;
-    sc->sumsq = sumsq;
-    sc->grad_norm = norm_f;
-    sc->clip_coef = coef_f;
-    sc->found_inf = found;
-    sc->clipped = clip;
-    sc->num_zeros = s_zero[0];
-    sc->kernel_error = kernel_error;
-    sc->reserved = 0;
-    if (d_norm) *d_norm = norm_f;
-    if (d_coef) *d_coef = coef_f;
-    if (d_found) *d_found = found;
-    if (step.d_step) {
-      const int64_t t = *step.d_step + 1;
-      const double lr = step.d_lr ? *step.d_lr : step.lr;
-      step.out->step_size = (float)(lr / (1.0 - pow_int(step.beta1, t)));
-      step.out->bc2_sqrt = (float)sqrt(1.0 - pow_int(step.beta2, t));
-      step.out->lr_wd = lr * step.wd;
-      if (!found) *step.d_step = t;  // a skipped step does not count
-    }
-  }
+k2_finalize(const FinalizeArgs f) {
+  finalize_block<kFinThreads>(f);
 }
 
 // ------------------------------------------- launch helpers (kernels.cuh) --
@@ -261,6 +179,8 @@ struct K1Job {
   int64_t amax_stride = 0;   // buckets of all buffers
   int32_t bucket_base = 0;   // number of the buffer's first bucket
   bool compact = false;      // 16-bit grads: keep the reduced grads in the grad dtype
+  const FinalizeArgs* fin = nullptr;  // finalize in the last launch's last CTA (fused step)
+  uint32_t* fin_counter = nullptr;
 };
 
 // Launches K1 over every chunk of a run list; with stats, chunk i writes its
@@ -287,6 +207,9 @@ int run_k1_runs(const std::vector<Run>& runs, int region_first, const K1Job& j, 
     kp.compact = j.compact && j.stats ? 1 : 0;
     kp.amax = j.amax;
     kp.amax_stride = j.amax_stride;
+    const bool last = &c == &chunks.back();
+    kp.fin_counter = (j.fin && last) ? j.fin_counter : nullptr;
+    if (kp.fin_counter) kp.fin = *j.fin;
     const K1Launch l{runs.data() + c.first, c.count, j.bucket_base, j.full, j.stats, j.amax != nullptr};
     int st;
     switch (j.gdt) {
@@ -353,22 +276,38 @@ DevStep* dev_step_ptr(void* ws) {
   return reinterpret_cast<DevStep*>(static_cast<char*>(ws) + kDevStepOffset);
 }
 
+// The finalize arguments of a step whose partial regions fill n_slots
+// slots of workspace ws (device step state from a when it has some).
+FinalizeArgs finalize_args(int n_slots, void* ws, double remote_sumsq, int32_t remote_found, double max_norm,
+                           float* d_norm, float* d_coef, int32_t* d_found, const dopt_step_args* a) {
+  FinalizeArgs f{};
+  f.parts = region_ptr(ws, 0);
+  f.n_slots = n_slots;
+  f.remote_found = remote_found ? 1 : 0;
+  f.remote_sumsq = remote_sumsq;
+  f.max_norm = max_norm;
+  f.sc = scalars_ptr(ws);
+  f.d_norm = d_norm;
+  f.d_coef = d_coef;
+  f.d_found = d_found;
+  f.err_flag = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset);
+  f.step = K2Step{nullptr, nullptr, 0.0, 0.0, 0.0, 0.0, dev_step_ptr(ws)};
+  if (a && a->d_step) {
+    f.step.d_step = a->d_step;
+    f.step.d_lr = a->d_lr;
+    f.step.lr = a->hp.lr;
+    f.step.wd = a->hp.weight_decay;
+    f.step.beta1 = a->hp.beta1;
+    f.step.beta2 = a->hp.beta2;
+  }
+  return f;
+}
+
 int run_k2_slots(int n_slots, void* ws, double remote_sumsq, int32_t remote_found, double max_norm,
                  float* d_norm, float* d_coef, int32_t* d_found, cudaStream_t s,
                  const dopt_step_args* a = nullptr) {
-  K2Step step{nullptr, nullptr, 0.0, 0.0, 0.0, 0.0, dev_step_ptr(ws)};
-  if (a && a->d_step) {
-    step.d_step = a->d_step;
-    step.d_lr = a->d_lr;
-    step.lr = a->hp.lr;
-    step.wd = a->hp.weight_decay;
-    step.beta1 = a->hp.beta1;
-    step.beta2 = a->hp.beta2;
-  }
-  k2_finalize<<<1, kFinThreads, 0, s>>>(region_ptr(ws, 0), n_slots, remote_sumsq, remote_found ? 1 : 0,
-                                     max_norm, scalars_ptr(ws), d_norm, d_coef, d_found,
-                                     reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset),
-                                     step);
+  k2_finalize<<<1, kFinThreads, 0, s>>>(
+      finalize_args(n_slots, ws, remote_sumsq, remote_found, max_norm, d_norm, d_coef, d_found, a));
   return check_launch("k2_finalize launch");
 }
 
@@ -700,14 +639,23 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
   cudaStream_t s = (cudaStream_t)a->stream;
   if ((st = record_stage(a, 0, s))) return st;
   if ((st = clear_amax(a, 0, bucket_number(m, nb, 0), s))) return st;
+  // the finalize runs in the last CTA of the last reduce launch: its ticket
+  // counter starts every step at zero
+  uint32_t* counter = reinterpret_cast<uint32_t*>(static_cast<char*>(a->workspace) + kFinCounterOffset);
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
+  const FinalizeArgs fin = finalize_args(total_regions(m, a->rank) * kMaxGrid, a->workspace, a->remote_sumsq,
+                                         a->remote_found_inf, a->max_norm, d_norm, nullptr, d_found_inf, a);
   for (int32_t b = 0; b < nb; ++b) {
-    if ((st = run_k1(m, b, a->rank, step_job(a, b), s))) return st;
+    K1Job j = step_job(a, b);
+    if (b == nb - 1) {
+      j.fin = &fin;
+      j.fin_counter = counter;
+    }
+    if ((st = run_k1(m, b, a->rank, j, s))) return st;
   }
   if ((st = record_stage(a, 1, s))) return st;
-  if ((st = run_k2(m, a->rank, a->workspace, a->remote_sumsq, a->remote_found_inf, a->max_norm, d_norm,
-                   nullptr, d_found_inf, s, a)))
-    return st;
-  if ((st = record_stage(a, 2, s))) return st;
+  if ((st = record_stage(a, 2, s))) return st;  // the finalize ran inside the last reduce launch
   for (int32_t b = 0; b < nb; ++b) {
     if ((st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s))) return st;
   }

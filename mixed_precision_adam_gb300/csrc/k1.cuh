@@ -468,7 +468,10 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
   if constexpr (CHECK) {
     if (cur_bucket >= 0) flush_bucket(cur_bucket);
   }
-  if (STATS) write_partial(acc, p.partials);
+  if (STATS) {
+    write_partial(acc, p.partials);
+    finalize_if_last(p);
+  }
 }
 
 // The common reductions: prescale by 1/N and sum (average_in_collective =
@@ -599,7 +602,10 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
   if constexpr (CHECK) {
     if (cur_bucket >= 0) flush_bucket(cur_bucket);
   }
-  if (STATS) write_partial(acc, p.partials);
+  if (STATS) {
+    write_partial(acc, p.partials);
+    finalize_if_last(p);
+  }
 }
 
 // ---------------------------------------------------------- K1 with TMA --
@@ -754,7 +760,10 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
   if constexpr (CHECK) {
     if (cur_bucket >= 0) flush_bucket(cur_bucket);
   }
-  if (STATS) write_partial(acc, p.partials);
+  if (STATS) {
+    write_partial(acc, p.partials);
+    finalize_if_last(p);
+  }
 }
 
 // ------------------------------------------------------------ launchers --

@@ -122,6 +122,34 @@ struct DevStep {
   double lr_wd;     // lr * weight_decay
 };
 constexpr int32_t kErrorMagic = 0x4B31544D;  // the flag's "set" value
+// Byte offset of the ticket counter of the in-kernel finalize: the CTAs of a
+// step's last reduce launch take tickets, and the last one finalizes.
+constexpr size_t kFinCounterOffset = 160;
+
+// The step number and learning rate of a step whose counter lives in device
+// memory: the finalize reads them, computes the step scalars for the next
+// step number and advances the counter only when the step is applied.
+struct K2Step {
+  int64_t* d_step;      // NULL: the host supplied the step scalars
+  const double* d_lr;   // NULL: lr below
+  double lr, wd, beta1, beta2;
+  DevStep* out;
+};
+
+// Everything the finalize (norm, clip coefficient, skip decision, step
+// statistics) reads and writes.
+struct FinalizeArgs {
+  const Partial* parts;  // every partial slot of the step, regions in order
+  int32_t n_slots;
+  int32_t remote_found;
+  double remote_sumsq, max_norm;
+  Scalars* sc;
+  float* d_norm;
+  float* d_coef;
+  int32_t* d_found;
+  int32_t* err_flag;
+  K2Step step;
+};
 
 struct K1Params {
   const void* rep[DOPT_MAX_REPLICAS];
@@ -142,6 +170,10 @@ struct K1Params {
   // the fp32 bits of replica k's largest |g| in that bucket (atomic max)
   uint32_t* amax;
   int64_t amax_stride;
+  // in-kernel finalize (the last reduce launch of a fused step): the last
+  // CTA to take a ticket from *fin_counter runs it; NULL: none
+  uint32_t* fin_counter;
+  FinalizeArgs fin;
   SegTable tab;
 };
 
@@ -178,6 +210,107 @@ __host__ __device__ __forceinline__ double pow_int(double b, int64_t t) {
     t >>= 1;
   }
   return r;
+}
+
+// The finalize, run by one CTA of NT threads: sums the partial slots in a
+// fixed order (each thread its slots at stride NT in four independent
+// chains, then chains and threads in a fixed tree), adds the remote terms,
+// and decides norm, clip coefficient and skip; writes the step statistics,
+// the optional device results and the device step scalars.  Partials are
+// read past L1 (they may have been written by other SMs moments before).
+template <int NT>
+__device__ __forceinline__ void finalize_block(const FinalizeArgs& f) {
+  __shared__ double s_sum[NT];
+  __shared__ int s_bad[NT];
+  __shared__ long long s_zero[NT];
+  double v[4] = {0.0, 0.0, 0.0, 0.0};
+  int b = 0;
+  long long z = 0;
+  int i = threadIdx.x;
+  const double* sum_p = reinterpret_cast<const double*>(f.parts);
+  const int2* flag_p = reinterpret_cast<const int2*>(f.parts);
+  for (; i + 3 * NT < f.n_slots; i += 4 * NT) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = i + q * NT;
+      v[q] += __ldcg(sum_p + 2 * j);
+      const int2 fz = __ldcg(flag_p + 2 * j + 1);
+      b |= fz.x;
+      z += fz.y;
+    }
+  }
+  for (; i < f.n_slots; i += NT) {
+    v[0] += __ldcg(sum_p + 2 * i);
+    const int2 fz = __ldcg(flag_p + 2 * i + 1);
+    b |= fz.x;
+    z += fz.y;
+  }
+  s_sum[threadIdx.x] = (v[0] + v[1]) + (v[2] + v[3]);
+  s_bad[threadIdx.x] = b;
+  s_zero[threadIdx.x] = z;
+  __syncthreads();
+  for (int w = NT / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) {
+      s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
+      s_bad[threadIdx.x] |= s_bad[threadIdx.x + w];
+      s_zero[threadIdx.x] += s_zero[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int kernel_error = __ldcg(f.err_flag) == kErrorMagic ? 1 : 0;
+    *f.err_flag = 0;
+    const double sumsq = s_sum[0] + f.remote_sumsq;
+    const int found = (s_bad[0] || f.remote_found || kernel_error) ? 1 : 0;
+    const double norm = sqrt(sumsq);
+    double coef = 1.0;
+    int clip = 0;
+    if (f.max_norm > 0.0) {
+      coef = f.max_norm / (norm + 1.0e-6);
+      clip = coef < 1.0;
+    }
+    const float coef_f = clip ? (float)coef : 1.0f;
+    const float norm_f = found ? __int_as_float(0x7FC00000) : (float)norm;
+    Scalars* sc = f.sc;
+    sc->sumsq = sumsq;
+    sc->grad_norm = norm_f;
+    sc->clip_coef = coef_f;
+    sc->found_inf = found;
+    sc->clipped = clip;
+    sc->num_zeros = s_zero[0];
+    sc->kernel_error = kernel_error;
+    sc->reserved = 0;
+    if (f.d_norm) *f.d_norm = norm_f;
+    if (f.d_coef) *f.d_coef = coef_f;
+    if (f.d_found) *f.d_found = found;
+    const K2Step& st = f.step;
+    if (st.d_step) {
+      const int64_t t = *st.d_step + 1;
+      const double lr = st.d_lr ? *st.d_lr : st.lr;
+      st.out->step_size = (float)(lr / (1.0 - pow_int(st.beta1, t)));
+      st.out->bc2_sqrt = (float)sqrt(1.0 - pow_int(st.beta2, t));
+      st.out->lr_wd = lr * st.wd;
+      if (!found) *st.d_step = t;  // a skipped step does not count
+    }
+  }
+}
+
+// Called by every thread of every CTA of a reduce launch after its partial
+// is written (by thread 0): with a ticket counter set, the last CTA to take
+// a ticket runs the finalize and returns the counter to zero for the next
+// step.  No CTA waits for another.
+__device__ __forceinline__ void finalize_if_last(const K1Params& p) {
+  if (!p.fin_counter) return;
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's partial (and error flag) before its ticket
+    s_last = atomicAdd(p.fin_counter, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  finalize_block<kThreads>(p.fin);
+  if (threadIdx.x == 0) *p.fin_counter = 0u;
 }
 
 // ------------------------------------------------------- host-side launch --
