@@ -70,7 +70,7 @@ constexpr int kTile3 = kThreads * kVec * kUnroll3;  // K3 elements per tile
 constexpr int kTmaTile = DOPT_TMA_TILE;    // elements per tile of the TMA-staged K1
 static_assert(kTmaTile % (kThreads * kVec) == 0, "TMA tile");
 constexpr int kMaxSeg = 960;               // runs per launch (kernel-parameter table)
-constexpr int kMaxGrid = 2048;             // partial slots per launch region
+constexpr int kMaxGrid = 1024;             // partial slots per launch region (CTAs per launch at most)
 constexpr int kBatch = 8;                  // replicas loaded together
 constexpr size_t kScalarBytes = 256;
 

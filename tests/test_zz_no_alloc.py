@@ -66,9 +66,9 @@ def test_noalloc_matches_dopt_step_two_calls(name):
 
 def test_noalloc_rejects_oversized_request():
     D = H.dopt()
-    # 30,000 params whose weight-decay multipliers alternate never merge into
-    # longer runs: 32 launch chunks need more partial slots than the scratch has
-    params = [dict(numel=64, dtype=1, wd_mult=float(i % 2)) for i in range(30_000)]
+    # 64,000 params whose weight-decay multipliers alternate never merge into
+    # longer runs: 67 launch chunks need more partial slots than the scratch has
+    params = [dict(numel=64, dtype=1, wd_mult=float(i % 2)) for i in range(64_000)]
     pm = D.dopt_build_shard_map(params, 1, -1, True)
     assert D.dopt_workspace_bytes(pm, 0) > D.NOALLOC_SCRATCH_BYTES
     info = D.dopt_buffer_info_get(pm, 0)
