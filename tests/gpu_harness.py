@@ -578,7 +578,7 @@ class FullCase:
                     self._fill_local(bi, rep, key, cfg["grad_sigma"], KIND[buf.grad_dtype])
         self.torch.cuda.synchronize()
 
-    def step(self, t):
+    def step(self, t, grad_amax=None):
         D = dopt()
         cfg = self.cfg
         args = D.StepArgs(self.pm, self.rank_arg, self.reps, self.main, self.master, self.m, self.v,
@@ -588,6 +588,8 @@ class FullCase:
                           average_in_collective=cfg["average"],
                           inv_loss_scale=float(np.float32(1.0 / cfg["loss_scale"])),
                           max_norm=cfg["max_norm"], stream=self.torch.cuda.current_stream())
+        if grad_amax is not None:
+            args.set_grad_check(grad_amax)
         return D.dopt_step(args)
 
     def pieces(self):

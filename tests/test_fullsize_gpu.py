@@ -116,3 +116,41 @@ def test_param_larger_than_2_pow_31_elements():
                                       dict(name="tail", numel=77, dtype=W.F32)],
                  dp=2, bucket_size=None, layout="shard", ranks=[1], steps=1, seed=21)
     _run(cfg, steps=1, n_random=2000)
+
+
+def test_grad_check_at_full_size_bench_workload():
+    """The pre-reduction grad check on the bench workload, in the launch
+    configuration `bench.py --check-grads` times: for the first, a middle
+    and the last bucket of the bf16 buffer and the fp32 buffer's bucket, the
+    largest |g| of every replica over the rank's pieces, regenerated on the
+    host from the seeded generator, equals the device table exactly."""
+    import synth
+    cfg = W.config("llama_7b_dp8_rank0")
+    fc = H.FullCase(cfg)
+    fc.fill_grads(1)
+    D = H.dopt()
+    total = D.dopt_total_buckets(fc.pm)
+    amax = torch.full((fc.n_rep, total), -1.0, dtype=torch.float32, device="cuda")
+    found, _ = fc.step(1, grad_amax=amax)
+    assert not found
+    got = amax.cpu().numpy()
+    assert (got > 0).all()  # every bucket holds some of rank 0's elements
+    r = fc.ranks[0]
+    kind = {H.F32: synth.OUT_F32, H.BF16: synth.OUT_BF16, H.F16: synth.OUT_F16}
+    checked = 0
+    for bi, buf in enumerate(fc.om.buffers):
+        nbk = len(buf.buckets)
+        for b in sorted({0, nbk // 2, nbk - 1}):
+            col = oracle.bucket_number(fc.om, bi, b)
+            for k in range(fc.n_rep):
+                key = synth.key(fc.seed, synth.STREAM_GRAD, 1, k)
+                m = 0.0
+                for pid, pb, v in fc.om.rank_pieces(bi, r):
+                    if pb != b:
+                        continue
+                    g = v["gbuf_world"]
+                    vals = synth.normal(g.size, key, g.start, cfg["grad_sigma"], kind[buf.grad_dtype])
+                    m = max(m, float(np.abs(vals.astype(np.float32)).max()))
+                assert got[k, col] == np.float32(m), (bi, b, k, got[k, col], m)
+                checked += 1
+    assert checked >= 8 * 4
