@@ -15,13 +15,16 @@
  *    no C++ exception crosses this boundary.  dopt_last_error() returns a
  *    thread-local message describing the last failure.
  *  - Device memory: every device pointer is allocated and owned by the
- *    caller, must be 16-byte aligned and stays owned by the caller.  The
- *    library allocates no device memory.  The only library-owned object is
- *    the opaque shard map (host memory), freed by dopt_shard_map_free().
+ *    caller, must be 16-byte aligned unless its description says otherwise,
+ *    and stays owned by the caller.  The library allocates no device memory.
+ *    The library-owned objects are the opaque shard map (host memory), freed
+ *    by dopt_shard_map_free(), and the copy stream and event that
+ *    dopt_step_from_host creates once per thread and device.
  *  - Streams: a dopt_stream is a cudaStream_t passed as a plain pointer
  *    (NULL = the legacy default stream).  Device entry points only enqueue
- *    work on it and return; dopt_step() alone waits for its stream, to hand
- *    back found_inf and the grad norm.
+ *    work on it and return; dopt_step(), dopt_step_noalloc() and
+ *    dopt_step_from_host() wait for their stream, to hand back found_inf and
+ *    the grad norm.
  *  - Element counts are int64; dtypes are dopt_dtype codes.
  *  - Rank selection: rank in [0, DP) steps that rank's shard; DOPT_ALL_RANKS
  *    emulates every rank of the instance on this GPU, their shard arrays laid
@@ -284,7 +287,9 @@ typedef struct {
   /* Optional tracing: NULL, or 4 cudaEvent_t handles (as plain pointers)
    * recorded on `stream` before the reduce/prepare pass, after it, after
    * the norm finalize and after the AdamW pass, so a caller can time each
-   * stage of the step with cudaEventElapsedTime. */
+   * stage of the step with cudaEventElapsedTime.  In the fused step the
+   * finalize runs inside the last reduce launch, so the second and third
+   * events are recorded back to back. */
   void* const* stage_events;
   /* scale_gradients factor (per-token loss normalization, 1/num_tokens):
    * multiplies the reduced grads in the grad dtype (one rounding) before
@@ -301,10 +306,10 @@ typedef struct {
    *   d_lr   -- device double: the learning rate, read by the finalize pass
    *             (only with d_step); NULL uses hp.lr.
    * Both 8-byte aligned.  With d_step, dopt_step_async, the bucket-staged
-   * entry points and dopt_step_noalloc issue only kernel launches on the
-   * stream once each kernel has run once on the device (its shared-memory
-   * attribute is set on first use), so a step can be captured in a graph
-   * after a warm-up step. */
+   * entry points and dopt_step_noalloc issue only kernel launches and
+   * memsets on the stream once each kernel has run once on the device (its
+   * shared-memory attribute is set on first use), so a step can be
+   * captured in a graph after a warm-up step. */
   int64_t* d_step;
   const double* d_lr;
   /* Optional check of every replica's gradients before their reduction
@@ -359,16 +364,18 @@ typedef struct {
 } dopt_step_stats;
 
 /* Copies the statistics of the last step run with `workspace` (fused or
- * bucket-staged layout) to the host; waits for `stream`.  dopt_step and
- * dopt_step_noalloc return DOPT_E_CUDA when kernel_error is set. */
+ * bucket-staged layout) to the host; waits for `stream`.  dopt_step,
+ * dopt_step_noalloc and dopt_step_from_host return DOPT_E_CUDA when
+ * kernel_error is set. */
 int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_stream stream);
 
 /*
  * One fused optimizer step (steps A2..A6): for every buffer, reduce the
  * replicas, unscale, check inf/NaN and accumulate the sum of squares in one
  * pass; then the global norm, clip coefficient and skip decision on the
- * device; then AdamW and the write-back, skipped on the device when
- * found_inf.  Waits for the stream, then returns *found_inf_out (0/1) and
+ * device (by the last CTA to finish the last reduce launch, without a
+ * launch of its own); then AdamW and the write-back, skipped on the device
+ * when found_inf.  Waits for the stream, then returns *found_inf_out (0/1) and
  * *grad_norm_out (NaN when skipped).  The caller advances its step count
  * only when *found_inf_out is 0.  MixedPrecisionOptimizer.step skeleton of
  * the distrib_optimizer page: prepare_grads -> (return on inf) ->
