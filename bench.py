@@ -442,7 +442,9 @@ def cpu_baseline(cfg, seconds_target=8.0, max_passes=40):
             "value_one_thread": sample.elements * p1 / e1}
 
 
-REFERENCE_BUDGET_ELEMENTS = 600_000_000  # ~1 minute of oracle work per run
+# oracle elements per reference run: about 6 s on 16 host cores (about 90 s
+# on one), so each step's sample stays a sizeable slice of the workload
+REFERENCE_BUDGET_ELEMENTS = 3_000_000_000
 
 
 def run_reference(args):
