@@ -85,3 +85,70 @@ def test_graph_replay_with_device_step_matches_host_steps(name):
             for x, y in zip(a, b):
                 if x is not None:
                     assert x.tobytes() == y.tobytes()
+
+
+def test_graph_replay_with_grad_check_matches_eager():
+    """The grad check inside a captured step (its table is cleared by a
+    memset node and merged into with atomic max): every replay gives the
+    table an eager step gives, with large and non-finite values planted at
+    different places from step to step."""
+    D = H.dopt()
+    cfg = dict(W.mini("llama_7b_dp8_rank0"), steps=3, inf_at=None)
+    hc = H.HostCase(cfg)
+    eager = H.DeviceCase(hc)
+    graphed = H.DeviceCase(hc)
+    warm = H.DeviceCase(hc)
+    total = D.dopt_total_buckets(hc.pm)
+    sites = H.plant_sites(hc)
+    plants = {1: [(0, 0, 9.0), (5, 3, -40.0)], 2: [(2, 1, np.nan), (7, 6, 3.0e4)], 3: [(4, 2, -np.inf)]}
+
+    def grads_of(step):
+        g = hc.grads(step)
+        for site, k, value in plants[step]:
+            bi, w = sites[site % len(sites)]
+            H.plant(hc, g, bi, k, w, value)
+        return g
+
+    first = grads_of(1)
+    reps = [[graphed._up(r) for r in g] for g in first]
+    d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+    d_lr = torch.tensor([cfg["hp"]["lr"]], dtype=torch.float64, device="cuda")
+    amax_g = torch.zeros((hc.n_rep, total), dtype=torch.float32, device="cuda")
+    warm_args = warm.step_args([[warm._up(r) for r in g] for g in first], 1)
+    warm_args.set_device_step(torch.zeros(1, dtype=torch.int64, device="cuda"), d_lr)
+    warm_args.set_grad_check(torch.zeros_like(amax_g))
+    D.dopt_step_async(warm_args)
+    torch.cuda.synchronize()
+
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        args = graphed.step_args(reps, 1, stream=s)
+        args.set_device_step(d_step, d_lr)
+        args.set_grad_check(amax_g)
+        with torch.cuda.graph(graph, stream=s):
+            D.dopt_step_async(args)
+    torch.cuda.synchronize()
+
+    t_applied = 0
+    for step in (1, 2, 3):
+        g = first if step == 1 else grads_of(step)
+        amax_e = torch.full((hc.n_rep, total), -5.0, dtype=torch.float32, device="cuda")
+        eargs = eager.step_args([[eager._up(r) for r in x] for x in g], t_applied + 1)
+        eargs.set_grad_check(amax_e)
+        found, _ = D.dopt_step(eargs)
+        for dst, src in zip(reps, g):
+            for d, h in zip(dst, src):
+                d.copy_(torch.from_numpy(h.view(np.int16) if h.dtype == np.uint16 else h))
+        amax_g.fill_(-5.0)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert H.amax_equal(amax_g.cpu().numpy(), amax_e.cpu().numpy().astype(np.float64)), step
+        if not found:
+            t_applied += 1
+        assert int(d_step.item()) == t_applied
+        for a, b in zip(eager.download(), graphed.download()):
+            for x, y in zip(a, b):
+                if x is not None:
+                    assert x.tobytes() == y.tobytes()
