@@ -759,6 +759,10 @@ namespace {
 struct HostCopyResources {
   cudaStream_t stream = nullptr;
   cudaEvent_t ready = nullptr;
+  ~HostCopyResources() {  // at thread exit; errors (a runtime already shut down) are moot
+    if (ready) cudaEventDestroy(ready);
+    if (stream) cudaStreamDestroy(stream);
+  }
 };
 thread_local HostCopyResources t_host_copy[kMaxDevices];
 
