@@ -108,8 +108,9 @@ def describe(cfg, n_elems):
         n_layers = sum(1 for p in cfg["params"] if p["name"].endswith("q_proj"))
         shape = (f"Llama-7B-shaped ({n_layers} layers, d=4096, ffn 11008, vocab 32000), bf16 params + "
                  f"fp32 RMSNorm group")
+    avg = ", averaged in the collective" if cfg.get("average") else ""
     return (f"{cfg['name']}: {shape}, DP={cfg['dp']} x {cfg['n_inst']} instance(s) emulated, {who}, "
-            f"{reps}, bucket {cfg['bucket_size']}, AdamW lr 1e-4 betas (0.9, 0.95) eps 1e-8 "
+            f"{reps}{avg}, bucket {cfg['bucket_size']}, AdamW lr 1e-4 betas (0.9, 0.95) eps 1e-8 "
             f"wd 0.1, clip 1.0")
 
 

@@ -104,6 +104,13 @@ def config(name):
         return _cfg(name=name, params=llama(32, 4096, 11008, 32000), dp=8,
                     bucket_size=40_000_000, grad_reduce_in_fp32=False, layout="shard",
                     ranks=[0], steps=10, seed=3)
+    if name == "llama_7b_dp8_rank0_avg":
+        # average_in_collective: the replicas are summed, then averaged
+        return dict(config("llama_7b_dp8_rank0"), name=name, average=True)
+    if name == "llama_7b_dp16_rank0":
+        # one instance of 16 ranks: 16 fp32 replica shards of rank 0
+        return _cfg(name=name, params=llama(32, 4096, 11008, 32000), dp=16,
+                    bucket_size=40_000_000, layout="shard", ranks=[0], steps=10, seed=5)
     if name.startswith("llama_7b_dp16_2x8"):
         bs = {"1m": 1_000_000, "10m": 10_000_000, "40m": 40_000_000,
               "100m": 100_000_000}[name.rsplit("_", 1)[1]]
@@ -136,6 +143,6 @@ def mini(name):
 
 
 NAMES = ["toy_mlp_dp4", "gpt2_small_dp8", "llama_1p3b_fp16_dp8", "llama_7b_dp8_rank0",
-         "llama_7b_dp8_rank0_bf16grads",
+         "llama_7b_dp8_rank0_bf16grads", "llama_7b_dp8_rank0_avg", "llama_7b_dp16_rank0",
          "llama_7b_dp16_2x8_1m", "llama_7b_dp16_2x8_10m", "llama_7b_dp16_2x8_40m",
          "llama_7b_dp16_2x8_100m"]
