@@ -205,6 +205,7 @@ class Workload:
                           self.v, self.params, self.cfg["hp"], self.t_applied + 1, self.ws,
                           self.ws_bytes, n_instances=self.cfg["n_inst"],
                           layout=D.LAYOUT_FULL_BUFFER if self.full else D.LAYOUT_SHARD_ONLY,
+                          average_in_collective=self.cfg.get("average", False),
                           inv_loss_scale=1.0 / self.cfg["loss_scale"], max_norm=self.cfg["max_norm"],
                           stream=self.torch.cuda.current_stream())
 
@@ -364,7 +365,8 @@ class OracleSample:
 
     def _reduce(self, lo, hi):
         c, L = self.ctypes, self.L
-        bad = L.or_reduce_prepare_run(self.arr, self.n_rep, self.cfg["n_inst"], self.gdt, 0, lo,
+        bad = L.or_reduce_prepare_run(self.arr, self.n_rep, self.cfg["n_inst"], self.gdt,
+                                      int(bool(self.cfg.get("average", False))), lo,
                                       hi - lo, c.c_float(1.0), c.c_float(self.inv_scale),
                                       self.main.ctypes.data + 4 * lo)
         return bad, L.or_sumsq_run(self.main.ctypes.data + 4 * lo, hi - lo)
