@@ -7,8 +7,9 @@ its Python binding) never imports it, and it imports nothing of the product.
 Parts:
   shard_map.py -- step A1 (buffers, buckets, per-rank views), plain Python.
   oracle.c     -- steps A2..A6 (replica reduction, unscale and inf check,
-                  fp64 sum of squares, clip coefficient, AdamW, write-back),
-                  scalar C compiled with -ffp-contract=off.
+                  fp64 sum of squares, clip coefficient, AdamW, write-back)
+                  and the pre-reduction grad check (largest |g| per replica
+                  and bucket), scalar C compiled with -ffp-contract=off.
   step()       -- one optimizer step composed from those parts, in the
                   order of the MixedPrecisionOptimizer step skeleton of the
                   distrib_optimizer page: prepare_grads (copy to fp32 main
