@@ -22,6 +22,10 @@
  *      reduced grads are multiplied by 1/num_tokens in the grad buffer; read
  *      as one multiply rounded to the grad dtype).  A factor of 1 is the
  *      identity and skips the step.
+ *   A2 check (check_for_nan_in_grad / check_for_large_grads): the Megatron
+ *      distributed-package page, sections 2.4 and 3.2 -- each bucket's grads
+ *      looked at for NaN, Inf and large values before the communication
+ *      (read as: the largest |g| per replica and bucket).
  *   A3 prepare_grads: distrib_optimizer page, "MixedPrecisionOptimizer" layer
  *      (copy to fp32 main grad, unscale, inf/NaN detection) and the grad copy
  *      listing (bf16 -> fp32 .float()).
