@@ -213,6 +213,26 @@ __device__ __forceinline__ float post_scaled(float red, float post_scale) {
   return post_scale == 1.0f ? red : GradT<GT>::round_to(__fmul_rn(red, post_scale));
 }
 
+// The same arithmetic with the averaging choice known at compile time (the
+// specialised kernels): a replica's term is prescaled by 1/N when the
+// collective sums, taken as is when it averages; an instance's sum is
+// averaged over its ranks (when averaging) and rounded to the grad dtype;
+// with several instances their sum is averaged (when averaging) and
+// rounded again.
+template <bool AVG>
+__device__ __forceinline__ float term_of(float x, float pre) {
+  return AVG ? x : __fmul_rn(x, pre);
+}
+template <typename GT, bool AVG>
+__device__ __forceinline__ float instance_value(float s, float inv_dpi) {
+  return GradT<GT>::round_to(AVG ? __fmul_rn(s, inv_dpi) : s);
+}
+template <typename GT, bool AVG, int NINST>
+__device__ __forceinline__ float across_instances(float t, float inv_ninst) {
+  if (NINST == 1) return t;
+  return GradT<GT>::round_to(AVG ? __fmul_rn(t, inv_ninst) : t);
+}
+
 // The reduced grad of an element in the grad dtype, after scale_gradients
 // (before the unscale that makes it the fp32 main grad).
 template <typename GT>
@@ -474,8 +494,8 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
   }
 }
 
-// The common reductions: prescale by 1/N and sum (average_in_collective =
-// false), NINST instances of DPI replicas each, both known at compile time.
+// The common reductions: NINST instances of DPI replicas each and the
+// averaging choice (AVG: average_in_collective) known at compile time.
 // Same arithmetic as the general kernel, in the same order (each instance's
 // replicas summed in order and rounded to the grad dtype, then the instance
 // sums in order, rounded again when there is more than one), without its
@@ -483,7 +503,7 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
 // CHECK every thread keeps a running maximum per replica in registers and
 // each warp merges it into the global table when its tiles move to another
 // bucket.
-template <typename GT, bool FULL, bool STATS, bool CHECK, int DPI, int NINST>
+template <typename GT, bool FULL, bool STATS, bool CHECK, bool AVG, int DPI, int NINST>
 __global__ void __launch_bounds__(kThreads, DOPT_K1_MIN_BLOCKS)
 k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
   constexpr int U = kUnroll1 * GradT<GT>::kUnroll;  // accesses per thread per tile
@@ -554,10 +574,10 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
       for (int u = 0; u < U; ++u) {
 #pragma unroll
         for (int q = 0; q < kVec; ++q) {
-          float sum = __fmul_rn(GradT<GT>::at(x[0][u], q), pre);
+          float sum = term_of<AVG>(GradT<GT>::at(x[0][u], q), pre);
 #pragma unroll
-          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::at(x[k][u], q), pre));
-          sum = GradT<GT>::round_to(sum);
+          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, term_of<AVG>(GradT<GT>::at(x[k][u], q), pre));
+          sum = instance_value<GT, AVG>(sum, p.inv_dpi);
           total[u][q] = (j == 0) ? sum : __fadd_rn(total[u][q], sum);
         }
       }
@@ -569,7 +589,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
         float m[kVec];
 #pragma unroll
         for (int q = 0; q < kVec; ++q) {
-          float tt = NINST > 1 ? GradT<GT>::round_to(total[u][q]) : total[u][q];
+          float tt = across_instances<GT, AVG, NINST>(total[u][q], p.inv_ninst);
           m[q] = post_scaled<GT>(tt, p.post_scale);
         }
         finish_store4<GT, STATS>(p, l0 + e, m);
@@ -584,14 +604,14 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
 #pragma unroll
             for (int k = 0; k < DPI; ++k) {
               const int64_t i = r0 + e + q;
-              const float term = __fmul_rn(GradT<GT>::widen1(p.rep[j * DPI + k], i), pre);
+              const float term = term_of<AVG>(GradT<GT>::widen1(p.rep[j * DPI + k], i), pre);
               sum = k == 0 ? term : __fadd_rn(sum, term);
               if (CHECK) amx[j][k] = GradT<GT>::amax(amx[j][k], GradT<GT>::abs1(p.rep[j * DPI + k], i));
             }
-            sum = GradT<GT>::round_to(sum);
+            sum = instance_value<GT, AVG>(sum, p.inv_dpi);
             tt = (j == 0) ? sum : __fadd_rn(tt, sum);
           }
-          if (NINST > 1) tt = GradT<GT>::round_to(tt);
+          tt = across_instances<GT, AVG, NINST>(tt, p.inv_ninst);
           const float m = finish_store1<GT, STATS>(p, l0 + e + q, post_scaled<GT>(tt, p.post_scale));
           if (STATS) acc.add1(m);
         }
@@ -631,7 +651,7 @@ __host__ __device__ constexpr size_t tma_smem_bytes() {
          DOPT_TMA_STAGES * sizeof(uint64_t);
 }
 
-template <typename GT, bool FULL, bool STATS, bool CHECK, int DPI>
+template <typename GT, bool FULL, bool STATS, bool CHECK, bool AVG, int DPI>
 __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __grid_constant__ K1Params p) {
   using E = typename GradBits<GT>::T;
   constexpr int S = DOPT_TMA_STAGES;
@@ -721,10 +741,10 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
         }
 #pragma unroll
         for (int q = 0; q < kVec; ++q) {
-          float sum = __fmul_rn(GradT<GT>::at(x[0], q), pre);
+          float sum = term_of<AVG>(GradT<GT>::at(x[0], q), pre);
 #pragma unroll
-          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, __fmul_rn(GradT<GT>::at(x[k], q), pre));
-          m[q] = post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale);
+          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, term_of<AVG>(GradT<GT>::at(x[k], q), pre));
+          m[q] = post_scaled<GT>(instance_value<GT, AVG>(sum, p.inv_dpi), p.post_scale);
         }
         finish_store4<GT, STATS>(p, l0 + e, m);
         if (STATS) acc.add4(m);
@@ -735,11 +755,12 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
           float sum = 0.f;
 #pragma unroll
           for (int k = 0; k < DPI; ++k) {
-            const float term = __fmul_rn(GradT<GT>::widen1(p.rep[k], r0 + e + q), pre);
+            const float term = term_of<AVG>(GradT<GT>::widen1(p.rep[k], r0 + e + q), pre);
             sum = k == 0 ? term : __fadd_rn(sum, term);
             if (CHECK) amx[k] = GradT<GT>::amax(amx[k], GradT<GT>::abs1(p.rep[k], r0 + e + q));
           }
-          const float m = finish_store1<GT, STATS>(p, l0 + e + q, post_scaled<GT>(GradT<GT>::round_to(sum), p.post_scale));
+          const float m =
+              finish_store1<GT, STATS>(p, l0 + e + q, post_scaled<GT>(instance_value<GT, AVG>(sum, p.inv_dpi), p.post_scale));
           if (STATS) acc.add1(m);
         }
       }
@@ -777,9 +798,9 @@ int launch_plain(K kern, const K1Params& kp, cudaStream_t s, const char* what) {
   return check_launch(what);
 }
 
-template <typename GT, bool FULL, bool STATS, bool CHECK, int DPI>
+template <typename GT, bool FULL, bool STATS, bool CHECK, bool AVG, int DPI>
 int launch_tma(K1Params& kp, cudaStream_t s) {
-  auto kern = k1_reduce_prepare_tma<GT, FULL, STATS, CHECK, DPI>;
+  auto kern = k1_reduce_prepare_tma<GT, FULL, STATS, CHECK, AVG, DPI>;
   const size_t smem = tma_smem_bytes<GT, DPI>();
   static std::atomic<uint64_t> attr_set{0};
   int st = allow_dynamic_smem(kern, smem, attr_set, "k1 tma");
@@ -791,16 +812,18 @@ int launch_tma(K1Params& kp, cudaStream_t s) {
   return check_launch("k1_reduce_prepare_tma launch");
 }
 
-// The specialised kernels cover prescale-and-sum with one instance of 1, 2,
-// 4 or 8 replicas, or two instances of 4 or 8; fp32 replicas in a single
-// instance whose runs are all 8-element aligned are staged by TMA (16-bit
-// replicas stream faster through registers: packed loads, four accesses per
-// thread).  Everything else runs the general kernel.
-template <typename GT, bool FULL, bool STATS, bool CHECK>
+// The specialised kernels cover one instance of 1, 2, 4 or 8 replicas, or
+// two instances of 4 or 8, summing or averaging (AVG must match the
+// launch's average_in_collective); fp32 replicas in a single instance whose
+// runs are all 8-element aligned are staged by TMA (16-bit replicas stream
+// faster through registers: packed loads, four accesses per thread).
+// Everything else runs the general kernel.
+template <typename GT, bool FULL, bool STATS, bool CHECK, bool AVG>
 int launch_k1_sel(K1Params& kp, const K1Launch& l, cudaStream_t s) {
   const int dpi = kp.n_rep / kp.n_inst;
-  const bool special = !kp.average && ((kp.n_inst == 1 && (dpi == 1 || dpi == 2 || dpi == 4 || dpi == 8)) ||
-                                       (kp.n_inst == 2 && (dpi == 4 || dpi == 8)));
+  const bool special = (kp.average != 0) == AVG &&
+                       ((kp.n_inst == 1 && (dpi == 1 || dpi == 2 || dpi == 4 || dpi == 8)) ||
+                        (kp.n_inst == 2 && (dpi == 4 || dpi == 8)));
   bool all_aligned = true;
   for (int k = 0; k < l.count; ++k) all_aligned &= seg_aligned(l.runs[k].local, l.runs[k].world);
   constexpr bool kTmaKind = DOPT_K1_TMA && STATS && std::is_same<GT, float>::value;
@@ -810,39 +833,45 @@ int launch_k1_sel(K1Params& kp, const K1Launch& l, cudaStream_t s) {
   if constexpr (kTmaKind) {
     if (tma) {
       switch (dpi) {
-        case 1: return launch_tma<GT, FULL, STATS, CHECK, 1>(kp, s);
-        case 2: return launch_tma<GT, FULL, STATS, CHECK, 2>(kp, s);
-        case 4: return launch_tma<GT, FULL, STATS, CHECK, 4>(kp, s);
-        default: return launch_tma<GT, FULL, STATS, CHECK, 8>(kp, s);
+        case 1: return launch_tma<GT, FULL, STATS, CHECK, AVG, 1>(kp, s);
+        case 2: return launch_tma<GT, FULL, STATS, CHECK, AVG, 2>(kp, s);
+        case 4: return launch_tma<GT, FULL, STATS, CHECK, AVG, 4>(kp, s);
+        default: return launch_tma<GT, FULL, STATS, CHECK, AVG, 8>(kp, s);
       }
     }
   }
   const char* what = "k1_reduce_prepare_n launch";
   if (special && kp.n_inst == 1) {
     switch (dpi) {
-      case 1: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 1, 1>, kp, s, what);
-      case 2: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 2, 1>, kp, s, what);
-      case 4: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 4, 1>, kp, s, what);
-      default: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 8, 1>, kp, s, what);
+      case 1: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, AVG, 1, 1>, kp, s, what);
+      case 2: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, AVG, 2, 1>, kp, s, what);
+      case 4: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, AVG, 4, 1>, kp, s, what);
+      default: return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, AVG, 8, 1>, kp, s, what);
     }
   }
   if (special) {
-    if (dpi == 4) return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 4, 2>, kp, s, what);
-    return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, 8, 2>, kp, s, what);
+    if (dpi == 4) return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, AVG, 4, 2>, kp, s, what);
+    return launch_plain(k1_reduce_prepare_n<GT, FULL, STATS, CHECK, AVG, 8, 2>, kp, s, what);
   }
   return launch_plain(k1_reduce_prepare<GT, FULL, STATS, CHECK>, kp, s, "k1_reduce_prepare launch");
 }
 
+template <typename GT, bool STATS, bool CHECK, bool AVG>
+int launch_k1_layout(K1Params& kp, const K1Launch& l, cudaStream_t s) {
+  return l.full ? launch_k1_sel<GT, true, STATS, CHECK, AVG>(kp, l, s)
+                : launch_k1_sel<GT, false, STATS, CHECK, AVG>(kp, l, s);
+}
+
 // The grad check rides on the statistics pass only (the fused and
-// bucket-staged steps); the plain reduction has no check.
+// bucket-staged steps); the plain reduction has no check, and averaging in
+// it takes the general kernel.
 template <typename GT>
 int launch_k1_for(K1Params& kp, const K1Launch& l, cudaStream_t s) {
   if (l.check && !l.stats) return fail(DOPT_E_INVALID, "the grad check needs the statistics pass");
-  if (!l.stats)
-    return l.full ? launch_k1_sel<GT, true, false, false>(kp, l, s) : launch_k1_sel<GT, false, false, false>(kp, l, s);
-  if (l.check)
-    return l.full ? launch_k1_sel<GT, true, true, true>(kp, l, s) : launch_k1_sel<GT, false, true, true>(kp, l, s);
-  return l.full ? launch_k1_sel<GT, true, true, false>(kp, l, s) : launch_k1_sel<GT, false, true, false>(kp, l, s);
+  if (!l.stats) return launch_k1_layout<GT, false, false, false>(kp, l, s);
+  if (kp.average)
+    return l.check ? launch_k1_layout<GT, true, true, true>(kp, l, s) : launch_k1_layout<GT, true, false, true>(kp, l, s);
+  return l.check ? launch_k1_layout<GT, true, true, false>(kp, l, s) : launch_k1_layout<GT, true, false, false>(kp, l, s);
 }
 
 }  // namespace dopt

@@ -295,6 +295,12 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f) {
   }
 }
 
+// The finalize of a reduce launch's last CTA, out of line: inlined, its
+// fp64 scalar work would set the register count of every reduce kernel
+// (88 where the streaming loop needs 48 to 62), costing occupancy on a path
+// that runs once per step in one CTA.
+static __device__ __noinline__ void finalize_call(const FinalizeArgs& f) { finalize_block<kThreads>(f); }
+
 // Called by every thread of every CTA of a reduce launch after its partial
 // is written (by thread 0): with a ticket counter set, the last CTA to take
 // a ticket runs the finalize and returns the counter to zero for the next
@@ -309,7 +315,7 @@ __device__ __forceinline__ void finalize_if_last(const K1Params& p) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  finalize_block<kThreads>(p.fin);
+  finalize_call(p.fin);
   if (threadIdx.x == 0) *p.fin_counter = 0u;
 }
 
