@@ -6,12 +6,14 @@
 // k1_f16.cu), each instantiating launch_k1_for<its dtype>.
 //
 // Three kernels, chosen per launch:
-//   k1_reduce_prepare      any replica count, instances, average_in_collective
-//   k1_reduce_prepare_n    prescale-and-sum with 1, 2, 4 or 8 replicas per
-//                          instance and one or two instances (compile time)
-//   k1_reduce_prepare_tma  the single-instance fp32 case with the replica
-//                          tiles staged in shared memory by bulk copies
-// All three compute the same values in the same order.
+//   k1_reduce_prepare      any replica and instance count (run time)
+//   k1_reduce_prepare_n    1, 2, 4 or 8 replicas per instance, one or two
+//                          instances, summing or averaging (compile time)
+//   k1_reduce_prepare_tma  the same with one instance, fp32 replicas, the
+//                          replica tiles staged in shared memory by bulk copies
+// All three compute the same values in the same order.  With 16-bit grads
+// the statistics pass may keep the reduced grads in the grad dtype instead
+// of the fp32 main grads (K1Params::compact).
 #pragma once
 
 #include <type_traits>
