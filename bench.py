@@ -295,12 +295,22 @@ def measured_peak_hbm():
 K1_SOURCES = ("kernels.cuh", "tma.cuh", "k1.cuh", "k1_f32.cu")
 
 
+def code_of(text):
+    """C/C++ source without comments and with whitespace runs collapsed:
+    what a change must touch to change the compiled kernel."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def k1_source_sha256():
-    """sha256 over the sources of the fp32 reduce/prepare kernel, in order."""
+    """sha256 over the code (comments and layout removed) of the sources of
+    the fp32 reduce/prepare kernel, in order."""
     h = hashlib.sha256()
     for f in K1_SOURCES:
-        with open(os.path.join(ROOT, "mixed_precision_adam_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "mixed_precision_adam_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_of(fh.read()).encode())
     return h.hexdigest()
 
 
