@@ -10,6 +10,8 @@
 #include <unordered_map>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.cuh"
 
 // Scratch of dopt_step_noalloc: the step scalars and partial-sum regions
@@ -20,6 +22,15 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[DOPT_NOALLOC_SC
 
 namespace {
 std::atomic<uint64_t> g_launches{0};  // kernels launched by this library
+
+// A named range on the host timeline of a profiler (NVTX; no cost without
+// one attached) around a step and its passes.
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
 }  // namespace
 
 namespace dopt {
@@ -632,6 +643,7 @@ int dopt_adam_step(const dopt_shard_map* map, int32_t buffer, int32_t rank, cons
 }
 
 int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm) {
+  Range step_range("dopt_step");
   int st = check_step_args(a, false, "dopt_step");
   if (st) return st;
   dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
@@ -646,18 +658,24 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
   if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
   const FinalizeArgs fin = finalize_args(total_regions(m, a->rank) * kMaxGrid, a->workspace, a->remote_sumsq,
                                          a->remote_found_inf, a->max_norm, d_norm, nullptr, d_found_inf, a);
-  for (int32_t b = 0; b < nb; ++b) {
-    K1Job j = step_job(a, b);
-    if (b == nb - 1) {
-      j.fin = &fin;
-      j.fin_counter = counter;
+  {
+    Range r("reduce_prepare+finalize");
+    for (int32_t b = 0; b < nb; ++b) {
+      K1Job j = step_job(a, b);
+      if (b == nb - 1) {
+        j.fin = &fin;
+        j.fin_counter = counter;
+      }
+      if ((st = run_k1(m, b, a->rank, j, s))) return st;
     }
-    if ((st = run_k1(m, b, a->rank, j, s))) return st;
   }
   if ((st = record_stage(a, 1, s))) return st;
   if ((st = record_stage(a, 2, s))) return st;  // the finalize ran inside the last reduce launch
-  for (int32_t b = 0; b < nb; ++b) {
-    if ((st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s))) return st;
+  {
+    Range r("adamw");
+    for (int32_t b = 0; b < nb; ++b) {
+      if ((st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s))) return st;
+    }
   }
   return record_stage(a, 3, s);
 }
@@ -672,6 +690,7 @@ size_t dopt_workspace_bytes_bucketed(const dopt_shard_map* map, int32_t rank) {
 
 int dopt_step_reduce_buckets(const dopt_step_args* a, int32_t buffer, int32_t bucket_first,
                              int32_t bucket_count) {
+  Range range("dopt_step_reduce_buckets");
   const char* fn = "dopt_step_reduce_buckets";
   int st = check_step_args(a, true, fn);
   if (st) return st;
@@ -688,6 +707,7 @@ int dopt_step_reduce_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
 }
 
 int dopt_step_finalize(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm) {
+  Range range("dopt_step_finalize");
   const char* fn = "dopt_step_finalize";
   int st = check_step_args(a, true, fn);
   if (st) return st;
@@ -699,6 +719,7 @@ int dopt_step_finalize(const dopt_step_args* a, int32_t* d_found_inf, float* d_n
 
 int dopt_step_update_buckets(const dopt_step_args* a, int32_t buffer, int32_t bucket_first,
                              int32_t bucket_count) {
+  Range range("dopt_step_update_buckets");
   const char* fn = "dopt_step_update_buckets";
   int st = check_step_args(a, true, fn);
   if (st) return st;
@@ -800,6 +821,7 @@ int finish_sync_step(const dopt_step_args* a, int32_t* found_inf_out, float* gra
 
 int dopt_step_from_host(const dopt_step_args* a, const void* const* const* host_replica_grads,
                         dopt_stream copy_stream, int32_t* found_inf_out, float* grad_norm_out) {
+  Range range("dopt_step_from_host");
   const char* fn = "dopt_step_from_host";
   int st = check_step_args(a, true, fn);
   if (st) return st;
