@@ -18,13 +18,16 @@
  *    caller, must be 16-byte aligned unless its description says otherwise,
  *    and stays owned by the caller.  The library allocates no device memory.
  *    The library-owned objects are the opaque shard map (host memory), freed
- *    by dopt_shard_map_free(), and the copy stream and event that
- *    dopt_step_from_host creates once per thread and device.
+ *    by dopt_shard_map_free(), and the side stream and event that
+ *    dopt_step and dopt_step_from_host create once per thread and device.
  *  - Streams: a dopt_stream is a cudaStream_t passed as a plain pointer
  *    (NULL = the legacy default stream).  Device entry points only enqueue
- *    work on it and return; dopt_step(), dopt_step_noalloc() and
- *    dopt_step_from_host() wait for their stream, to hand back found_inf and
- *    the grad norm.
+ *    work on it and return; dopt_step() and dopt_step_noalloc() wait until
+ *    the step's results (found_inf, the grad norm) are known -- the AdamW
+ *    pass may still be running on the stream when they return -- and
+ *    dopt_step_from_host() waits for the whole step.  Work queued later on
+ *    the same stream sees the updated state; a reader on the host or on
+ *    another stream synchronises with the step's stream first.
  *  - Element counts are int64; dtypes are dopt_dtype codes.
  *  - Rank selection: rank in [0, DP) steps that rank's shard; DOPT_ALL_RANKS
  *    emulates every rank of the instance on this GPU, their shard arrays laid
@@ -375,9 +378,13 @@ int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_strea
  * pass; then the global norm, clip coefficient and skip decision on the
  * device (by the last CTA to finish the last reduce launch, without a
  * launch of its own); then AdamW and the write-back, skipped on the device
- * when found_inf.  Waits for the stream, then returns *found_inf_out (0/1) and
- * *grad_norm_out (NaN when skipped).  The caller advances its step count
- * only when *found_inf_out is 0.  MixedPrecisionOptimizer.step skeleton of
+ * when found_inf.  Waits until the finalize has run (the AdamW pass is
+ * already queued and may still be running), then returns *found_inf_out
+ * (0/1) and *grad_norm_out (NaN when skipped) -- like the pages' optimizer,
+ * whose step reads the norm back and leaves the update running.  The
+ * caller advances its step count only when *found_inf_out is 0.  The
+ * results are copied on a side stream (the one dopt_step_from_host uses),
+ * so the AdamW pass does not wait for the copy.  MixedPrecisionOptimizer.step skeleton of
  * the distrib_optimizer page: prepare_grads -> (return on inf) ->
  * clip_grad_norm -> step_with_ready_grads.
  */

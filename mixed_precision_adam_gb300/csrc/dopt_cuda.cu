@@ -522,6 +522,49 @@ int record_stage(const dopt_step_args* a, int i, cudaStream_t s) {
   return DOPT_OK;
 }
 
+// The fused step, enqueued in two parts split where its results are known:
+// the reduce launches with the finalize in the last one (stage events 0-2),
+// then the AdamW launches (stage event 3).  Arguments already checked.
+int enqueue_reduce(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm) {
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  const int32_t nb = (int32_t)m->buffers.size();
+  cudaStream_t s = (cudaStream_t)a->stream;
+  int st = record_stage(a, 0, s);
+  if (st) return st;
+  if ((st = clear_amax(a, 0, bucket_number(m, nb, 0), s))) return st;
+  // the finalize runs in the last CTA of the last reduce launch: its ticket
+  // counter starts every step at zero
+  uint32_t* counter = reinterpret_cast<uint32_t*>(static_cast<char*>(a->workspace) + kFinCounterOffset);
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(uint32_t), s);
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
+  const FinalizeArgs fin = finalize_args(total_regions(m, a->rank) * kMaxGrid, a->workspace, a->remote_sumsq,
+                                         a->remote_found_inf, a->max_norm, d_norm, nullptr, d_found_inf, a);
+  {
+    Range r("reduce_prepare+finalize");
+    for (int32_t b = 0; b < nb; ++b) {
+      K1Job j = step_job(a, b);
+      if (b == nb - 1) {
+        j.fin = &fin;
+        j.fin_counter = counter;
+      }
+      if ((st = run_k1(m, b, a->rank, j, s))) return st;
+    }
+  }
+  if ((st = record_stage(a, 1, s))) return st;
+  return record_stage(a, 2, s);  // the finalize ran inside the last reduce launch
+}
+
+int enqueue_update(const dopt_step_args* a) {
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  cudaStream_t s = (cudaStream_t)a->stream;
+  Range r("adamw");
+  for (int32_t b = 0; b < (int32_t)m->buffers.size(); ++b) {
+    int st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s);
+    if (st) return st;
+  }
+  return record_stage(a, 3, s);
+}
+
 }  // namespace
 
 using namespace dopt;
@@ -646,38 +689,8 @@ int dopt_step_async(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm
   Range step_range("dopt_step");
   int st = check_step_args(a, false, "dopt_step");
   if (st) return st;
-  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
-  const int32_t nb = (int32_t)m->buffers.size();
-  cudaStream_t s = (cudaStream_t)a->stream;
-  if ((st = record_stage(a, 0, s))) return st;
-  if ((st = clear_amax(a, 0, bucket_number(m, nb, 0), s))) return st;
-  // the finalize runs in the last CTA of the last reduce launch: its ticket
-  // counter starts every step at zero
-  uint32_t* counter = reinterpret_cast<uint32_t*>(static_cast<char*>(a->workspace) + kFinCounterOffset);
-  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(uint32_t), s);
-  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("dopt_step: ") + cudaGetErrorString(e));
-  const FinalizeArgs fin = finalize_args(total_regions(m, a->rank) * kMaxGrid, a->workspace, a->remote_sumsq,
-                                         a->remote_found_inf, a->max_norm, d_norm, nullptr, d_found_inf, a);
-  {
-    Range r("reduce_prepare+finalize");
-    for (int32_t b = 0; b < nb; ++b) {
-      K1Job j = step_job(a, b);
-      if (b == nb - 1) {
-        j.fin = &fin;
-        j.fin_counter = counter;
-      }
-      if ((st = run_k1(m, b, a->rank, j, s))) return st;
-    }
-  }
-  if ((st = record_stage(a, 1, s))) return st;
-  if ((st = record_stage(a, 2, s))) return st;  // the finalize ran inside the last reduce launch
-  {
-    Range r("adamw");
-    for (int32_t b = 0; b < nb; ++b) {
-      if ((st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s))) return st;
-    }
-  }
-  return record_stage(a, 3, s);
+  if ((st = enqueue_reduce(a, d_found_inf, d_norm))) return st;
+  return enqueue_update(a);
 }
 
 size_t dopt_workspace_bytes_bucketed(const dopt_shard_map* map, int32_t rank) {
@@ -964,9 +977,29 @@ int dopt_state_from_model(const dopt_shard_map* map, int32_t buffer, int32_t ran
 }
 
 int dopt_step(const dopt_step_args* a, int32_t* found_inf_out, float* grad_norm_out) {
-  int st = dopt_step_async(a, nullptr, nullptr);
+  const char* fn = "dopt_step";
+  Range step_range(fn);
+  int st = check_step_args(a, false, fn);
   if (st) return st;
-  return finish_sync_step(a, found_inf_out, grad_norm_out, "dopt_step");
+  HostCopyResources* res = nullptr;
+  if ((st = host_copy_resources(&res))) return st;
+  cudaStream_t s = (cudaStream_t)a->stream;
+  if ((st = enqueue_reduce(a, nullptr, nullptr))) return st;
+  // the results are known once the finalize has run: copy them on the side
+  // stream while the AdamW pass runs on the step's stream
+  cudaError_t e = cudaEventRecord(res->ready, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(res->stream, res->ready, 0);
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+  if ((st = enqueue_update(a))) return st;
+  Scalars host{};
+  e = cudaMemcpyAsync(&host, a->workspace, sizeof(Scalars), cudaMemcpyDeviceToHost, res->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(res->stream);
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+  if (found_inf_out) *found_inf_out = host.found_inf;
+  if (grad_norm_out) *grad_norm_out = host.grad_norm;
+  if (host.kernel_error)
+    return fail(DOPT_E_CUDA, std::string(fn) + ": a kernel gave up waiting for its own data copies; the step was skipped");
+  return DOPT_OK;
 }
 
 }  // extern "C"
