@@ -85,7 +85,7 @@ def _cfg(**kw):
 
 
 def config(name):
-    """The five workloads by name, at full size."""
+    """The workloads of NAMES, at full size."""
     if name == "toy_mlp_dp4":
         return _cfg(name=name, params=toy_mlp(), dp=4, bucket_size=1_000_000,
                     steps=3, seed=0)
