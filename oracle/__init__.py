@@ -79,18 +79,23 @@ def _ptr(a, offset=0):
     return ctypes.c_void_p(a.ctypes.data + offset * a.itemsize)
 
 
+def _f32_args(x):
+    # each value handed over as its fp32 bit pattern: a trip through a Python
+    # float (a double) would quiet a signalling NaN before the cast sees it
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32).ravel())
+    return [ctypes.c_float.from_buffer_copy(x[i:i + 1].tobytes()) for i in range(x.size)]
+
+
 def round_bf16(x):
     """RNE fp32 -> bfloat16 bits, elementwise (oracle's own definition)."""
     L = lib()
-    x = np.asarray(x, dtype=np.float32).ravel()
-    return np.array([L.or_round_bf16(float(v)) for v in x], dtype=np.uint16)
+    return np.array([L.or_round_bf16(v) for v in _f32_args(x)], dtype=np.uint16)
 
 
 def round_f16(x):
     """RNE fp32 -> binary16 bits, elementwise (oracle's own definition)."""
     L = lib()
-    x = np.asarray(x, dtype=np.float32).ravel()
-    return np.array([L.or_round_f16(float(v)) for v in x], dtype=np.uint16)
+    return np.array([L.or_round_f16(v) for v in _f32_args(x)], dtype=np.uint16)
 
 
 def reduce_prepare(replicas, gdt, index0, length, inv_scale, n_inst=1, average=False,

@@ -158,6 +158,17 @@ def test_rne_casts_match_libraries():
     assert oracle.round_bf16([1 + 3 * 2**-8])[0] == 0x3F82
 
 
+def test_casts_keep_nan_a_nan():
+    """IEEE: a NaN operand gives a NaN, also when its payload sits only in
+    the low bits that the cast drops (which truncation alone would turn into
+    an infinity)."""
+    nans = np.array([0x7F800001, 0xFF800001, 0x7F80FFFF, 0x7FC00000, 0xFFFFFFFF], np.uint32).view(np.float32)
+    for h in oracle.round_bf16(nans):
+        assert (h & 0x7F80) == 0x7F80 and (h & 0x007F) != 0, hex(h)
+    for h in oracle.round_f16(nans):
+        assert (h & 0x7C00) == 0x7C00 and (h & 0x03FF) != 0, hex(h)
+
+
 # --------------------------------------------------------------------------
 # A2 reduce-scatter semantics and A3 prepare
 
@@ -203,6 +214,22 @@ def test_reduce_rounds_once_to_grad_dtype():
             acc = acc + r.float() * 0.125
         want = acc.to(tdt).float().numpy()
         assert (out == want).all()
+
+
+def test_reduced_grads_are_grad_dtype_values_at_every_level():
+    """The reduce-scatter writes into the grad buffer, and the all-reduce
+    between instances reduces those buffers: with bf16/fp16 grads the result
+    is a value of that dtype at either level, so widening it and casting it
+    back to the dtype (torch's cast) changes nothing."""
+    rng = np.random.RandomState(5)
+    reps32 = [(rng.standard_normal(2000) * 1e-3).astype(np.float32) for _ in range(16)]
+    for gdt, tdt in ((BF16, torch.bfloat16), (F16, torch.float16)):
+        bits = [torch.from_numpy(r).to(tdt).view(torch.int16).numpy().view(np.uint16) for r in reps32]
+        for n_inst in (1, 2, 4):
+            for average in (False, True):
+                out, _ = oracle.reduce_prepare(bits, gdt, 0, 2000, 1.0, n_inst=n_inst, average=average)
+                back = torch.from_numpy(out).to(tdt).float().numpy()
+                assert (back == out).all(), (gdt, n_inst, average)
 
 
 def test_scale_gradients_rounds_once_in_grad_dtype():
@@ -298,6 +325,81 @@ def test_norm_matches_library_vector_norm():
     allm = np.concatenate(res["main"]).astype(np.float64)
     want = torch.linalg.vector_norm(torch.from_numpy(allm)).item()
     assert abs(res["norm"] - want) <= 1e-12 * want
+
+
+def test_norm_adds_the_remote_sum_of_squares():
+    """The norm covers the whole optimizer instance: the remote ranks' sum
+    of squares adds under the square root.  Local grads all 2^-7 over 4^6
+    elements give 0.25; a remote 0.75 makes the norm exactly 1."""
+    n = 4**6
+    m = oracle.ShardMap([dict(numel=n, dtype=BF16)], 4, None, True)
+    grads = [[np.full(n, 2.0**-7, np.float32) for _ in range(4)]]
+    st = [{"exp_avg": np.zeros(n, np.float32), "exp_avg_sq": np.zeros(n, np.float32),
+           "master": np.zeros(n, np.float32)}]
+    res = oracle.step(m, [0, 1, 2, 3], grads, st, [np.zeros(n, np.uint16)], W.HP, 1,
+                      max_norm=0.0, remote_sumsq=0.75)
+    assert res["sumsq"] == 1.0 and res["norm"] == 1.0
+
+
+def _zero_state(m, ranks):
+    st, pb = [], []
+    for i, b in enumerate(m.buffers):
+        n = len(ranks) * m.shard_numel(i)
+        st.append({"exp_avg": np.zeros(n, np.float32), "exp_avg_sq": np.zeros(n, np.float32),
+                   **({"master": np.zeros(n, np.float32)} if b.param_dtype != F32 else {})})
+        pb.append(np.zeros(b.numel, np.uint16 if b.param_dtype != F32 else np.float32))
+    return st, pb
+
+
+def test_count_zeros_counts_main_grads_equal_to_zero():
+    """count_zeros counts the stepped main grads equal to zero, +0 or -0.
+    Zeros are planted three ways (all replicas +0, all -0, and x / -x that
+    cancel exactly after the 1/2 prescale); every other element is nonzero
+    and padding is never stepped, so the count is the number of planted
+    param elements."""
+    params = [dict(numel=n, dtype=d) for n, d in [(70, BF16), (5, F32), (130, BF16), (33, F32)]]
+    m = oracle.ShardMap(params, 2, 100, True)
+    rng = np.random.RandomState(11)
+    grads, want = [], 0
+    for buf in m.buffers:
+        owned = np.zeros(buf.numel, bool)
+        for pid in buf.params:
+            s0, e0, _ = buf.index[pid]
+            owned[s0:e0] = True
+        a = rng.uniform(0.5, 1.5, buf.numel).astype(np.float32)
+        r0, r1 = a.copy(), a.copy()
+        for w in range(0, buf.numel, 5):
+            kind = (w // 5) % 3
+            if kind == 0:
+                r0[w] = r1[w] = 0.0
+            elif kind == 1:
+                r0[w] = r1[w] = -0.0
+            else:
+                r0[w], r1[w] = 0.75, -0.75
+            want += int(owned[w])
+        grads.append([r0, r1])
+    st, pb = _zero_state(m, [0, 1])
+    res = oracle.step(m, [0, 1], grads, st, pb, W.HP, 1)
+    assert res["num_zeros"] == want and want > 0
+
+
+def test_zero_grads_with_no_decay_group_leave_params_unchanged():
+    """wd_mult scales the decoupled decay per param: with a zero grad, m = v
+    = 0 and the update term is 0, so a param with wd_mult 0 keeps its value
+    bit for bit while a param with wd_mult 1 decays."""
+    params = [dict(numel=300, dtype=BF16, wd_mult=0.0), dict(numel=500, dtype=BF16, wd_mult=1.0)]
+    hp = dict(lr=1e-2, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    m = oracle.ShardMap(params, 1, None, True)
+    (buf,) = m.buffers
+    p0 = synth.normal(buf.numel, synth.key(13, synth.STREAM_PARAM, 0, 0), 0, 0.02, synth.OUT_F32_OF_BF16)
+    st = [{"master": p0.copy(), "exp_avg": np.zeros(buf.numel, np.float32),
+           "exp_avg_sq": np.zeros(buf.numel, np.float32)}]
+    oracle.step(m, [0], [[np.zeros(buf.numel, np.float32)]], st, [np.zeros(buf.numel, np.uint16)], hp, 1)
+    s0, e0, _ = buf.index[0]
+    s1, e1, _ = buf.index[1]
+    assert (st[0]["master"][s0:e0] == p0[s0:e0]).all()
+    nz = p0[s1:e1] != 0
+    assert (np.abs(st[0]["master"][s1:e1][nz]) < np.abs(p0[s1:e1][nz])).all()
 
 
 def test_step_dp1_matches_torch_adamw_and_clip():
@@ -548,6 +650,26 @@ def test_grad_check_locates_each_planted_value():
                 else:
                     assert len(hit) == 0, (ranks, bi, w)
                 assert set(np.unique(amax[amax != 1.0e3])) <= {0.0, base}
+
+
+def test_grad_check_nan_in_any_piece_makes_the_bucket_nan():
+    """A bucket holding several params: a NaN at any element a selected
+    rank reads makes that replica's entry NaN, whichever piece it sits in
+    and whatever the other pieces hold; the other replicas' entries keep
+    their largest magnitude."""
+    params = [dict(numel=n, dtype=BF16) for n in (40, 24, 64, 8)]
+    m = oracle.ShardMap(params, 2, 10**6, True)
+    (buf,) = m.buffers
+    assert len(buf.buckets) == 1
+    owned = [w for pid in buf.params for w in range(buf.index[pid][0], buf.index[pid][1])]
+    assert len(owned) == 136
+    for w in owned[::3] + [owned[-1]]:
+        q = w % 2
+        grads = [[np.full(buf.numel, 2.0, np.float32) for _ in range(2)]]
+        grads[0][q][w] = np.nan
+        st, pb = _zero_state(m, [0, 1])
+        amax = oracle.step(m, [0, 1], grads, st, pb, W.HP, 1, check_grads=True)["grad_amax"]
+        assert math.isnan(amax[q, 0]) and amax[1 - q, 0] == 2.0, w
 
 
 def test_stream_sumsq_equals_array_path():
