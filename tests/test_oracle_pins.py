@@ -54,6 +54,10 @@ def test_bucketing_hand_worked_cases():
         got = [buf.index[i][:2] for i in range(len(params))]
         assert [list(x) for x in got] == case["param_ranges"], case["why"]
         assert [[b.offset, b.numel, b.numel_unpadded] for b in buf.buckets] == case["buckets"], case["why"]
+        # the buffer's sizes: the last bucket's end, and the sum of the
+        # buckets' unpadded sizes (the page's final size assertions)
+        assert buf.numel == case["buckets"][-1][0] + case["buckets"][-1][1], case["why"]
+        assert buf.numel_unpadded == sum(b[2] for b in case["buckets"]), case["why"]
 
 
 def _random_params(rng, n):
@@ -503,6 +507,34 @@ def test_sharding_invariance(dp):
     assert ca < 1 and abs(ca - cb) <= 1e-6 * ca
     for pid in a:
         assert oracle.float_ulp_diff(a[pid], b[pid]).max() <= 4
+
+
+@pytest.mark.parametrize("rank", [1, 3])
+def test_shard_only_replicas_equal_the_full_buffers_slice(rank):
+    """A shard-only replica holds exactly the rank's slice of every bucket of
+    the full grad buffer, concatenated in bucket order: stepping a rank from
+    those slices gives the same main grads, state and params as stepping it
+    from the full buffers."""
+    params = W.gpt2(layers=1, d=64, ffn=256, vocab=97, n_pos=33)
+    m, _, grads, st_full, pb_full = _setup(params, 4, 9000, seed=17, ranks=[rank])
+    _, _, _, st_shard, pb_shard = _setup(params, 4, 9000, seed=17, ranks=[rank])
+    sliced = []
+    for bi, buf in enumerate(m.buffers):
+        idx = np.concatenate([np.arange(*m.bucket_world_range(bi, b, rank).as_tuple())
+                              for b in range(len(buf.buckets))])
+        assert idx.size == m.shard_numel(bi)
+        sliced.append([g[idx].copy() for g in grads[bi]])
+    a = oracle.step(m, [rank], grads, st_full, pb_full, W.HP, 1, layout="full")
+    b = oracle.step(m, [rank], sliced, st_shard, pb_shard, W.HP, 1, layout="shard")
+    assert a["sumsq"] == b["sumsq"] and a["coef"] == b["coef"]
+    for x, y in zip(a["main"], b["main"]):
+        assert x.tobytes() == y.tobytes()
+    for s0, s1 in zip(st_full, st_shard):
+        for k in s0:
+            assert s0[k].tobytes() == s1[k].tobytes()
+    for p0, p1 in zip(pb_full, pb_shard):
+        assert p0.tobytes() == p1.tobytes()
+    assert len(m.buffers) == 2 and any(len(buf.buckets) > 1 for buf in m.buffers)
 
 
 def test_skip_leaves_state_untouched():
