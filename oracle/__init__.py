@@ -16,6 +16,11 @@ Parts:
                   grad, unscale, inf/NaN) -> skip on inf -> clip_grad_norm ->
                   inner AdamW step -> copy main params back to the model
                   param buffer.
+
+Parity unpinned, and not restated here: A7, the dynamic loss scaler's
+backoff, growth and hysteresis policy (host code of the library).  The pages
+fix only a dynamic scale that starts at 2^16; the library's policy is
+checked by hand-worked unit cases, not against this oracle.
 """
 
 import ctypes
