@@ -384,9 +384,9 @@ int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_strea
  * whose step reads the norm back and leaves the update running.  The
  * caller advances its step count only when *found_inf_out is 0.  The
  * results are copied on a side stream (the one dopt_step_from_host uses),
- * so the AdamW pass does not wait for the copy.  MixedPrecisionOptimizer.step skeleton of
- * the distrib_optimizer page: prepare_grads -> (return on inf) ->
- * clip_grad_norm -> step_with_ready_grads.
+ * so the AdamW pass does not wait for the copy.  MixedPrecisionOptimizer.step
+ * skeleton of the distrib_optimizer page: prepare_grads -> (return on inf)
+ * -> clip_grad_norm -> step_with_ready_grads.
  */
 int dopt_step(const dopt_step_args* args, int32_t* found_inf_out, float* grad_norm_out);
 
