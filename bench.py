@@ -314,16 +314,27 @@ def k1_source_sha256():
     return h.hexdigest()
 
 
-def recorded_traffic(elements_k1):
+def k1_variant(cfg, check_grads):
+    """What selects the reduce/prepare kernel of a workload's bf16 buffer:
+    replicas per instance, instances, grad dtype, replica layout, averaging
+    and the grad check."""
+    return {"replicas": cfg["dp"], "instances": cfg["n_inst"],
+            "grad_dtype": "f32" if cfg["grad_reduce_in_fp32"] else "16-bit",
+            "layout": cfg["layout"], "average": bool(cfg.get("average", False)),
+            "grad_check": bool(check_grads)}
+
+
+def recorded_traffic(elements_k1, variant):
     """DRAM traffic of the reduce/prepare pass from the committed ncu summary,
     scaled to this launch's elements; None when the kernel source changed
-    since the counters were taken."""
+    since the counters were taken, or when this workload runs another
+    variant of the kernel than the one captured."""
     path = os.path.join(ROOT, "profiles", "ncu_k1_traffic.json")
     try:
         rec = json.load(open(path))
     except (OSError, ValueError):
         return None
-    if k1_source_sha256() != rec.get("source_sha256"):
+    if k1_source_sha256() != rec.get("source_sha256") or rec.get("variant") != variant:
         return None
     return rec["dram_bytes_per_element"] * elements_k1
 
@@ -572,7 +583,7 @@ def run_ours(args):
     k1_gbs = wl.k1_bytes / (k1 * 1e-3) / 1e9
     k3_gbs = wl.k3_bytes / (k3 * 1e-3) / 1e9
     step_gbs = (wl.k1_bytes + wl.k3_bytes) / (slowest / args.steps * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.elements)
+    traffic = recorded_traffic(wl.elements, k1_variant(cfg, args.check_grads))
 
     # end to end: the step's inputs (the replica grads) copied in from pinned
     # host memory every step, then the C-ABI step, which reads back found_inf

@@ -29,3 +29,24 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_recorded_traffic_applies_only_to_the_captured_variant():
+    """The committed DRAM-traffic record scales to a launch of the kernel
+    variant it was captured on, and to no other (another replica count,
+    dtype, layout, averaging or grad check moves other bytes)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth import workloads as W
+    rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_k1_traffic.json")))
+    default = bench.k1_variant(W.config("llama_7b_dp8_rank0"), False)
+    assert rec["variant"] == default
+    got = bench.recorded_traffic(1000, default)
+    if bench.k1_source_sha256() == rec["source_sha256"]:
+        assert got == rec["dram_bytes_per_element"] * 1000
+    else:
+        assert got is None
+    for name, check in (("toy_mlp_dp4", False), ("llama_7b_dp8_rank0_bf16grads", False),
+                        ("llama_7b_dp8_rank0_avg", False), ("llama_7b_dp16_2x8_40m", False),
+                        ("llama_7b_dp8_rank0", True)):
+        assert bench.recorded_traffic(1000, bench.k1_variant(W.config(name), check)) is None, name
