@@ -272,6 +272,33 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(self.samples)}
 
 
+REJECTED_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def clocks_rejected(clk, low=0.85):
+    """A timed region's clock record that does not count: a hardware or
+    thermal slowdown was active, or the median SM clock sat below `low` x
+    its maximum with no reason active (a clock lock).  sw_power_cap alone
+    is kept."""
+    if any(r in clk["reasons"] for r in REJECTED_REASONS):
+        return True
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    return bool(sm and mx and sm < low * mx and not clk["reasons"])
+
+
+def any_rank(flag, world):
+    """True on every rank when `flag` is true on any rank."""
+    if world <= 1:
+        return bool(flag)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([1.0 if flag else 0.0], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return bool(t.item() > 0)
+
+
 def host_available_bytes():
     """MemAvailable of /proc/meminfo (bytes); a large value when unknown."""
     try:
@@ -542,38 +569,50 @@ def run_ours(args):
         wl.step(sargs)
     torch.cuda.synchronize()
 
-    # device-resident timed region
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for e4 in ev:  # torch creates the CUDA event on its first record
-        for e in e4:
-            e.record()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    # inputs smaller than L2 (the toy MLP): write a buffer of twice the L2
-    # size between the timed steps and time each step from its own first to
-    # last stage event, so the flushes stay outside the timed work
+    # device-resident timed region.  Inputs smaller than L2 (the toy MLP):
+    # write a buffer of twice the L2 size between the timed steps and time
+    # each step from its own first to last stage event, so the flushes stay
+    # outside the timed work.
     l2_bytes = torch.cuda.get_device_properties(local_rank).L2_cache_size
     rep_bytes = sum(r.numel() * r.element_size() for reps in wl.reps for r in reps)
-    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if rep_bytes < 2 * l2_bytes else None
-    clocks = ClockSampler(local_rank)
-    time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    launches0 = D.dopt_kernel_launches()
-    start.record()
-    for i in range(args.steps):
-        if flush is not None:
-            flush.fill_(i & 0xFF)
-        wl.step(sargs, ev[i])
-    end.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    launches = D.dopt_kernel_launches() - launches0
-    clocks.stop()
-    if flush is None:
-        elapsed = start.elapsed_time(end)
-    else:
-        elapsed = sum(e[0].elapsed_time(e[3]) for e in ev)
-        del flush
+
+    def timed_region():
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for e4 in ev:  # torch creates the CUDA event on its first record
+            for e in e4:
+                e.record()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if rep_bytes < 2 * l2_bytes else None
+        clocks = ClockSampler(local_rank)
+        time.sleep(0.3)
+        barrier(world)
+        torch.cuda.synchronize()
+        launches0 = D.dopt_kernel_launches()
+        start.record()
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            wl.step(sargs, ev[i])
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        launches = D.dopt_kernel_launches() - launches0
+        clocks.stop()
+        if flush is None:
+            elapsed = start.elapsed_time(end)
+        else:
+            elapsed = sum(e[0].elapsed_time(e[3]) for e in ev)
+        return elapsed, ev, launches, clocks.summary()
+
+    # a run whose clocks show a hardware or thermal slowdown, or SM clocks
+    # held well below their maximum with no reason given (a clock lock left
+    # behind), is taken once more; every rank decides alike
+    elapsed, ev, launches, clk = timed_region()
+    first_clocks = None
+    if any_rank(clocks_rejected(clk), world):
+        first_clocks = clk
+        log(f"[bench] rank {rank}: timed region taken again (clocks {clk})")
+        elapsed, ev, launches, clk = timed_region()
     k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     k2 = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     k3 = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
@@ -682,8 +721,10 @@ def run_ours(args):
         "stages": {"reduce_prepare_ms": k1, "norm_finalize_ms": k2, "adamw_ms": k3,
                    "adamw_gbs": k3_gbs, "adamw_frac": k3_gbs / peak,
                    "step_bytes": wl.k1_bytes + wl.k3_bytes},
-        "e2e": e2e, "gpu_launches": launches, "clocks": clocks.summary(), "cpu_baseline": cpu,
+        "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
     }
+    if first_clocks is not None:
+        line["remeasured"] = {"first_clocks": first_clocks}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

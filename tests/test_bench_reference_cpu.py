@@ -50,3 +50,19 @@ def test_recorded_traffic_applies_only_to_the_captured_variant():
                         ("llama_7b_dp8_rank0_avg", False), ("llama_7b_dp16_2x8_40m", False),
                         ("llama_7b_dp8_rank0", True)):
         assert bench.recorded_traffic(1000, bench.k1_variant(W.config(name), check)) is None, name
+
+
+def test_clock_records_that_are_rejected():
+    """A timed region is taken again when a hardware or thermal slowdown was
+    active, or when SM clocks sat well below their maximum with no reason
+    (a clock lock); a power cap alone is kept."""
+    sys.path.insert(0, ROOT)
+    import bench
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10}
+    assert not bench.clocks_rejected(ok)
+    assert not bench.clocks_rejected(dict(ok, sm_mhz=1600.0, reasons=["sw_power_cap"]))
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected(dict(ok, reasons=[r]))
+    assert bench.clocks_rejected(dict(ok, sm_mhz=1200.0))
+    assert not bench.clocks_rejected(dict(ok, sm_mhz=None, sm_max_mhz=None, samples=0))
+    assert bench.any_rank(True, 1) and not bench.any_rank(False, 1)

@@ -40,7 +40,10 @@ def _aggregate_worker(rank, world, port, out):
     _init(rank, world, port)
     elapsed = [100.0, 250.0][rank]
     value, slowest = bench.aggregate(elapsed, 1_000_000, 10, world)
-    out[rank] = (value, slowest)
+    # the re-measure decision: one rank's bad clock record decides for all
+    again = bench.any_rank(rank == 1, world)
+    never = bench.any_rank(False, world)
+    out[rank] = (value, slowest, again, never)
     dist.destroy_process_group()
 
 
@@ -51,7 +54,8 @@ def test_bench_aggregate_max_over_ranks():
         mp.spawn(_aggregate_worker, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)
     for r in (0, 1):
-        value, slowest = res[r]
+        value, slowest, again, never = res[r]
+        assert again is True and never is False
         assert slowest == 250.0
         assert value == pytest.approx(1_000_000 * 10 * 2 / 0.25)
 
