@@ -132,6 +132,40 @@ def algorithmic_bytes(D, pm, n_rep, ranks):
     return k1, k3, elems
 
 
+def line_config(cfg, elements, rep_bytes, l2_bytes, check_grads):
+    """The `config` object of both arms' lines: the workload, its stepped
+    elements and replicas, how L2 is kept out of the timing, the
+    parallelism and the grad check."""
+    if l2_bytes is None:
+        l2 = "L2 size unknown (no GPU visible)"
+    elif rep_bytes < 2 * l2_bytes:
+        l2 = (f"inputs smaller than L2 ({rep_bytes / 1e6:.1f} MB of replica grads): "
+              f"{2 * l2_bytes / 1e6:.0f} MB written between timed steps, each step timed "
+              "from its first to its last event")
+    else:
+        l2 = ("no flush needed: inputs larger than L2 (the replica grads alone are "
+              f"{rep_bytes / 1e9:.1f} GB per step)")
+    return {"workload": describe(cfg, elements), "elements_per_step": elements,
+            "replicas": cfg["dp"] * cfg["n_inst"], "l2": l2,
+            "parallelism": "replicas only: each GPU runs its own emulated DP instance",
+            "grad_check": bool(check_grads)}
+
+
+def oracle_counts(cfg):
+    """Stepped elements and replica-grad bytes of one step, counted from the
+    oracle's shard map (the reference arm's path: no product code)."""
+    import oracle
+    m = oracle.ShardMap(cfg["params"], cfg["dp"], cfg["bucket_size"], cfg["grad_reduce_in_fp32"])
+    ranks = list(range(cfg["dp"])) if cfg["ranks"] == "all" else list(cfg["ranks"])
+    n_rep = cfg["dp"] * cfg["n_inst"]
+    elements = rep_bytes = 0
+    for bi, buf in enumerate(m.buffers):
+        elements += sum(v["gbuf_local"].size for r in ranks for _, _, v in m.rank_pieces(bi, r))
+        n = buf.numel if cfg["layout"] == "full" else m.shard_numel(bi)
+        rep_bytes += n_rep * n * ELEM_BYTES[buf.grad_dtype]
+    return elements, rep_bytes
+
+
 class Workload:
     """Device tensors of one rank's shard, filled by the seeded generator."""
 
@@ -503,6 +537,15 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg = workload_config(args.workload, args.layers)
+    # the same config object as this workload's line of the GPU arm
+    elements, rep_bytes = oracle_counts(cfg)
+    l2_bytes = None
+    try:
+        import torch
+        if torch.cuda.is_available():
+            l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
+    except ImportError:
+        pass
     per_step = REFERENCE_BUDGET_ELEMENTS // max(1, args.steps + args.warmup)
     per_step = max(1 << 20, min(CPU_SAMPLE_ELEMENTS, per_step))
     sample = OracleSample(cfg, per_step)
@@ -522,7 +565,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{cfg['name']}, a bounded sample per step (see cpu_baseline)"},
+            "config": line_config(cfg, elements, rep_bytes, l2_bytes, False),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step: {sample.describe()}, {cores} threads "
                                        "(one fixed chunk each)"},
@@ -704,15 +747,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": slowest / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": describe(cfg, wl.elements), "elements_per_step": wl.elements,
-                   "replicas": wl.n_rep,
-                   "l2": (f"inputs smaller than L2 ({rep_bytes / 1e6:.1f} MB of replica grads): "
-                          f"{2 * l2_bytes / 1e6:.0f} MB written between timed steps, each step timed "
-                          "from its first to its last event" if rep_bytes < 2 * l2_bytes else
-                          "no flush needed: inputs larger than L2 (the replica grads alone are "
-                          f"{rep_bytes / 1e9:.1f} GB per step)"),
-                   "parallelism": "replicas only: each GPU runs its own emulated DP instance",
-                   "grad_check": bool(args.check_grads)},
+        "config": line_config(cfg, wl.elements, rep_bytes, l2_bytes, args.check_grads),
         "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
         "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s",
                      "frac": k1_gbs / peak, "traffic": traffic, "kernel": "k1_reduce_prepare",

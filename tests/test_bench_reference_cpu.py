@@ -66,3 +66,20 @@ def test_clock_records_that_are_rejected():
     assert bench.clocks_rejected(dict(ok, sm_mhz=1200.0))
     assert not bench.clocks_rejected(dict(ok, sm_mhz=None, sm_max_mhz=None, samples=0))
     assert bench.any_rank(True, 1) and not bench.any_rank(False, 1)
+
+
+def test_both_arms_count_the_same_workload():
+    """The reference arm counts the stepped elements with the oracle's shard
+    map, the GPU arm with the library's: the two agree on every workload, so
+    both lines carry the same config."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import mixed_precision_adam_gb300 as D
+    from synth import workloads as W
+    for name in W.NAMES:
+        cfg = W.config(name)
+        pm = D.dopt_build_shard_map(cfg["params"], cfg["dp"], cfg["bucket_size"],
+                                    cfg["grad_reduce_in_fp32"], False)
+        ranks = list(range(cfg["dp"])) if cfg["ranks"] == "all" else list(cfg["ranks"])
+        _, _, elements = bench.algorithmic_bytes(D, pm, cfg["dp"] * cfg["n_inst"], ranks)
+        assert bench.oracle_counts(cfg)[0] == elements, name
