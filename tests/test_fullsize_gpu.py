@@ -95,6 +95,15 @@ def test_hierarchical_llama7b_dp16_2x8_1m_buckets():
     _run(W.config("llama_7b_dp16_2x8_1m"), steps=1)
 
 
+def test_average_in_collective_llama7b_dp8_rank0():
+    _run(W.config("llama_7b_dp8_rank0_avg"), steps=1)
+
+
+def test_dp16_one_instance_general_reduce_kernel():
+    # 16 replicas in one instance: the reduce pass's general kernel
+    _run(W.config("llama_7b_dp16_rank0"), steps=1)
+
+
 def test_gpt2_small_all_ranks_with_skipped_step():
     _run(W.config("gpt2_small_dp8"), steps=3)
 
