@@ -166,6 +166,23 @@ def oracle_counts(cfg):
     return elements, rep_bytes
 
 
+def read_once_bytes(D, pm, n_rep, ranks):
+    """Bytes of one step if every input were read once and every output
+    written once, with no main grad between two passes: the replica grads,
+    master, m and v read; master, m, v and (16-bit buffers) the param
+    written.  A global-norm clip cannot reach it (the update of any element
+    needs every element's grad first), so it is reported beside the
+    two-pass count, not as the target."""
+    total = 0
+    for b in range(D.dopt_num_buffers(pm)):
+        info = D.dopt_buffer_info_get(pm, b)
+        n = sum(s["gbuf_local"][1] - s["gbuf_local"][0]
+                for r in ranks for s in D.dopt_rank_shards(pm, b, r))
+        p = ELEM_BYTES[info["param_dtype"]] if info["param_dtype"] != F32 else 0
+        total += n * (n_rep * ELEM_BYTES[info["grad_dtype"]] + 24 + p)
+    return total
+
+
 class Workload:
     """Device tensors of one rank's shard, filled by the seeded generator."""
 
@@ -231,6 +248,7 @@ class Workload:
         torch.cuda.synchronize()
         self.k1_bytes, self.k3_bytes, self.elements = algorithmic_bytes(D, self.pm, self.n_rep,
                                                                         self.ranks)
+        self.read_once_bytes = read_once_bytes(D, self.pm, self.n_rep, self.ranks)
         self.t_applied = 0
 
     def args(self, reps=None):
@@ -749,6 +767,11 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": line_config(cfg, wl.elements, rep_bytes, l2_bytes, args.check_grads),
         "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+        "read_once_ideal": {"bytes_per_step": wl.read_once_bytes,
+                            "ms_at_peak": wl.read_once_bytes / (peak * 1e9) * 1e3,
+                            "step_frac": wl.read_once_bytes / (peak * 1e9) * 1e3 / (slowest / args.steps),
+                            "note": "every input read once, no main grad between two passes: "
+                                    "out of reach with a global-norm clip"},
         "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s",
                      "frac": k1_gbs / peak, "traffic": traffic, "kernel": "k1_reduce_prepare",
                      "algorithmic_bytes_per_launch": wl.k1_bytes, "peak_source": peak_src},

@@ -83,3 +83,17 @@ def test_both_arms_count_the_same_workload():
         ranks = list(range(cfg["dp"])) if cfg["ranks"] == "all" else list(cfg["ranks"])
         _, _, elements = bench.algorithmic_bytes(D, pm, cfg["dp"] * cfg["n_inst"], ranks)
         assert bench.oracle_counts(cfg)[0] == elements, name
+
+
+def test_read_once_ideal_is_4n_plus_26_bytes():
+    """The read-once ideal of a bf16-param buffer is 4N + 26 B per element
+    for N fp32 replicas (2N + 26 for 16-bit grads); an fp32-param buffer
+    writes no separate param (4N + 24)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import mixed_precision_adam_gb300 as D
+    for grad_fp32, dp, want in ((True, 8, 4 * 8 + 26), (False, 8, 2 * 8 + 26), (True, 4, 4 * 4 + 26)):
+        pm = D.dopt_build_shard_map([dict(numel=1 << 16, dtype=D.BF16)], dp, 0, grad_fp32, False)
+        assert bench.read_once_bytes(D, pm, dp, list(range(dp))) == want * (1 << 16)
+    pm = D.dopt_build_shard_map([dict(numel=4096, dtype=D.F32)], 4, 0, True, False)
+    assert bench.read_once_bytes(D, pm, 4, [1]) == (4 * 4 + 24) * 1024
