@@ -576,6 +576,17 @@ int dopt_state_from_model(const dopt_shard_map* map, int32_t buffer, int32_t ran
  * hook off (the default).  Not for production use. */
 int dopt_debug_starve_copy(int32_t tile);
 
+/* Debug builds only (compiled with DOPT_BOUNDS_CHECK=1; the default build
+ * returns DOPT_E_INVALID).  Every kernel of such a build checks each tile's
+ * element ranges against the extents of the buffers it reads and writes
+ * (each replica, the main grad, master/m/v, the param buffer, the grad-check
+ * slots) and skips a tile that falls outside them instead of touching it.
+ * This call copies the record of such tiles on the current device to out[4]
+ * -- the number of failed checks, the first failure's check site, first
+ * element and extent -- clears it, and waits for the device.  A count of 0
+ * means every access stayed inside its buffer. */
+int dopt_debug_bounds_record(int64_t* out);
+
 /* Number of kernels this library has launched in this process (all
  * devices, all threads); a caller can difference it around a region. */
 uint64_t dopt_kernel_launches(void);

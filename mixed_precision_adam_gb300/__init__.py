@@ -11,7 +11,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "lib", "libdopt.so")
+# DOPT_LIBRARY may name another in-tree build of the same library (the
+# bounds-checked debug build, lib/libdopt_checked.so)
+LIB_PATH = os.environ.get("DOPT_LIBRARY") or os.path.join(HERE, "lib", "libdopt.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
@@ -146,6 +148,7 @@ _c = {
                                       ctypes.POINTER(dopt_loss_scaler), _I32),
     "dopt_kernel_launches": _proto("dopt_kernel_launches", ctypes.c_uint64),
     "dopt_debug_starve_copy": _proto("dopt_debug_starve_copy", ctypes.c_int, _I32),
+    "dopt_debug_bounds_record": _proto("dopt_debug_bounds_record", ctypes.c_int, ctypes.POINTER(_I64)),
     "dopt_read_step_stats": _proto("dopt_read_step_stats", ctypes.c_int, _P,
                                    ctypes.POINTER(dopt_step_stats), _P),
     "dopt_last_error": _proto("dopt_last_error", ctypes.c_char_p),
@@ -465,6 +468,14 @@ def dopt_read_step_stats(workspace, stream=None):
 
 def dopt_debug_starve_copy(tile):
     _check(_c["dopt_debug_starve_copy"](tile))
+
+
+def dopt_debug_bounds_record():
+    """(failed checks, first site, first element, extent) of a bounds-checked
+    build's record on the current device, which the call clears."""
+    out = (_I64 * 4)()
+    _check(_c["dopt_debug_bounds_record"](out))
+    return tuple(out)
 
 
 def dopt_kernel_launches():

@@ -20,6 +20,12 @@
 // comes from cudaGetSymbolAddress, once per device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DOPT_NOALLOC_SCRATCH_BYTES];
 
+#if DOPT_BOUNDS_CHECK
+// Debug builds: the record of the first tile found outside its buffers
+// ([count, site, first element, extent]), read by dopt_debug_bounds_record.
+static __device__ unsigned long long g_bounds_record[4];
+#endif
+
 namespace {
 std::atomic<uint64_t> g_launches{0};  // kernels launched by this library
 
@@ -192,7 +198,37 @@ struct K1Job {
   bool compact = false;      // 16-bit grads: keep the reduced grads in the grad dtype
   const FinalizeArgs* fin = nullptr;  // finalize in the last launch's last CTA (fused step)
   uint32_t* fin_counter = nullptr;
+  int64_t ext_rep = 0, ext_main = 0;  // element extents of each replica and of main_grad
 };
+
+// Element extents of a rank selection's flat-shard arrays and of one
+// replica in the given layout (whole buffer, or the selection's shard).
+int64_t shard_extent(const dopt_shard_map* m, int32_t buffer, int32_t rank) {
+  return (int64_t)n_rank_slots(m, rank) * shard_numel(m, buffer);
+}
+int64_t replica_extent(const dopt_shard_map* m, int32_t buffer, int32_t rank, bool full) {
+  return full ? m->buffers[buffer].numel : shard_extent(m, buffer, rank);
+}
+
+#if DOPT_BOUNDS_CHECK
+// Device address of g_bounds_record on the current device.
+int bounds_record(unsigned long long** out) {
+  static std::mutex mu;
+  static unsigned long long* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return fail(DOPT_E_CUDA, "bounds record: cudaGetDevice");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_bounds_record);
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("bounds record: ") + cudaGetErrorString(e));
+    addr[dev] = static_cast<unsigned long long*>(a);
+  }
+  *out = addr[dev];
+  return DOPT_OK;
+}
+#endif
 
 // Launches K1 over every chunk of a run list; with stats, chunk i writes its
 // partials to workspace region region_first + i.
@@ -221,6 +257,10 @@ int run_k1_runs(const std::vector<Run>& runs, int region_first, const K1Job& j, 
     const bool last = &c == &chunks.back();
     kp.fin_counter = (j.fin && last) ? j.fin_counter : nullptr;
     if (kp.fin_counter) kp.fin = *j.fin;
+#if DOPT_BOUNDS_CHECK
+    kp.ext = Extents{j.ext_rep, j.ext_main, 0, 0, j.amax_stride, nullptr};
+    if (int st = bounds_record(&kp.ext.record)) return st;
+#endif
     const K1Launch l{runs.data() + c.first, c.count, j.bucket_base, j.full, j.stats, j.amax != nullptr};
     int st;
     switch (j.gdt) {
@@ -261,6 +301,8 @@ K1Job step_job(const dopt_step_args* a, int32_t b) {
   j.amax_stride = bucket_number(m, (int32_t)m->buffers.size(), 0);
   j.bucket_base = bucket_number(m, b, 0);
   j.compact = j.gdt != DOPT_F32;
+  j.ext_rep = replica_extent(m, b, a->rank, j.full);
+  j.ext_main = shard_extent(m, b, a->rank);
   return j;
 }
 
@@ -353,6 +395,7 @@ struct K3Job {
   const float* d_coef = nullptr;
   const int32_t* d_found = nullptr;
   const DevStep* dev = nullptr;   // device step scalars, or NULL: from hp
+  int64_t ext_main = 0, ext_state = 0, ext_param = 0;  // element extents (debug builds check them)
 };
 
 int run_k3_runs(const std::vector<Run>& runs, const K3Job& j, cudaStream_t s) {
@@ -377,6 +420,10 @@ int run_k3_runs(const std::vector<Run>& runs, const K3Job& j, cudaStream_t s) {
     kp.step_size = (float)(hp->lr / (1.0 - pow_int(hp->beta1, hp->step)));
     kp.bc2_sqrt = (float)std::sqrt(1.0 - pow_int(hp->beta2, hp->step));
     kp.inv_scale = j.inv_scale;
+#if DOPT_BOUNDS_CHECK
+    kp.ext = Extents{0, j.ext_main, j.ext_state, j.ext_param, 0, nullptr};
+    if (int st = bounds_record(&kp.ext.record)) return st;
+#endif
     int st = launch_k3(j.param_dtype, j.main_dtype, kp, runs.data() + c.first, c.count, s);
     if (st) return st;
   }
@@ -401,6 +448,8 @@ K3Job step_job3(const dopt_step_args* a, int32_t b) {
   j.d_coef = &sc->clip_coef;
   j.d_found = &sc->found_inf;
   j.dev = a->d_step ? dev_step_ptr(a->workspace) : nullptr;
+  j.ext_main = j.ext_state = shard_extent(m, b, a->rank);
+  j.ext_param = m->buffers[b].numel;
   return j;
 }
 
@@ -573,6 +622,23 @@ extern "C" {
 
 uint64_t dopt_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int dopt_debug_bounds_record(int64_t* out) {
+  if (!out) return fail(DOPT_E_INVALID, "dopt_debug_bounds_record: NULL out");
+#if DOPT_BOUNDS_CHECK
+  unsigned long long* rec = nullptr;
+  if (int st = bounds_record(&rec)) return st;
+  unsigned long long h[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaMemcpy(h, rec, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(rec, 0, sizeof(h));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("dopt_debug_bounds_record: ") + cudaGetErrorString(e));
+  for (int k = 0; k < 4; ++k) out[k] = (int64_t)h[k];
+  return DOPT_OK;
+#else
+  return fail(DOPT_E_INVALID, "dopt_debug_bounds_record: this library was built without DOPT_BOUNDS_CHECK");
+#endif
+}
+
 int dopt_debug_starve_copy(int32_t tile) {
   if (tile < -1) return fail(DOPT_E_INVALID, "dopt_debug_starve_copy: tile < -1");
   g_starve_tile.store(tile, std::memory_order_relaxed);
@@ -618,6 +684,8 @@ int dopt_grad_reduce_shard(const dopt_shard_map* map, int32_t buffer, int32_t ra
   j.average = average_in_collective;
   j.gdt = m->buffers[buffer].grad_dtype;
   j.main_grad = main_grad;
+  j.ext_rep = replica_extent(m, buffer, rank, j.full);
+  j.ext_main = shard_extent(m, buffer, rank);
   return run_k1(m, buffer, rank, j, (cudaStream_t)stream);
 }
 
@@ -642,6 +710,7 @@ int dopt_prepare_grads(const dopt_shard_map* map, int32_t buffer, int32_t rank,
   j.main_grad = main_grad;
   j.stats = true;
   j.ws = workspace;
+  j.ext_rep = j.ext_main = shard_extent(m, buffer, rank);
   return run_k1(m, buffer, rank, j, (cudaStream_t)stream);
 }
 
@@ -682,6 +751,8 @@ int dopt_adam_step(const dopt_shard_map* map, int32_t buffer, int32_t rank, cons
   j.hp = hp;
   j.d_coef = d_clip_coef;
   j.d_found = d_found_inf;
+  j.ext_main = j.ext_state = shard_extent(m, buffer, rank);
+  j.ext_param = m->buffers[buffer].numel;
   return run_k3_runs(runs_for(m, buffer, rank), j, (cudaStream_t)stream);
 }
 

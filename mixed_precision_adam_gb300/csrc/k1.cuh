@@ -406,6 +406,9 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
     const int64_t l0 = sg.local + off;
     const int64_t r0 = FULL ? sg.world + off : l0;
     const bool aligned = seg_aligned(sg.local, sg.world);
+    if (!(DOPT_RANGE_OK(p, kSiteK1Rep, r0, n, rep) && DOPT_RANGE_OK(p, kSiteK1Main, l0, n, main) &&
+          (!CHECK || DOPT_RANGE_OK(p, kSiteK1Bucket, sg.bucket, 1, buckets))))
+      continue;  // debug builds only: a tile outside its buffers is skipped (CTA-uniform)
     if constexpr (CHECK) {
       if (sg.bucket != cur_bucket) {
         if (cur_bucket >= 0) flush_bucket(cur_bucket);
@@ -535,6 +538,9 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
     const int64_t l0 = sg.local + off;
     const int64_t r0 = FULL ? sg.world + off : l0;
     const bool aligned = seg_aligned(sg.local, sg.world);
+    if (!(DOPT_RANGE_OK(p, kSiteK1Rep, r0, n, rep) && DOPT_RANGE_OK(p, kSiteK1Main, l0, n, main) &&
+          (!CHECK || DOPT_RANGE_OK(p, kSiteK1Bucket, sg.bucket, 1, buckets))))
+      continue;  // debug builds only: a tile outside its buffers is skipped (CTA-uniform)
     if constexpr (CHECK) {
       if (sg.bucket != cur_bucket) {
         if (cur_bucket >= 0) flush_bucket(cur_bucket);
@@ -680,8 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
     const int nv = n & ~(VALIGN - 1);
     const int64_t r0 = FULL ? sg.world + off : sg.local + off;
     const int stage = i % S;
-    mbar_arrive_expect_tx(&bars[stage], (unsigned)(nv * sizeof(E)) * DPI);
-    if (nv > 0 && !(blockIdx.x == 0 && i == p.starve_tile)) {
+    // debug builds: a tile outside the replicas is not copied, and its stage
+    // completes on the arrival alone
+    const bool copy_ok = DOPT_RANGE_OK(p, kSiteTmaCopy, r0, n, rep);
+    mbar_arrive_expect_tx(&bars[stage], copy_ok ? (unsigned)(nv * sizeof(E)) * DPI : 0u);
+    if (copy_ok && nv > 0 && !(blockIdx.x == 0 && i == p.starve_tile)) {
 #pragma unroll
       for (int k = 0; k < DPI; ++k)
         bulk_load(tiles + ((size_t)stage * DPI + k) * kTmaTile, static_cast<const E*>(p.rep[k]) + r0,
@@ -717,10 +726,15 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
     si = seek(p.tab, si, t);
     const Seg& sg = p.tab.seg[si];
     const int64_t off = (int64_t)(t - sg.tile0) * kTmaTile;
-    const int n = (int)min((int64_t)kTmaTile, (int64_t)sg.len - off);
-    const int nv = n & ~(VALIGN - 1);
     const int64_t l0 = sg.local + off;
     const int64_t r0 = FULL ? sg.world + off : l0;
+    const int n_run = (int)min((int64_t)kTmaTile, (int64_t)sg.len - off);
+    // debug builds: a tile outside its buffers gets no elements (no access)
+    const int n = (DOPT_RANGE_OK(p, kSiteK1Rep, r0, n_run, rep) && DOPT_RANGE_OK(p, kSiteK1Main, l0, n_run, main) &&
+                   (!CHECK || DOPT_RANGE_OK(p, kSiteK1Bucket, sg.bucket, 1, buckets)))
+                      ? n_run
+                      : 0;
+    const int nv = n & ~(VALIGN - 1);
     const E* st = tiles + (size_t)stage * DPI * kTmaTile;
     if constexpr (CHECK) {
       if (sg.bucket != cur_bucket) {

@@ -159,6 +159,12 @@ __device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, 
   T.l0 = sg.local + off;
   T.w0 = sg.world + off;
   T.m0 = ParamT<PT>::kInPlace ? T.w0 : T.l0;
+  // debug builds: a tile outside its buffers gets no elements (no access)
+  if (!(DOPT_RANGE_OK(p, kSiteK3Main, T.l0, T.n, main) && DOPT_RANGE_OK(p, kSiteK3State, T.l0, T.n, state) &&
+        (ParamT<PT>::kInPlace ? DOPT_RANGE_OK(p, kSiteK3Master, T.m0, T.n, param)
+                              : DOPT_RANGE_OK(p, kSiteK3Master, T.m0, T.n, state) &&
+                                    DOPT_RANGE_OK(p, kSiteK3Param, T.w0, T.n, param))))
+    T.n = 0;
   T.aligned = seg_aligned(sg.local, sg.world);
   T.decay = decay;
 #pragma unroll

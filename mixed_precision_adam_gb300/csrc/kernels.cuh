@@ -58,6 +58,9 @@
 #ifndef DOPT_K3_MIN_BLOCKS
 #define DOPT_K3_MIN_BLOCKS 4
 #endif
+#ifndef DOPT_BOUNDS_CHECK
+#define DOPT_BOUNDS_CHECK 0  // 1: debug build; every tile is checked against the extents of its buffers
+#endif
 
 namespace dopt {
 
@@ -151,6 +154,40 @@ struct FinalizeArgs {
   K2Step step;
 };
 
+// Debug builds (DOPT_BOUNDS_CHECK=1): the extents, in elements, of the
+// buffers a launch touches, and a device record of the first tile whose
+// range falls outside one of them: [count, site, first element, extent].
+// Such a tile is skipped, not accessed.
+struct Extents {
+  int64_t rep;      // each replica (K1)
+  int64_t main;     // the main-grad array (K1 writes, K3 reads)
+  int64_t state;    // master, exp_avg, exp_avg_sq (K3)
+  int64_t param;    // the param buffer (K3)
+  int64_t buckets;  // grad-check slots per replica (K1 with the check)
+  unsigned long long* record;
+};
+
+// Where a range is checked, as recorded.
+enum BoundsSite : int {
+  kSiteK1Rep = 1, kSiteK1Main = 2, kSiteK1Bucket = 3, kSiteTmaCopy = 4,
+  kSiteK3Main = 5, kSiteK3State = 6, kSiteK3Master = 7, kSiteK3Param = 8
+};
+
+#if DOPT_BOUNDS_CHECK
+__device__ __forceinline__ bool range_ok(const Extents& x, int site, int64_t lo, int64_t n, int64_t extent) {
+  if (lo >= 0 && n >= 0 && lo + n <= extent) return true;
+  if (atomicAdd(x.record, 1ull) == 0ull) {
+    x.record[1] = (unsigned long long)site;
+    x.record[2] = (unsigned long long)lo;
+    x.record[3] = (unsigned long long)extent;
+  }
+  return false;
+}
+#define DOPT_RANGE_OK(params, site, lo, n, field) ::dopt::range_ok((params).ext, (site), (lo), (n), (params).ext.field)
+#else
+#define DOPT_RANGE_OK(params, site, lo, n, field) true
+#endif
+
 struct K1Params {
   const void* rep[DOPT_MAX_REPLICAS];
   float* main_grad;
@@ -174,6 +211,9 @@ struct K1Params {
   // CTA to take a ticket from *fin_counter runs it; NULL: none
   uint32_t* fin_counter;
   FinalizeArgs fin;
+#if DOPT_BOUNDS_CHECK
+  Extents ext;
+#endif
   SegTable tab;
 };
 
@@ -189,6 +229,9 @@ struct K3Params {
   double lr_wd;        // lr * weight_decay (host step)
   float b1, b2, omb1, omb2, eps, step_size, bc2_sqrt;
   float inv_scale;     // compact main grads: main = widen(stored) * inv_scale
+#if DOPT_BOUNDS_CHECK
+  Extents ext;
+#endif
   SegTable tab;
 };
 

@@ -224,3 +224,13 @@ def test_bad_arguments_return_status():
         with pytest.raises(dopt.DoptError) as e:
             dopt.dopt_bucket_number(m, buffer, bucket)
         assert e.value.status == dopt.E_INVALID
+
+
+def test_bounds_record_needs_the_checked_build():
+    """The default build exports the debug query but refuses it: its kernels
+    carry no bounds checks."""
+    if os.environ.get("DOPT_LIBRARY"):
+        pytest.skip("another build of the library is loaded")
+    with pytest.raises(dopt.DoptError) as e:
+        dopt.dopt_debug_bounds_record()
+    assert e.value.status == dopt.E_INVALID
