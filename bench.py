@@ -552,7 +552,7 @@ REFERENCE_BUDGET_ELEMENTS = 3_000_000_000
 
 
 def run_reference(args):
-    rank, _, world = dist_env()
+    rank, _, _ = dist_env()
     if rank != 0:
         return 0
     cfg = workload_config(args.workload, args.layers)
@@ -697,8 +697,8 @@ def run_ours(args):
         # (the bytes moved per step stay the same)
         per_rep = [r.numel() * r.element_size() for reps in wl.reps for r in reps]
         budget = 0.5 * host_available_bytes() / world
-        host_reps, src_of, used = [], {}, 0
-        for bi, reps in enumerate(wl.reps):
+        host_reps, used = [], 0
+        for reps in wl.reps:
             hb = []
             for k, r in enumerate(reps):
                 nbytes = r.numel() * r.element_size()

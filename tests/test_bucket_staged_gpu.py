@@ -3,7 +3,6 @@ finalize, AdamW and write-back per bucket in the order the next forward
 needs them) against the fused step: the same arithmetic, so the results must
 be bit-identical, whatever the grouping of buckets and the streams used."""
 
-import numpy as np
 import pytest
 
 from synth import workloads as W
