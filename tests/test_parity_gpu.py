@@ -228,3 +228,30 @@ def test_bounded_wait_runs_out_and_reports():
     found, norm = dc.step(grads, 1)
     assert H.compare_step(hc, dc, ores, found, norm, snap, report), "\n".join(report)
     assert D.dopt_read_step_stats(dc.ws)["kernel_error"] == 0
+
+
+@pytest.mark.parametrize("t", [2, 37, 1000, 123_457, 2**31 + 5])
+@pytest.mark.parametrize("device_step", [False, True])
+def test_bias_correction_at_large_step_numbers(t, device_step):
+    """The bias corrections 1 - beta1^t and sqrt(1 - beta2^t) at step
+    numbers far past those the workloads reach, where beta^t falls below an
+    fp32 ulp of 1: one step from a warm state (nonzero m and v) with step
+    number t, from host-computed step scalars and from the device step
+    counter (holding t - 1), against the oracle."""
+    D = H.dopt()
+    cfg = _tiny(RAGGED[:6], 4, bucket_size=3000, warm_state=True, steps=1, grad_sigma=1e-2)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    grads = hc.grads(1)
+    before = H.snapshot(hc)
+    ores = hc.oracle_step(grads, t)
+    if device_step:
+        args = dc.step_args([[dc._up(r) for r in g] for g in grads], 1)
+        d_step = torch.tensor([t - 1], dtype=torch.int64, device="cuda")
+        args.set_device_step(d_step)
+        found, norm = D.dopt_step(args)
+        assert int(d_step.item()) == (t - 1 if found else t)
+    else:
+        found, norm = dc.step(grads, t)
+    report = []
+    assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
