@@ -255,3 +255,49 @@ def test_bias_correction_at_large_step_numbers(t, device_step):
         found, norm = dc.step(grads, t)
     report = []
     assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
+
+
+def _bf16_value(x):
+    """The nearest bf16 value of x, as a float (exact in the bf16 bits)."""
+    return float(torch.tensor([x], dtype=torch.float32).to(torch.bfloat16).float().item())
+
+
+@pytest.mark.parametrize("grad_fp32", [False, True])
+@pytest.mark.parametrize("values", ["below_2_62", "above_2_62", "mixed_max"])
+def test_huge_finite_grads_are_finite(grad_fp32, values):
+    """Finite grads whose squares overflow fp32 (or come within a factor 16
+    of it: the largest values the norm's fp32 accumulator takes, 16 of them
+    per thread and tile in the 16-bit reduce kernel) must neither set
+    found_inf nor lose the norm: every replica holds the same value v at an
+    element, so the reduced grad is v exactly, with alternating signs and,
+    for "mixed_max", values up to the dtype's largest."""
+    big = 2.0**62 * (1 - 2.0**-8)  # bf16-representable, square just below 2^124
+    pool = {"below_2_62": [big],
+            "above_2_62": [2.0**70, 2.0**100],
+            "mixed_max": [big, 2.0**64, 2.0**120, 1.0e-3]}[values]
+    pool = [_bf16_value(v) for v in pool]
+    cfg = _tiny(RAGGED, 4, bucket_size=5000, grad_reduce_in_fp32=grad_fp32, steps=1, max_norm=1.0)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    grads = hc.grads(1)
+    for bi, reps in enumerate(grads):
+        n = reps[0].size
+        idx = np.arange(n)
+        vals = np.array(pool)[idx % len(pool)] * np.where(idx % 2 == 0, 1.0, -1.0)
+        if reps[0].dtype == np.uint16:  # a 16-bit grad buffer
+            kind = torch.bfloat16 if hc.om.buffers[bi].grad_dtype == H.BF16 else torch.float16
+            if kind == torch.float16:  # fp16 grads top out at 65504
+                vals = np.clip(vals, -6e4, 6e4)
+            bits = torch.from_numpy(vals.astype(np.float32)).to(kind).view(torch.int16).numpy().view(np.uint16)
+            for r in reps:
+                r[:] = bits
+        else:
+            for r in reps:
+                r[:] = vals.astype(np.float32)
+    before = H.snapshot(hc)
+    ores = hc.oracle_step(grads, 1)
+    assert not ores["found_inf"] and np.isfinite(ores["sumsq"])
+    found, norm = dc.step(grads, 1)
+    report = []
+    assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
+    assert not found
