@@ -301,3 +301,33 @@ def test_huge_finite_grads_are_finite(grad_fp32, values):
     report = []
     assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
     assert not found
+
+
+@pytest.mark.parametrize("grad_fp32", [False, True])
+def test_subnormal_grads_keep_their_values(grad_fp32):
+    """Subnormal grads (fp32 and bf16 subnormals, and fp16 subnormals that the
+    loss scale divides further) are summed, unscaled and stepped like any
+    value on both sides: no flush to zero.  Zeros of both signs mix in."""
+    pool = [1.0e-40, -3.0e-39, 1.4e-45, -1.0e-30, 0.0, -0.0, 5.9e-8, -6.0e-8]
+    cfg = _tiny(RAGGED, 4, bucket_size=5000, grad_reduce_in_fp32=grad_fp32, steps=1,
+                loss_scale=65536.0, max_norm=0.0)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    grads = hc.grads(1)
+    for bi, reps in enumerate(grads):
+        n = reps[0].size
+        vals = np.array(pool, np.float32)[np.arange(n) % len(pool)]
+        if reps[0].dtype == np.uint16:
+            kind = torch.bfloat16 if hc.om.buffers[bi].grad_dtype == H.BF16 else torch.float16
+            bits = torch.from_numpy(vals).to(kind).view(torch.int16).numpy().view(np.uint16)
+            for r in reps:
+                r[:] = bits
+        else:
+            for r in reps:
+                r[:] = vals
+    before = H.snapshot(hc)
+    ores = hc.oracle_step(grads, 1)
+    assert ores["num_zeros"] > 0 and ores["sumsq"] > 0
+    found, norm = dc.step(grads, 1)
+    report = []
+    assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
