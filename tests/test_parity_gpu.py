@@ -331,3 +331,26 @@ def test_subnormal_grads_keep_their_values(grad_fp32):
     found, norm = dc.step(grads, 1)
     report = []
     assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
+
+
+@pytest.mark.parametrize("hp", [
+    dict(lr=0.0, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1),   # no update at all
+    dict(lr=1e-3, beta1=0.0, beta2=0.0, eps=1e-8, weight_decay=0.0),   # m = g, v = g^2
+    dict(lr=1e-2, beta1=0.5, beta2=0.999, eps=1.0, weight_decay=1.0),  # eps dominates, strong decay
+], ids=["lr0", "beta0", "eps1"])
+def test_degenerate_hyperparameters(hp):
+    """Edge values the hyper-parameter checks accept, against the oracle over
+    three steps from a warm state; with lr = 0 the masters and params stay
+    bit for bit what they were."""
+    cfg = _tiny(RAGGED, 3, bucket_size=5000, steps=3, warm_state=True, grad_sigma=1e-2, hp=hp)
+    _check(cfg)
+    if hp["lr"] == 0.0:
+        hc = H.HostCase(cfg)
+        dc = H.DeviceCase(hc)
+        before = [t.clone() for t in dc.params] + [t.clone() for t in dc.master if t is not None]
+        for t in range(1, 4):
+            found, _ = dc.step(hc.grads(t), t)
+            assert not found
+        after = list(dc.params) + [t for t in dc.master if t is not None]
+        for b, a in zip(before, after):
+            assert torch.equal(b, a)
