@@ -354,3 +354,43 @@ def test_degenerate_hyperparameters(hp):
         after = list(dc.params) + [t for t in dc.master if t is not None]
         for b, a in zip(before, after):
             assert torch.equal(b, a)
+
+
+def test_concurrent_steps_from_two_threads_on_two_streams():
+    """Two independent optimizers stepped at the same time from two host
+    threads, each on its own stream with its own map and workspace: the
+    library's per-thread and per-device host state (launch scratch, side
+    streams, caches) keeps them apart, and each matches its oracle."""
+    import threading
+    cfgs = [_tiny(RAGGED, 4, bucket_size=5000, steps=3, seed=31),
+            dict(W.mini("llama_7b_dp8_rank0"), steps=3)]
+    results = [None, None]
+
+    def run(i):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                hc = H.HostCase(cfgs[i])
+                dc = H.DeviceCase(hc)
+                report, ok = [], True
+                for t_step in range(1, 4):
+                    grads = hc.grads(t_step)
+                    t = hc.t_applied + 1
+                    before = H.snapshot(hc)
+                    ores = hc.oracle_step(grads, t)
+                    found, norm = dc.step(grads, t)
+                    ok &= H.compare_step(hc, dc, ores, found, norm, before, report)
+                    if not ores["found_inf"]:
+                        hc.t_applied += 1
+                s.synchronize()
+            results[i] = (ok, report)
+        except Exception as e:  # reported below, in the main thread
+            results[i] = (False, [repr(e)])
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    for ok, report in results:
+        assert ok, "\n".join(report)
