@@ -17,10 +17,11 @@ Parts:
                   inner AdamW step -> copy main params back to the model
                   param buffer.
 
-Parity unpinned, and not restated here: A7, the dynamic loss scaler's
-backoff, growth and hysteresis policy (host code of the library).  The pages
-fix only a dynamic scale that starts at 2^16; the library's policy is
-checked by hand-worked unit cases, not against this oracle.
+Not restated here: A7, the dynamic loss scaler's backoff, growth and
+hysteresis policy (host code of the library).  The pages fix only a dynamic
+scale that starts at 2^16.  With a hysteresis of 1 the library's policy is
+pinned to torch's GradScaler update routine; above 1 its parity is unpinned
+and hand-worked unit cases check it.
 """
 
 import ctypes

@@ -10,6 +10,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from synth import workloads as W
@@ -234,3 +235,28 @@ def test_bounds_record_needs_the_checked_build():
     with pytest.raises(dopt.DoptError) as e:
         dopt.dopt_debug_bounds_record()
     assert e.value.status == dopt.E_INVALID
+
+
+@pytest.mark.parametrize("growth,backoff,interval,p_inf", [(2.0, 0.5, 1, 0.4), (2.0, 0.5, 3, 0.25),
+                                                           (4.0, 0.25, 2, 0.4), (2.0, 0.125, 1, 0.25)])
+def test_loss_scaler_with_hysteresis_1_equals_torch_gradscaler_update(growth, backoff, interval, p_inf):
+    """With a hysteresis of 1 the dynamic loss scaler reduces to the
+    backoff/growth rule of torch's GradScaler (torch._amp_update_scale_, an
+    independent library routine): back off on every step with an inf, grow
+    after `interval` clean steps in a row.  Same scale and growth counter
+    after every step of a seeded random inf pattern (powers of two: exact in
+    torch's float32 scale and the library's double; the inf rate keeps the
+    scale inside float32's normal range, so the library's min_scale floor,
+    which torch lacks, never acts)."""
+    rng = random.Random(int(growth * 100 + interval))
+    s = dopt.dopt_loss_scaler_init(2.0**16, growth, backoff, interval, 1, min_scale=2.0**-140)
+    t_scale = torch.tensor([2.0**16], dtype=torch.float32)
+    t_track = torch.tensor([0], dtype=torch.int32)
+    for step in range(300):
+        found = rng.random() < p_inf
+        dopt.dopt_loss_scaler_update(s, found)
+        torch._amp_update_scale_(t_scale, t_track, torch.tensor([1.0 if found else 0.0]), growth, backoff,
+                                 interval)
+        assert s.scale == t_scale.item(), step
+        assert s.growth_tracker == t_track.item(), step
+        assert 2.0**-126 <= s.scale < 2.0**127
