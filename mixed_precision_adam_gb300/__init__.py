@@ -12,8 +12,9 @@ import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 # DOPT_LIBRARY may name another in-tree build of the same library (the
-# bounds-checked debug build, lib/libdopt_checked.so)
-LIB_PATH = os.environ.get("DOPT_LIBRARY") or os.path.join(HERE, "lib", "libdopt.so")
+# bounds-checked debug build, libdopt_checked.so): only its file name counts,
+# and the file must sit in this package's lib/ directory
+LIB_PATH = os.path.join(HERE, "lib", os.path.basename(os.environ.get("DOPT_LIBRARY") or "libdopt.so"))
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
