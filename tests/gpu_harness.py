@@ -416,12 +416,13 @@ def state_close(got, want, before):
             np.abs(got.astype(np.float64) - want.astype(np.float64)) <= 1e-6 * scale)
 
 
-def compare_step(hc, dc, ores, found, norm, before, report, compact=True):
+def compare_step(hc, dc, ores, found, norm, before, report, compact=True, ws=None):
     """Compares the device state after a step with the oracle's.  `before`
     holds the oracle's state before the step; compact: the step was fused or
     bucket-staged, so 16-bit grad buffers left their main grads in compact
-    form (decode_main).  Appends findings to report and returns True when
-    every check passes."""
+    form (decode_main); ws: the workspace that holds the step's statistics
+    (the bucket-staged step's own, or by default the fused step's).  Appends
+    findings to report and returns True when every check passes."""
     ok = True
     if hasattr(dc, "check_guards") and not dc.check_guards():
         report.append("a write landed outside a device buffer (guard bytes changed)")
@@ -434,7 +435,7 @@ def compare_step(hc, dc, ores, found, norm, before, report, compact=True):
         if not rel <= 1e-5:
             report.append(f"grad_norm device={norm} oracle={ores['norm']} rel={rel:.3g}")
             ok = False
-    stats = dopt().dopt_read_step_stats(dc.ws)
+    stats = dopt().dopt_read_step_stats(dc.ws if ws is None else ws)
     if stats["num_zeros"] != ores["num_zeros"]:
         report.append(f"num_zeros device={stats['num_zeros']} oracle={ores['num_zeros']}")
         ok = False

@@ -1,8 +1,9 @@
 """Randomized parity: seeded random parameter lists, DP sizes, bucket sizes,
 dtype pairs, replica layouts, rank selections, instances, averaging,
-scale_gradients, loss scales and the grad check, each stepped through the
-C ABI and compared with the CPU oracle element by element (with the canary
-guards of the harness around every device buffer)."""
+scale_gradients, loss scales, remote norm terms and the grad check, each
+stepped through the C ABI (fused, separate or bucket-staged) and compared
+with the CPU oracle element by element (with the canary guards of the
+harness around every device buffer)."""
 
 import random
 
@@ -57,3 +58,44 @@ def test_random_grad_check_matches_oracle(seed):
     cfg["grad_scale"] = 1.0
     ok, report = H.run_check(cfg, [[(i, i, 5.0 * (i + 1)) for i in range(4)], [(1, 0, np.inf)]])
     assert ok, "\n".join(report)
+
+
+@pytest.mark.parametrize("seed", range(32, 48))
+def test_random_paths_and_odd_dp_match_oracle(seed):
+    """Seeded random maps at DP sizes the workloads do not use (5, 6, 7, 12,
+    16, 32: uneven equal splits and the general reduce kernel), with remote
+    norm terms, stepped through one of the three paths at random -- the
+    fused step, the separate entry points, or the bucket-staged step with
+    random bucket groups on two side streams."""
+    cfg = _random_cfg(seed)
+    rng = random.Random(9000 + seed)
+    cfg["dp"] = rng.choice([5, 6, 7, 12, 16, 32])
+    cfg["n_inst"] = rng.choice([1, 1, 2])
+    if cfg["ranks"] != "all":
+        cfg["ranks"] = [rng.randrange(cfg["dp"])]
+    cfg["remote_sumsq"] = rng.choice([0.0, 0.0, 1e-3, 5.0])
+    path = rng.choice(["fused", "separate", "staged"])
+    if path == "separate":
+        cfg["grad_scale"] = 1.0  # scale_gradients is a step option of the fused and staged paths
+    group = rng.choice([1, 2, 5])
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    report, ok = [], True
+    for t_step in range(1, cfg["steps"] + 1):
+        grads = hc.grads(t_step)
+        t = hc.t_applied + 1
+        before = H.snapshot(hc)
+        ores = hc.oracle_step(grads, t)
+        if path == "fused":
+            found, norm = dc.step(grads, t)
+        elif path == "separate":
+            found, norm = dc.step_separate(grads, t)
+        else:
+            found, norm = H.staged_step(dc, [[dc._up(r) for r in g] for g in grads], t, group, streams)
+        ok &= H.compare_step(hc, dc, ores, found, norm, before, report, compact=path != "separate",
+                             ws=dc.bws if path == "staged" else None)
+        if not ores["found_inf"]:
+            hc.t_applied += 1
+    assert ok, f"{cfg['name']}: path={path} dp={cfg['dp']} n_inst={cfg['n_inst']} layout={cfg['layout']} " \
+               f"ranks={cfg['ranks']}\n" + "\n".join(report)
