@@ -260,3 +260,23 @@ def test_loss_scaler_with_hysteresis_1_equals_torch_gradscaler_update(growth, ba
         assert s.scale == t_scale.item(), step
         assert s.growth_tracker == t_track.item(), step
         assert 2.0**-126 <= s.scale < 2.0**127
+
+
+@pytest.mark.parametrize("dp", [2, 8, 64])
+def test_rank_buffer_sizes_equal_the_ledger(dp):
+    """A bf16 model (2-byte params and grads, as the ledger assumes): what one
+    rank holds -- the whole param buffer, its grad buffer (whole in the full
+    layout, its shard in the shard-only layout) and the fp32 master, m and v
+    of its shard -- is exactly the ledger's ZeRO-1 and ZeRO-2 per-card bytes
+    for P = the buffer's size (padding included)."""
+    params = [dict(numel=n, dtype=dopt.BF16) for n in (4096 * 4096, 11008 * 4096, 4096, 32000 * 4096)]
+    m = dopt.dopt_build_shard_map(params, dp, 0, False, False)  # grads in the param dtype
+    assert dopt.dopt_num_buffers(m) == 1
+    info = dopt.dopt_buffer_info_get(m, 0)
+    P, S = info["numel"], info["shard_numel"]
+    assert S * dp == P
+    state = 3 * 4 * S                       # master, exp_avg, exp_avg_sq
+    zero1 = 2 * P + 2 * P + state           # params + whole grad buffer
+    zero2 = 2 * P + 2 * S + state           # params + grad shard
+    assert dopt.dopt_memory_ledger(P, dp, 1)[0] == zero1
+    assert dopt.dopt_memory_ledger(P, dp, 2)[0] == zero2
