@@ -13,7 +13,10 @@
 //                          replica tiles staged in shared memory by bulk copies
 // All three compute the same values in the same order.  With 16-bit grads
 // the statistics pass may keep the reduced grads in the grad dtype instead
-// of the fp32 main grads (K1Params::compact).
+// of the fp32 main grads (K1Params::compact).  Debug builds
+// (DOPT_BOUNDS_CHECK=1) check each tile's ranges against the extents of the
+// replicas, the main grad and the grad-check slots, and skip a tile outside
+// them (DOPT_RANGE_OK); the default build compiles the checks out.
 #pragma once
 
 #include <type_traits>

@@ -4,7 +4,9 @@
 // casts the new master into the bf16/fp16 param buffer at the element's
 // buffer offset (the stand-in for the param all-gather).  An fp32 param
 // buffer is its own master and is stepped in place.  A step the finalize
-// pass marked as skipped writes nothing.
+// pass marked as skipped writes nothing.  Debug builds (DOPT_BOUNDS_CHECK=1)
+// check each tile against the extents of the main grad, master/m/v and the
+// param buffer and skip a tile outside them.
 #include "kernels.cuh"
 
 namespace dopt {
