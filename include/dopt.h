@@ -335,6 +335,22 @@ typedef struct {
    * non-finite grad already skips the step through found_inf.  Costs no
    * extra memory traffic (the replica grads are read once either way). */
   float* grad_amax;
+  /* Optional global norm terms in device memory, for a multi-rank step
+   * whose ranks combine their local statistics on the device (the
+   * all-reduce of get_grad_stats_parallel_group, distrib_optimizer page,
+   * MegatronOptimizer utilities): NULL, or an 8-byte aligned double holding
+   * the sum of squares over every rank of the optimizer instance, and a
+   * 4-byte aligned int32 that is nonzero when any rank found a non-finite
+   * grad -- typically the sum and the max, over the ranks, of what
+   * dopt_step_local_stats wrote.  When d_global_sumsq is set, the finalize
+   * reads both when it runs (in stream order) and uses them in place of its
+   * own partial sums plus remote_sumsq / remote_found_inf; this rank's own
+   * non-finite grads still skip the step.  Both must be set together.  Only
+   * dopt_step_finalize uses them: the fused steps and dopt_step_from_host,
+   * whose finalize follows the reduce inside one call, refuse them
+   * (DOPT_E_INVALID). */
+  const double* d_global_sumsq;
+  const int32_t* d_global_found_inf;
 } dopt_step_args;
 
 /* The main-grad buffers of dopt_step_args are scratch between the reduce
@@ -422,6 +438,15 @@ size_t dopt_workspace_bytes_bucketed(const dopt_shard_map* map, int32_t rank);
 int dopt_step_reduce_buckets(const dopt_step_args* args, int32_t buffer, int32_t bucket_first,
                              int32_t bucket_count);
 int dopt_step_finalize(const dopt_step_args* args, int32_t* d_found_inf, float* d_norm);
+/* Between steps 1 and 2 of the bucket-staged sequence, for multi-rank
+ * steps: writes this rank's local statistics to device memory on
+ * args->stream -- *d_local_sumsq (8-byte aligned) = the fixed-order fp64 sum
+ * of squares of the rank's main grads, *d_local_found_inf (4-byte aligned)
+ * = 1 when one of them is non-finite (or a reduce launch gave up waiting),
+ * else 0 -- and finalizes nothing.  The caller combines them across ranks
+ * on the device and passes the results as args->d_global_sumsq and
+ * args->d_global_found_inf to dopt_step_finalize. */
+int dopt_step_local_stats(const dopt_step_args* args, double* d_local_sumsq, int32_t* d_local_found_inf);
 int dopt_step_update_buckets(const dopt_step_args* args, int32_t buffer, int32_t bucket_first,
                              int32_t bucket_count);
 

@@ -75,7 +75,8 @@ class dopt_step_args(ctypes.Structure):
                 ("max_norm", _D), ("remote_sumsq", _D), ("hp", dopt_adamw_hparams),
                 ("workspace", _P), ("workspace_bytes", _SZ), ("stream", _P),
                 ("stage_events", ctypes.POINTER(_P)), ("grad_scale", _F), ("reserved", _I32),
-                ("d_step", _P), ("d_lr", _P), ("grad_amax", _P)]
+                ("d_step", _P), ("d_lr", _P), ("grad_amax", _P),
+                ("d_global_sumsq", _P), ("d_global_found_inf", _P)]
 
 
 class dopt_step_stats(ctypes.Structure):
@@ -149,6 +150,7 @@ _c = {
                                       ctypes.POINTER(dopt_loss_scaler), _I32),
     "dopt_kernel_launches": _proto("dopt_kernel_launches", ctypes.c_uint64),
     "dopt_debug_starve_copy": _proto("dopt_debug_starve_copy", ctypes.c_int, _I32),
+    "dopt_step_local_stats": _proto("dopt_step_local_stats", ctypes.c_int, ctypes.POINTER(dopt_step_args), _P, _P),
     "dopt_debug_bounds_record": _proto("dopt_debug_bounds_record", ctypes.c_int, ctypes.POINTER(_I64)),
     "dopt_read_step_stats": _proto("dopt_read_step_stats", ctypes.c_int, _P,
                                    ctypes.POINTER(dopt_step_stats), _P),
@@ -374,6 +376,13 @@ class StepArgs:
         self.c.d_step = _ptr(d_step)
         self.c.d_lr = _ptr(d_lr)
 
+    def set_global_stats(self, d_sumsq, d_found_inf):
+        """Global norm terms in device memory for dopt_step_finalize (a
+        device float64 scalar and a device int32 scalar, or None, None)."""
+        self._global = (d_sumsq, d_found_inf)
+        self.c.d_global_sumsq = _ptr(d_sumsq)
+        self.c.d_global_found_inf = _ptr(d_found_inf)
+
     def set_grad_check(self, grad_amax):
         """Turns on the pre-reduction grad check: grad_amax is a device
         float32 array of n_replicas x dopt_total_buckets(map) (or None to
@@ -454,6 +463,12 @@ def dopt_step_reduce_buckets(args, buffer, bucket_first, bucket_count=1):
 
 def dopt_step_finalize(args, d_found_inf=None, d_norm=None):
     _check(_c["dopt_step_finalize"](ctypes.byref(args.c), _ptr(d_found_inf), _ptr(d_norm)))
+
+
+def dopt_step_local_stats(args, d_local_sumsq, d_local_found_inf):
+    """This rank's local sum of squares (device float64) and non-finite flag
+    (device int32) after its bucket-staged reduces, for a device all-reduce."""
+    _check(_c["dopt_step_local_stats"](ctypes.byref(args.c), _ptr(d_local_sumsq), _ptr(d_local_found_inf)))
 
 
 def dopt_step_update_buckets(args, buffer, bucket_first, bucket_count=1):

@@ -345,6 +345,10 @@ FinalizeArgs finalize_args(int n_slots, void* ws, double remote_sumsq, int32_t r
   f.d_found = d_found;
   f.err_flag = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kErrorFlagOffset);
   f.step = K2Step{nullptr, nullptr, 0.0, 0.0, 0.0, 0.0, dev_step_ptr(ws)};
+  if (a) {
+    f.d_global_sumsq = a->d_global_sumsq;
+    f.d_global_found = a->d_global_found_inf;
+  }
   if (a && a->d_step) {
     f.step.d_step = a->d_step;
     f.step.d_lr = a->d_lr;
@@ -538,6 +542,14 @@ int check_step_args(const dopt_step_args* a, bool bucketed, const char* fn) {
     return dopt::fail(DOPT_E_ALIGN, std::string(fn) + ": d_step / d_lr not 8-byte aligned");
   if (a->grad_amax && (reinterpret_cast<uintptr_t>(a->grad_amax) & 3))
     return fail(DOPT_E_ALIGN, std::string(fn) + ": grad_amax not 4-byte aligned");
+  if (!bucketed && a->d_global_sumsq)
+    return fail(DOPT_E_INVALID, std::string(fn) +
+                                    ": d_global_sumsq is for the bucket-staged finalize (dopt_step_finalize)");
+  if (!a->d_global_sumsq != !a->d_global_found_inf)
+    return fail(DOPT_E_INVALID, std::string(fn) + ": d_global_sumsq and d_global_found_inf go together");
+  if ((a->d_global_sumsq && (reinterpret_cast<uintptr_t>(a->d_global_sumsq) & 7)) ||
+      (a->d_global_found_inf && (reinterpret_cast<uintptr_t>(a->d_global_found_inf) & 3)))
+    return fail(DOPT_E_ALIGN, std::string(fn) + ": d_global_sumsq / d_global_found_inf misaligned");
   if (!a->replica_grads || !a->main_grad || !a->master || !a->exp_avg || !a->exp_avg_sq || !a->param_buffer)
     return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": NULL per-buffer array");
   if (!std::isfinite(a->inv_loss_scale) || !(a->remote_sumsq >= 0) || std::isnan(a->max_norm) ||
@@ -801,6 +813,24 @@ int dopt_step_finalize(const dopt_step_args* a, int32_t* d_found_inf, float* d_n
                       nullptr, d_found_inf, (cudaStream_t)a->stream, a);
 }
 
+int dopt_step_local_stats(const dopt_step_args* a, double* d_local_sumsq, int32_t* d_local_found_inf) {
+  Range range("dopt_step_local_stats");
+  const char* fn = "dopt_step_local_stats";
+  int st = check_step_args(a, true, fn);
+  if (st) return st;
+  if (!d_local_sumsq || !d_local_found_inf)
+    return fail(DOPT_E_INVALID, std::string(fn) + ": NULL d_local_sumsq or d_local_found_inf");
+  if ((reinterpret_cast<uintptr_t>(d_local_sumsq) & 7) || (reinterpret_cast<uintptr_t>(d_local_found_inf) & 3))
+    return fail(DOPT_E_ALIGN, std::string(fn) + ": d_local_sumsq / d_local_found_inf misaligned");
+  dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
+  const int n_slots = bucketed_region(m, a->rank, (int32_t)m->buffers.size(), 0) * kMaxGrid;
+  FinalizeArgs f = finalize_args(n_slots, a->workspace, 0.0, 0, a->max_norm, nullptr, nullptr, nullptr, nullptr);
+  f.local_sumsq = d_local_sumsq;
+  f.local_found = d_local_found_inf;
+  k2_finalize<<<1, kFinThreads, 0, (cudaStream_t)a->stream>>>(f);
+  return check_launch("k2_finalize (local statistics) launch");
+}
+
 int dopt_step_update_buckets(const dopt_step_args* a, int32_t buffer, int32_t bucket_first,
                              int32_t bucket_count) {
   Range range("dopt_step_update_buckets");
@@ -909,6 +939,8 @@ int dopt_step_from_host(const dopt_step_args* a, const void* const* const* host_
   const char* fn = "dopt_step_from_host";
   int st = check_step_args(a, true, fn);
   if (st) return st;
+  if (a->d_global_sumsq)
+    return fail(DOPT_E_INVALID, std::string(fn) + ": d_global_sumsq is for the bucket-staged finalize (dopt_step_finalize)");
   dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
   const int32_t nb = (int32_t)m->buffers.size();
   const int32_t n_rep = m->dp * a->n_instances;

@@ -152,6 +152,14 @@ struct FinalizeArgs {
   int32_t* d_found;
   int32_t* err_flag;
   K2Step step;
+  // global terms in device memory (a multi-rank step): when set, they
+  // replace the partial sum plus remote_sumsq / remote_found
+  const double* d_global_sumsq;
+  const int32_t* d_global_found;
+  // local-only pass: when set, the block writes this rank's sum of squares
+  // and non-finite flag here and finalizes nothing
+  double* local_sumsq;
+  int32_t* local_found;
 };
 
 // Debug builds (DOPT_BOUNDS_CHECK=1): the extents, in elements, of the
@@ -300,11 +308,19 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f) {
     }
     __syncthreads();
   }
+  if (f.local_sumsq) {  // local statistics only; the finalize comes later
+    if (threadIdx.x == 0) {
+      *f.local_sumsq = s_sum[0];
+      *f.local_found = (s_bad[0] || __ldcg(f.err_flag) == kErrorMagic) ? 1 : 0;
+    }
+    return;
+  }
   if (threadIdx.x == 0) {
     const int kernel_error = __ldcg(f.err_flag) == kErrorMagic ? 1 : 0;
     *f.err_flag = 0;
-    const double sumsq = s_sum[0] + f.remote_sumsq;
-    const int found = (s_bad[0] || f.remote_found || kernel_error) ? 1 : 0;
+    const double sumsq = f.d_global_sumsq ? __ldcg(f.d_global_sumsq) : s_sum[0] + f.remote_sumsq;
+    const int remote_bad = f.d_global_sumsq ? (__ldcg(f.d_global_found) != 0) : (f.remote_found != 0);
+    const int found = (s_bad[0] || remote_bad || kernel_error) ? 1 : 0;
     const double norm = sqrt(sumsq);
     double coef = 1.0;
     int clip = 0;

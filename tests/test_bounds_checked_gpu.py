@@ -23,7 +23,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CHECKED = os.path.join(ROOT, "mixed_precision_adam_gb300", "lib", "libdopt_checked.so")
 FILES = ["test_parity_gpu.py", "test_random_gpu.py", "test_fullsize_gpu.py", "test_bucket_staged_gpu.py",
          "test_grad_check_gpu.py", "test_graph_gpu.py", "test_from_host_gpu.py", "test_state_model_gpu.py",
-         "test_memory_gpu.py", "test_zz_no_alloc.py"]
+         "test_memory_gpu.py", "test_multirank_device_gpu.py", "test_zz_no_alloc.py"]
 
 
 def test_gpu_suite_under_the_bounds_checked_build():
