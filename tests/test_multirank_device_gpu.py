@@ -125,3 +125,86 @@ def test_two_ranks_combine_statistics_on_the_device():
                     assert ok.all(), (t_step, r, bi, name)
         t_applied += 1
     assert t_applied == CFG["steps"] - 1
+
+
+def test_two_rank_step_captured_in_one_graph():
+    """The whole two-rank step -- both ranks' reduces, local statistics, the
+    device add and max standing in for the all-reduce, both finalizes and
+    updates -- captured in one CUDA graph with device step counters, and
+    replayed with fresh grads each step (one of them with an inf): bit for
+    bit the eager composition's state."""
+    D = H.dopt()
+    hc_all = H.HostCase(dict(CFG, ranks="all", layout="full"))
+
+    def shards(t_step):
+        full = hc_all.grads(t_step)
+        return [[[_shard(hc_all, bi, x, r) for x in reps] for bi, reps in enumerate(full)] for r in (0, 1)]
+
+    def body(ranks, glob, gflag):
+        for rk in ranks:
+            for bi, buf in enumerate(rk.hc.om.buffers):
+                D.dopt_step_reduce_buckets(rk.args, bi, 0, len(buf.buckets))
+            D.dopt_step_local_stats(rk.args, rk.local, rk.flag)
+        torch.add(ranks[0].local, ranks[1].local, out=glob)
+        torch.maximum(ranks[0].flag, ranks[1].flag, out=gflag)
+        for rk in ranks:
+            D.dopt_step_finalize(rk.args)
+            for bi, buf in enumerate(rk.hc.om.buffers):
+                for k in reversed(range(len(buf.buckets))):
+                    D.dopt_step_update_buckets(rk.args, bi, k, 1)
+
+    def setup(ranks, grads, stream):
+        glob = torch.zeros(1, dtype=torch.float64, device="cuda")
+        gflag = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for rk, g in zip(ranks, grads):
+            rk.reps = [[rk.dc._up(x) for x in reps] for reps in g]
+            rk.args = rk.dc.step_args(rk.reps, 1, stream=stream)
+            rk.args.c.workspace, rk.args.c.workspace_bytes = rk.ws.data_ptr(), rk.ws_bytes
+            rk.d_step = torch.zeros(1, dtype=torch.int64, device="cuda")
+            rk.args.set_device_step(rk.d_step)
+            rk.args.set_global_stats(glob, gflag)
+        return glob, gflag
+
+    first = shards(1)
+    warm = [Rank(0), Rank(1)]  # runs every kernel once outside the capture
+    body(warm, *setup(warm, first, torch.cuda.current_stream()))
+    torch.cuda.synchronize()
+
+    graphed = [Rank(0), Rank(1)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        glob, gflag = setup(graphed, first, s)
+        with torch.cuda.graph(graph, stream=s):
+            body(graphed, glob, gflag)
+    torch.cuda.synchronize()
+
+    eager = [Rank(0), Rank(1)]
+    t_applied = 0
+    for t_step in range(1, CFG["steps"] + 1):
+        g = shards(t_step)
+        for rk, gr in zip(graphed, g):
+            for dst_b, src_b in zip(rk.reps, gr):
+                for dst, src in zip(dst_b, src_b):
+                    dst.copy_(rk.dc._up(src))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        t = t_applied + 1
+        for rk, gr in zip(eager, g):
+            rk.reduce(gr, t)
+        eg = eager[0].local + eager[1].local
+        ef = torch.maximum(eager[0].flag, eager[1].flag)
+        found = []
+        for rk in eager:
+            rk.args.set_global_stats(eg, ef)
+            found.append(rk.finish()[0])
+        assert found[0] == found[1] == (t_step == 2)
+        if not found[0]:
+            t_applied += 1
+        for a, b in zip(graphed, eager):
+            assert int(a.d_step.item()) == t_applied
+            for x_arr, y_arr in zip(a.dc.download()[:4], b.dc.download()[:4]):
+                for x, y in zip(x_arr, y_arr):
+                    assert (x is None and y is None) or x.tobytes() == y.tobytes(), t_step
