@@ -208,3 +208,70 @@ def test_two_rank_step_captured_in_one_graph():
             for x_arr, y_arr in zip(a.dc.download()[:4], b.dc.download()[:4]):
                 for x, y in zip(x_arr, y_arr):
                     assert (x is None and y is None) or x.tobytes() == y.tobytes(), t_step
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_maps_every_rank_on_the_device(seed):
+    """Seeded random maps (dtypes, bucket sizes, padding, instances,
+    averaging, loss scales) at DP 2 to 4, every rank stepped on its own shard
+    with the norm statistics combined on the device, against the all-ranks
+    oracle step."""
+    import random as _random
+    import test_random_gpu as R
+    cfg = R._random_cfg(100 + seed)
+    rng = _random.Random(500 + seed)
+    dp = rng.choice([2, 3, 4])
+    cfg.update(dp=dp, layout="shard", ranks=[0], steps=2, grad_scale=1.0, remote_sumsq=0.0, inf_at=None)
+    hc_all = H.HostCase(dict(cfg, ranks="all", layout="full"))
+    D = H.dopt()
+    ranks = []
+    for r in range(dp):
+        hc = H.HostCase(dict(cfg, ranks=[r]))
+        dc = H.DeviceCase(hc)
+        wsb = D.dopt_workspace_bytes_bucketed(hc.pm, r)
+        ranks.append(dict(hc=hc, dc=dc, wsb=wsb, ws=torch.empty(wsb, dtype=torch.uint8, device="cuda"),
+                          local=torch.zeros(1, dtype=torch.float64, device="cuda"),
+                          flag=torch.zeros(1, dtype=torch.int32, device="cuda")))
+    t_applied = 0
+    for t_step in range(1, cfg["steps"] + 1):
+        t = t_applied + 1
+        full = hc_all.grads(t_step)
+        before = H.snapshot(hc_all)
+        ores = hc_all.oracle_step(full, t)
+        for r, rk in enumerate(ranks):
+            reps = [[rk["dc"]._up(_shard(hc_all, bi, x, r)) for x in g] for bi, g in enumerate(full)]
+            rk["args"] = rk["dc"].step_args(reps, t)
+            rk["args"].c.workspace, rk["args"].c.workspace_bytes = rk["ws"].data_ptr(), rk["wsb"]
+            for bi, buf in enumerate(rk["hc"].om.buffers):
+                D.dopt_step_reduce_buckets(rk["args"], bi, 0, len(buf.buckets))
+            D.dopt_step_local_stats(rk["args"], rk["local"], rk["flag"])
+        glob = torch.stack([rk["local"] for rk in ranks]).sum(0)
+        gflag = torch.stack([rk["flag"] for rk in ranks]).amax(0)
+        found = []
+        for rk in ranks:
+            rk["args"].set_global_stats(glob, gflag)
+            d_found = torch.zeros(1, dtype=torch.int32, device="cuda")
+            d_norm = torch.zeros(1, dtype=torch.float32, device="cuda")
+            D.dopt_step_finalize(rk["args"], d_found, d_norm)
+            for bi, buf in enumerate(rk["hc"].om.buffers):
+                D.dopt_step_update_buckets(rk["args"], bi, 0, len(buf.buckets))
+            torch.cuda.synchronize()
+            found.append((bool(d_found.item()), float(d_norm.item())))
+        assert all(f == ores["found_inf"] for f, _ in found), (found, ores["found_inf"])
+        if ores["found_inf"]:
+            continue
+        for _, n in found:
+            assert abs(n - ores["norm"]) <= 1e-5 * ores["norm"], (n, ores["norm"])
+        for r, rk in enumerate(ranks):
+            params, master, exp_avg, exp_avg_sq, _ = rk["dc"].download()
+            for bi, buf in enumerate(hc_all.om.buffers):
+                S = hc_all.om.shard_numel(bi)
+                sl = slice(r * S, (r + 1) * S)
+                mask = hc_all.piece_mask(bi)[sl]
+                st = hc_all.state[bi]
+                for name, got in (("exp_avg", exp_avg[bi]), ("exp_avg_sq", exp_avg_sq[bi]), ("master", master[bi])):
+                    if got is None:
+                        continue
+                    assert H.state_close(got[mask], st[name][sl][mask], before[bi][name][sl][mask]).all(), \
+                        (seed, t_step, r, bi, name)
+        t_applied += 1
