@@ -69,6 +69,10 @@ def parse_args(argv=None):
     p.add_argument("--staged", action="store_true",
                    help="time the bucket-staged step against the fused step, with the grads "
                         "produced bucket by bucket by a stand-in for the backward pass")
+    p.add_argument("--multirank", action="store_true",
+                   help="time two ranks of the workload's instance on this GPU, their norm "
+                        "statistics combined through the host, on the device, or on the device "
+                        "inside one CUDA graph")
     return p.parse_args(argv)
 
 
@@ -877,6 +881,99 @@ def run_staged(args):
     return 0
 
 
+def run_multirank(args):
+    """Ranks 0 and 1 of a shard-layout workload's instance, one after the other
+    on this GPU, each through the bucket-staged entry points, their norm
+    statistics combined three ways: read to the host and passed back as
+    remote terms (a host round trip between the passes), combined on the
+    device (dopt_step_local_stats, a device add and max, d_global_*), and the
+    device form captured in one CUDA graph with device step counters.  The
+    two ranks' sum stands in for the instance's all-reduce (timing only)."""
+    import torch
+    import mixed_precision_adam_gb300 as D
+    cfg = workload_config(args.workload, args.layers)
+    if cfg["layout"] != "shard":
+        raise SystemExit("--multirank takes a shard-layout workload")
+    ranks = []
+    for r in (0, 1):
+        wl = Workload(dict(cfg, ranks=[r]))
+        wsb = D.dopt_workspace_bytes_bucketed(wl.pm, r)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        a = wl.args()
+        a.c.workspace, a.c.workspace_bytes = ws.data_ptr(), wsb
+        ranks.append(dict(wl=wl, ws=ws, args=a, local=torch.zeros(1, dtype=torch.float64, device="cuda"),
+                          flag=torch.zeros(1, dtype=torch.int32, device="cuda")))
+    nbk = [[D.dopt_buffer_info_get(rk["wl"].pm, b)["n_buckets"] for b in range(D.dopt_num_buffers(rk["wl"].pm))]
+           for rk in ranks]
+    glob = torch.zeros(1, dtype=torch.float64, device="cuda")
+    gflag = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def reduce_all():
+        for rk, nb in zip(ranks, nbk):
+            for b, n in enumerate(nb):
+                D.dopt_step_reduce_buckets(rk["args"], b, 0, n)
+            D.dopt_step_local_stats(rk["args"], rk["local"], rk["flag"])
+
+    def update_all():
+        for rk, nb in zip(ranks, nbk):
+            D.dopt_step_finalize(rk["args"])
+            for b, n in enumerate(nb):
+                D.dopt_step_update_buckets(rk["args"], b, 0, n)
+
+    def host_step():
+        reduce_all()
+        loc = [float(rk["local"].item()) for rk in ranks]  # the host round trip
+        bad = [int(rk["flag"].item()) for rk in ranks]
+        for i, rk in enumerate(ranks):
+            rk["args"].set_global_stats(None, None)
+            rk["args"].c.remote_sumsq, rk["args"].c.remote_found_inf = loc[1 - i], bad[1 - i]
+        update_all()
+
+    def device_step():
+        reduce_all()
+        torch.add(ranks[0]["local"], ranks[1]["local"], out=glob)
+        torch.maximum(ranks[0]["flag"], ranks[1]["flag"], out=gflag)
+        for rk in ranks:
+            rk["args"].c.remote_sumsq, rk["args"].c.remote_found_inf = 0.0, 0
+            rk["args"].set_global_stats(glob, gflag)
+        update_all()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    t_host = timed(host_step)
+    t_dev = timed(device_step)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for rk in ranks:
+            rk["d_step"] = torch.zeros(1, dtype=torch.int64, device="cuda")
+            rk["args"].set_device_step(rk["d_step"])
+            rk["args"].set_stream(s)
+        with torch.cuda.graph(graph, stream=s):
+            device_step()
+    torch.cuda.synchronize()
+    t_graph = timed(graph.replay)
+    line = {"metric": "two ranks' bucket-staged steps: norm statistics combined through the host vs on the "
+                      "device vs on the device in one CUDA graph (ms per step of both ranks)",
+            "workload": describe(cfg, ranks[0]["wl"].elements) + "; ranks 0 and 1, one after the other",
+            "steps": args.steps, "warmup": args.warmup, "host_combined_ms": t_host,
+            "device_combined_ms": t_dev, "device_graph_ms": t_graph,
+            "elements_per_step": ranks[0]["wl"].elements + ranks[1]["wl"].elements}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_graph(args):
     """The fused step three ways: dopt_step calls (each waits for found_inf),
     dopt_step_async calls back to back, and one CUDA-graph replay per step
@@ -929,6 +1026,8 @@ def main(argv=None):
         return run_reference(args)
     if args.staged:
         return run_staged(args)
+    if args.multirank:
+        return run_multirank(args)
     if args.graph:
         return run_graph(args)
     return run_ours(args)

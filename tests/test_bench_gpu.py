@@ -56,3 +56,9 @@ def test_bucket_staged_line():
     d = _bench("--staged", "--layers", "2", "--steps", "5", "--warmup", "3")
     assert d["buckets"] > 1
     assert d["produce_then_fused_ms"] > 0 and d["bucket_staged_overlapped_ms"] > 0
+
+
+def test_multirank_line():
+    d = _bench("--multirank", "--layers", "2", "--steps", "5", "--warmup", "3")
+    for key in ("host_combined_ms", "device_combined_ms", "device_graph_ms"):
+        assert d[key] > 0, key
