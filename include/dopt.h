@@ -433,6 +433,9 @@ int dopt_step_async(const dopt_step_args* args, int32_t* d_found_inf, float* d_n
  * The workspace must hold dopt_workspace_bytes_bucketed(map, rank) bytes (one
  * partial-sum region per bucket); args->stage_events is not used.  A bucket
  * left out of step 1 leaves stale partials behind, and the norm is wrong.
+ * dopt_step_reduce_buckets reduces a group of buckets in as few launches as
+ * the kernels' run tables allow (one, for groups of up to 960 runs); with
+ * d_step set it issues only launches and memsets, like the fused step.
  */
 size_t dopt_workspace_bytes_bucketed(const dopt_shard_map* map, int32_t rank);
 int dopt_step_reduce_buckets(const dopt_step_args* args, int32_t buffer, int32_t bucket_first,

@@ -796,8 +796,22 @@ int dopt_step_reduce_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
   cudaStream_t s = (cudaStream_t)a->stream;
   if ((st = clear_amax(a, bucket_number(m, buffer, bucket_first), bucket_count, s))) return st;
   const K1Job j = step_job(a, buffer);
+  // the group's runs in as few launches as the run tables allow; their
+  // partials fill the group's first regions, and the group's other regions
+  // are zeroed so that no partial of an earlier step is left in them
+  std::vector<Run> runs;
+  int regions = 0;
   for (int32_t k = bucket_first; k < bucket_first + bucket_count; ++k) {
-    if ((st = run_k1_runs(by[k], bucketed_region(m, a->rank, buffer, k), j, s))) return st;
+    runs.insert(runs.end(), by[k].begin(), by[k].end());
+    regions += (int)chunks_of(by[k]).size();
+  }
+  const int first = bucketed_region(m, a->rank, buffer, bucket_first);
+  if ((st = run_k1_runs(runs, first, j, s))) return st;
+  const int used = (int)chunks_of(runs).size();
+  if (used < regions) {
+    cudaError_t e = cudaMemsetAsync(region_ptr(a->workspace, first + used), 0,
+                                    (size_t)(regions - used) * kMaxGrid * sizeof(Partial), s);
+    if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
   }
   return DOPT_OK;
 }
