@@ -278,24 +278,21 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f) {
   int b = 0;
   long long z = 0;
   int i = threadIdx.x;
-  const double* sum_p = reinterpret_cast<const double*>(f.parts);
-  const int2* flag_p = reinterpret_cast<const int2*>(f.parts);
-  for (; i + 3 * NT < f.n_slots; i += 4 * NT) {
+  // one 16-byte load per slot (the fp64 sum, then the flag and zero count
+  // as the low and high words of the second half), eight slots in flight
+  const double2* slot = reinterpret_cast<const double2*>(f.parts);
+  auto take = [&](int j, int q) {
+    const double2 d = __ldcg(slot + j);
+    const long long fz = __double_as_longlong(d.y);
+    v[q] += d.x;
+    b |= (int)(fz & 0xFFFFFFFFll);
+    z += (int)(fz >> 32);
+  };
+  for (; i + 7 * NT < f.n_slots; i += 8 * NT) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = i + q * NT;
-      v[q] += __ldcg(sum_p + 2 * j);
-      const int2 fz = __ldcg(flag_p + 2 * j + 1);
-      b |= fz.x;
-      z += fz.y;
-    }
+    for (int q = 0; q < 8; ++q) take(i + q * NT, q & 3);
   }
-  for (; i < f.n_slots; i += NT) {
-    v[0] += __ldcg(sum_p + 2 * i);
-    const int2 fz = __ldcg(flag_p + 2 * i + 1);
-    b |= fz.x;
-    z += fz.y;
-  }
+  for (; i < f.n_slots; i += NT) take(i, 0);
   s_sum[threadIdx.x] = (v[0] + v[1]) + (v[2] + v[3]);
   s_bad[threadIdx.x] = b;
   s_zero[threadIdx.x] = z;
