@@ -502,7 +502,14 @@ int dopt_step_from_host(const dopt_step_args* args, const void* const* const* ho
  *    and output (replica grads, main grad, master, m, v, param buffers).
  *  - The first call on a device looks up the device address of the scratch
  *    array (with that device current); make that first call before any
- *    stream capture.  Later calls on the device reuse the address.
+ *    stream capture.  Later calls on the device reuse the address.  The
+ *    address is kept for the life of the process: after cudaDeviceReset
+ *    the library's module is loaded afresh, and this entry point must not
+ *    be called again in that process.
+ *  - The first call on each host thread and device also creates the side
+ *    stream and event that dopt_step reads its results back on (no device
+ *    memory).  A caller that allows no resource creation after start-up
+ *    makes one call per thread and device during start-up.
  *  - Returns DOPT_E_SIZE when the map and rank selection need more scratch
  *    than the array holds (dopt_workspace_bytes(map, rank) >
  *    DOPT_NOALLOC_SCRATCH_BYTES): no work is enqueued then.
@@ -512,8 +519,12 @@ int dopt_step_from_host(const dopt_step_args* args, const void* const* const* ho
  *    reads).  Calls that overlap on the GPU -- on two streams, or from two
  *    threads without ordering -- race on the array and give wrong results:
  *    order them.
- * Waits for args->stream and returns found_inf and the grad norm like
- * dopt_step.
+ * Returns found_inf and the grad norm like dopt_step, and like dopt_step it
+ * waits only until those two are known: the AdamW pass may still be running
+ * on args->stream when it returns, and it still reads the step scalars in
+ * the shared array.  Queue the next call of this entry point behind
+ * args->stream -- on the same stream, or after an event recorded on it or a
+ * synchronize -- never on another stream that is not ordered after it.
  */
 #define DOPT_NOALLOC_SCRATCH_BYTES (1u << 20)
 int dopt_step_noalloc(const dopt_step_args* args, int32_t* found_inf_out, float* grad_norm_out);

@@ -16,12 +16,13 @@ Parts:
                   grad, unscale, inf/NaN) -> skip on inf -> clip_grad_norm ->
                   inner AdamW step -> copy main params back to the model
                   param buffer.
-
-Not restated here: A7, the dynamic loss scaler's backoff, growth and
-hysteresis policy (host code of the library).  The pages fix only a dynamic
-scale that starts at 2^16.  With a hysteresis of 1 the library's policy is
-pinned to torch's GradScaler update routine; above 1 its parity is unpinned
-and hand-worked unit cases check it.
+  loss_scale.py -- step A7, the fp16 dynamic loss scale (start at 2^16 from
+                  the DeepSpeed setting initial_scale_power 16; backoff on
+                  an overflow after the hysteresis strikes, growth after a
+                  run of clean steps), plain Python.  With a hysteresis of 1
+                  it is pinned to torch's GradScaler update routine and to
+                  hand-worked sequences; above 1 only hand-worked sequences
+                  pin it.
 """
 
 import ctypes
@@ -29,6 +30,7 @@ import ctypes
 import numpy as np
 
 from . import build as _build
+from .loss_scale import LossScale, initial_scale  # noqa: F401
 from .shard_map import BF16, F16, F32, Range, ShardMap, pad_up  # noqa: F401
 
 _lib = None
@@ -262,6 +264,7 @@ def master_close(got, want, before, scale_floor, ulps=4):
     return np.abs(got.astype(np.float64) - want.astype(np.float64)) <= tol
 
 
-__all__ = ["ShardMap", "Range", "pad_up", "F32", "BF16", "F16", "step", "lib",
+__all__ = ["ShardMap", "Range", "pad_up", "F32", "BF16", "F16", "step", "lib", "LossScale",
+           "initial_scale",
            "reduce_prepare", "stream_sumsq", "round_bf16", "round_f16",
            "float_ulp_diff", "master_close"]

@@ -16,7 +16,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-C, PY, SM = "oracle/oracle.c", "oracle/__init__.py", "oracle/shard_map.py"
+C, PY, SM, LS = "oracle/oracle.c", "oracle/__init__.py", "oracle/shard_map.py", "oracle/loss_scale.py"
 
 # (file, text in the oracle, its replacement, what the mistake is)
 MUTANTS = [
@@ -94,6 +94,21 @@ MUTANTS = [
      "shard-only replicas read at the bucket-local index"),
     (PY, '                local = slot * S + v["shard_offset"]', '                local = v["shard_offset"]',
      "rank slot ignored"),
+    # A7 loss scale
+    (LS, "    return math.ldexp(1.0, int(initial_scale_power))", "    return math.ldexp(1.0, int(initial_scale_power) - 1)",
+     "loss scale starts at 2^15"),
+    (LS, "                self.scale = max(self.scale * self.backoff_factor, self.min_scale)",
+     "                self.scale = max(self.scale, self.min_scale)", "no backoff on an overflow"),
+    (LS, "                self.scale = max(self.scale * self.backoff_factor, self.min_scale)",
+     "                self.scale = self.scale * self.backoff_factor", "no min_scale floor"),
+    (LS, "            if self.strikes_left <= 0:", "            if self.strikes_left < 0:", "one strike too many"),
+    (LS, "            self.clean_steps = 0\n            self.strikes_left -= 1",
+     "            self.strikes_left -= 1", "an overflow does not restart the clean run"),
+    (LS, "                self.strikes_left = self.hysteresis\n", "", "growth does not restore the strikes"),
+    (LS, "            if self.clean_steps == self.growth_interval:", "            if self.clean_steps > self.growth_interval:",
+     "grows one step late"),
+    (LS, "                self.scale = self.scale * self.growth_factor", "                self.scale = self.scale * 2.0",
+     "growth factor ignored"),
     # A1 shard map
     (SM, "    for pid in reversed(buf.params):", "    for pid in buf.params:", "forward walk"),
     (SM, "        start = pad_up(cursor, 64)", "        start = cursor", "no 64-element start pad"),

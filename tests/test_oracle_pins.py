@@ -736,3 +736,64 @@ def test_generator_truncations_are_exact_16_bit_values():
     x = synth.normal(50000, k, 0, 0.02)
     assert (np.abs(v16) <= np.abs(x)).all() and (np.abs(v) <= np.abs(x)).all()
     assert abs(float(x.std()) - 0.02) < 5e-4
+
+
+# --------------------------------------------------------------------------
+# A7 the fp16 dynamic loss scale
+
+
+def test_loss_scale_starts_at_the_deepspeed_initial_scale_power():
+    g = _golden("deepspeed_fp16_config.json")
+    assert g["fp16"]["loss_scale"] == 0  # 0 selects the dynamic scale
+    assert oracle.initial_scale(g["fp16"]["initial_scale_power"]) == g["expected_initial_scale"]
+    assert oracle.LossScale().scale == g["expected_initial_scale"]
+    # a clean step of a fresh scale changes nothing until the growth interval
+    s = oracle.LossScale()
+    assert s.update(False) == g["expected_initial_scale"]
+
+
+@pytest.mark.parametrize("growth,backoff,interval,p_inf", [(2.0, 0.5, 1, 0.4), (2.0, 0.5, 3, 0.25),
+                                                           (2.0, 0.5, 1000, 0.002), (4.0, 0.25, 2, 0.4)])
+def test_loss_scale_hysteresis_1_equals_torch_gradscaler_update(growth, backoff, interval, p_inf):
+    """With one hysteresis strike the dynamic scale follows the backoff and
+    growth rule of torch's GradScaler (torch._amp_update_scale_, an
+    independent library routine) after every step of a seeded inf pattern.
+    Powers of two keep both exact; min_scale is set below every scale the
+    pattern reaches, since torch has no floor."""
+    rng = random.Random(int(growth * 1000 + interval))
+    s = oracle.LossScale(2.0**16, growth, backoff, interval, hysteresis=1, min_scale=2.0**-140)
+    t_scale = torch.tensor([2.0**16], dtype=torch.float32)
+    t_track = torch.tensor([0], dtype=torch.int32)
+    steps = 3000 if interval == 1000 else 300
+    for step in range(steps):
+        found = rng.random() < p_inf
+        s.update(found)
+        torch._amp_update_scale_(t_scale, t_track, torch.tensor([1.0 if found else 0.0]), growth,
+                                 backoff, interval)
+        assert s.scale == t_scale.item(), step
+        assert 2.0**-126 <= s.scale < 2.0**127
+
+
+def test_loss_scale_hand_worked_hysteresis_growth_and_floor():
+    """Sequences worked by hand from the rule: strikes absorb overflows,
+    the last strike backs off, growth restores the strikes, an overflow
+    restarts the run of clean steps, and the scale never drops below
+    min_scale."""
+    s = oracle.LossScale(65536.0, 2.0, 0.5, growth_interval=3, hysteresis=2)
+    seq = [(True, 65536.0),    # first strike absorbed
+           (True, 32768.0),    # second strike: halve
+           (True, 16384.0),    # no strike left: halve again
+           (False, 16384.0), (False, 16384.0),
+           (True, 8192.0),     # breaks the clean run; still no strike left
+           (False, 8192.0), (False, 8192.0),
+           (False, 16384.0),   # three clean in a row: grow, strikes back to 2
+           (True, 16384.0),    # absorbed again
+           (False, 16384.0), (False, 16384.0), (False, 32768.0)]
+    for i, (found, want) in enumerate(seq):
+        assert s.update(found) == want, i
+    f = oracle.LossScale(4.0, 2.0, 0.5, growth_interval=1000, hysteresis=1, min_scale=1.0)
+    assert [f.update(True) for _ in range(4)] == [2.0, 1.0, 1.0, 1.0]
+    g = oracle.LossScale(1.0, 2.0, 0.5, growth_interval=1, hysteresis=3, min_scale=1.0)
+    assert [g.update(False) for _ in range(3)] == [2.0, 4.0, 8.0]
+    assert [g.update(True) for _ in range(3)] == [8.0, 8.0, 4.0]
+    assert oracle.LossScale(3.0).inv_scale() == float(np.float32(1.0 / 3.0))

@@ -168,32 +168,42 @@ def test_scale_gradients_and_zero_count(grad_fp32):
 
 
 def test_dynamic_loss_scaler_through_a_skipped_step():
-    """fp16 with the library's dynamic loss scaler driving inv_loss_scale:
-    an overflow at step 2 skips the step and halves the scale; the next
-    steps run with the new scale (both sides follow the same trajectory)."""
+    """fp16 with a dynamic loss scale through an overflow: the oracle keeps
+    its own scale (oracle.LossScale) and steps with it; the device steps
+    with the library's scaler (dopt_loss_scaler_*), each side's unscale
+    factor from its own scale.  An overflow at step 2 skips the step and
+    halves the scale; two clean steps later it grows back.  The two scale
+    trajectories must be equal, and so must every step's results."""
+    import oracle
     D = H.dopt()
     cfg = W.mini("llama_1p3b_fp16_dp8")
-    cfg = dict(cfg, inf_at=dict(step=2, replica=3, buffer_frac=0.3), steps=4)
+    cfg = dict(cfg, inf_at=dict(step=2, replica=3, buffer_frac=0.3), steps=5)
     hc = H.HostCase(cfg)
     dc = H.DeviceCase(hc)
+    o_scale = oracle.LossScale(oracle.initial_scale(16), 2.0, 0.5, growth_interval=2, hysteresis=1)
     scaler = D.dopt_loss_scaler_init(65536.0, 2.0, 0.5, growth_interval=2, hysteresis=1)
     report = []
-    scales = []
-    for step in range(1, 5):
-        hc.cfg["loss_scale"] = scaler.scale
-        scales.append(scaler.scale)
+    o_traj, d_traj = [], []
+    for step in range(1, 6):
+        o_traj.append(o_scale.scale)
+        d_traj.append(scaler.scale)
         grads = hc.grads(step)
         t = hc.t_applied + 1
         before = H.snapshot(hc)
+        hc.cfg["loss_scale"] = o_scale.scale  # the oracle's unscale factor
         ores = hc.oracle_step(grads, t)
+        hc.cfg["loss_scale"] = scaler.scale  # the device's
         found, norm = dc.step(grads, t)
+        hc.cfg["loss_scale"] = o_scale.scale  # compare_step decodes with the oracle's
         assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
         assert found == (step == 2)
         if not found:
             hc.t_applied += 1
+        o_scale.update(ores["found_inf"])
         D.dopt_loss_scaler_update(scaler, found)
-    assert scales == [65536.0, 65536.0, 32768.0, 32768.0]
-    assert scaler.scale == 65536.0  # two clean steps after the backoff: growth
+    assert d_traj == o_traj
+    assert o_traj == [65536.0, 65536.0, 32768.0, 32768.0, 65536.0]
+    assert scaler.scale == o_scale.scale == 65536.0
 
 
 def test_bounded_wait_runs_out_and_reports():
