@@ -63,6 +63,9 @@ def lib():
         L.or_stream_sumsq.argtypes = [ctypes.POINTER(ctypes.c_uint64), I32, I32, I32, I32, F,
                                       ctypes.c_uint64, I64, F, F, ctypes.POINTER(I64)]
         L.or_stream_sumsq.restype = D
+        L.or_stream_reduce_prepare_run.argtypes = [ctypes.POINTER(ctypes.c_uint64), I32, I32, I32, I32, F,
+                                                   ctypes.c_uint64, I64, F, F, P]
+        L.or_stream_reduce_prepare_run.restype = I64
         L.or_round_bf16.argtypes = [F]
         L.or_round_bf16.restype = ctypes.c_uint16
         L.or_round_f16.argtypes = [F]
@@ -242,6 +245,26 @@ def stream_sumsq(keys, gdt, factor, index0, length, inv_scale=1.0, n_inst=1, ave
     return s, bad.value
 
 
+def stream_reduce_prepare(keys, gdt, factor, index0, length, out=None, inv_scale=1.0, n_inst=1,
+                          average=False, grad_scale=1.0):
+    """A2 + A3 over a run whose replica gradients are drawn from the seeded
+    generator (keys: one generator key per replica), keeping the main grads.
+    Writes them to `out` (a float32 array of `length`, allocated when None)
+    and returns (out, count of non-finite main grads)."""
+    L = lib()
+    n = len(keys)
+    karr = (ctypes.c_uint64 * n)(*keys)
+    if out is None:
+        out = np.empty(length, dtype=np.float32)
+    assert out.dtype == np.float32 and out.flags.c_contiguous and out.size >= length
+    bad = L.or_stream_reduce_prepare_run(karr, n, n_inst, gdt, int(average), ctypes.c_float(factor),
+                                         index0, length, ctypes.c_float(grad_scale),
+                                         ctypes.c_float(inv_scale), _ptr(out))
+    if bad < 0:
+        raise ValueError("invalid replica / instance counts")
+    return out, bad
+
+
 def float_ulp_diff(a, b):
     """Distance in units of last place between float32 arrays (same sign)."""
     ai = np.asarray(a, dtype=np.float32).view(np.int32).astype(np.int64)
@@ -266,5 +289,5 @@ def master_close(got, want, before, scale_floor, ulps=4):
 
 __all__ = ["ShardMap", "Range", "pad_up", "F32", "BF16", "F16", "step", "lib", "LossScale",
            "initial_scale",
-           "reduce_prepare", "stream_sumsq", "round_bf16", "round_f16",
+           "reduce_prepare", "stream_sumsq", "stream_reduce_prepare", "round_bf16", "round_f16",
            "float_ulp_diff", "master_close"]

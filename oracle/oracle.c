@@ -344,3 +344,33 @@ double or_stream_sumsq(const uint64_t* keys, int32_t n_rep, int32_t n_inst,
   *n_bad = bad;
   return s;
 }
+
+/* The same streaming draw as or_stream_sumsq, keeping the main grads: A2 +
+ * A2' + A3 over a run whose replica k is generator stream keys[k] at
+ * indices index0 .. index0 + len - 1.  main_out[j] receives the element's
+ * main grad; returns the count of non-finite ones (-1 on bad counts).  Lets
+ * a full-size check recompute every element of a window of whole buckets
+ * without holding the replicas in host RAM. */
+int64_t or_stream_reduce_prepare_run(const uint64_t* keys, int32_t n_rep, int32_t n_inst,
+                                     int32_t gdt, int32_t average, float factor,
+                                     uint64_t index0, int64_t len, float grad_scale,
+                                     float inv_scale, float* main_out) {
+  float g[256];
+  int64_t bad = 0;
+  if (n_rep <= 0 || n_rep > 256 || n_inst <= 0 || n_rep % n_inst) return -1;
+  for (int64_t j = 0; j < len; ++j) {
+    for (int32_t k = 0; k < n_rep; ++k) {
+      float x = synth_normal(keys[k], index0 + (uint64_t)j, factor);
+      if (gdt == OR_BF16) g[k] = or_bf16_to_f32(synth_bf16_trunc_bits(x));
+      else if (gdt == OR_F16) g[k] = or_f16_to_f32(synth_f16_trunc_bits(x));
+      else g[k] = x;
+    }
+    {
+      float mg = or_scale_gradients(or_reduce_element(g, n_rep, n_inst, gdt, average),
+                                    grad_scale, gdt) * inv_scale;
+      main_out[j] = mg;
+      if (!or_is_finite(mg)) ++bad;
+    }
+  }
+  return bad;
+}

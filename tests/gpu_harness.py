@@ -720,3 +720,173 @@ class FullCase:
                            else g["param"])
             got[bi] = g
         return got
+
+    # ---- element-wise parity on a window of whole buckets ------------------
+
+    def window_buckets(self, min_elems=64 << 20):
+        """Whole buckets to compare element by element: every bucket of every
+        buffer after the first (the small fp32 norm-weight buffers), and of
+        buffer 0 its first, middle and last bucket, then more buckets taken
+        alternately from the front and the back until the window holds at
+        least min_elems of the selected ranks' buffer elements (or all of
+        them).  Returns sorted (buffer, bucket) pairs."""
+        om = self.om
+        per = len(self.ranks)
+        out = set()
+        size = 0
+
+        def take(bi, b):
+            nonlocal size
+            if (bi, b) not in out:
+                out.add((bi, b))
+                size += per * (om.buffers[bi].buckets[b].numel // om.dp)
+
+        for bi in range(1, len(om.buffers)):
+            for b in range(len(om.buffers[bi].buckets)):
+                take(bi, b)
+        nbk = len(om.buffers[0].buckets)
+        for b in (0, nbk // 2, nbk - 1):
+            take(0, b)
+        lo, hi = 1, nbk - 2
+        while size < min_elems and lo <= hi:
+            take(0, lo)
+            if size < min_elems:
+                take(0, hi)
+            lo, hi = lo + 1, hi - 1
+        return sorted(out)
+
+    def window_pieces(self, buckets):
+        """Param pieces of the selected ranks inside the given buckets, per
+        buffer: {bi: [(param id, flat-shard offset, buffer offset, length,
+        offset in the window arrays)]}."""
+        sel = {}
+        for bi, b in buckets:
+            sel.setdefault(bi, set()).add(b)
+        out = {}
+        for bi, bs in sorted(sel.items()):
+            S = self.om.shard_numel(bi)
+            lst, off = [], 0
+            for slot, r in enumerate(self.ranks):
+                for pid, b, v in self.om.rank_pieces(bi, r):
+                    if b in bs:
+                        n = v["gbuf_local"].size
+                        lst.append((pid, slot * S + v["shard_offset"], v["gbuf_world"].start, n, off))
+                        off += n
+            out[bi] = lst
+        return out
+
+    def window_initial_state(self, pieces):
+        """The oracle's starting state of the window (master from the
+        generator, m = v = 0), per buffer: float32 arrays master, exp_avg,
+        exp_avg_sq (for an fp32 buffer the master is the param itself)."""
+        cfg = self.cfg
+        st = {}
+        for bi, lst in pieces.items():
+            n = lst[-1][4] + lst[-1][3] if lst else 0
+            pdt = self.om.buffers[bi].param_dtype
+            kind = synth.OUT_F32 if pdt == F32 else VALUE_KIND[pdt]
+            master = np.empty(n, np.float32)
+            for pid, lo, w, k, off in lst:
+                master[off:off + k] = synth.normal(k, self.pkey, w, cfg["param_sigma"], kind)
+            st[bi] = {"master": master, "exp_avg": np.zeros(n, np.float32),
+                      "exp_avg_sq": np.zeros(n, np.float32)}
+        return st
+
+    def window_device(self, pieces):
+        """The device's window: per buffer main (fp32, decoded from the
+        compact form for 16-bit grads), master, exp_avg, exp_avg_sq and param
+        (16-bit bits, or fp32) arrays in window order."""
+        torch = self.torch
+        inv = np.float32(1.0 / self.cfg["loss_scale"])
+        got = {}
+        for bi, lst in pieces.items():
+            buf = self.om.buffers[bi]
+            n = lst[-1][4] + lst[-1][3] if lst else 0
+            g = {k: np.empty(n, np.float32) for k in ("main", "master", "exp_avg", "exp_avg_sq")}
+            g["param"] = np.empty(n, np.uint16 if buf.param_dtype != F32 else np.float32)
+            for pid, lo, w, k, off in lst:
+                if buf.grad_dtype == F32:
+                    g["main"][off:off + k] = self.main[bi][lo:lo + k].cpu().numpy()
+                else:
+                    raw = self.main[bi].view(torch.int16)[lo:lo + k].cpu().numpy()
+                    g["main"][off:off + k] = decode_main(raw, buf.grad_dtype, inv, k)
+                g["exp_avg"][off:off + k] = self.m[bi][lo:lo + k].cpu().numpy()
+                g["exp_avg_sq"][off:off + k] = self.v[bi][lo:lo + k].cpu().numpy()
+                p = self.params[bi][w:w + k].cpu().numpy()
+                g["param"][off:off + k] = p.view(np.uint16) if p.dtype == np.int16 else p
+                if self.master[bi] is not None:
+                    g["master"][off:off + k] = self.master[bi][lo:lo + k].cpu().numpy()
+                else:
+                    g["master"][off:off + k] = g["param"][off:off + k]
+            got[bi] = g
+        return got
+
+    def window_oracle_step(self, pieces, st, t_step, t, coef, clip, chunk=1 << 20):
+        """Advances the window's oracle state by one applied step (t None:
+        only the main grads).  The main grads of every element are redrawn
+        from the generator (oracle.stream_reduce_prepare); AdamW and the
+        write-back run per param piece (or_adamw_run), in chunks on a thread
+        pool (the C oracle releases the GIL).  Returns per buffer the main
+        grads and the expected params (16-bit bits, or fp32)."""
+        import os
+        from concurrent.futures import ThreadPoolExecutor
+        cfg = self.cfg
+        L = oracle.lib()
+        h = oracle.Hparams(**cfg["hp"])
+        keys = [synth.key(self.seed, synth.STREAM_GRAD, t_step, k) for k in range(self.n_rep)]
+        fac = synth.factor(cfg["grad_sigma"])
+        inv = float(np.float32(1.0 / cfg["loss_scale"]))
+        res, jobs = {}, []
+        for bi, lst in pieces.items():
+            buf = self.om.buffers[bi]
+            n = st[bi]["master"].size
+            main = np.empty(n, np.float32)
+            param = np.empty(n, np.uint16) if buf.param_dtype != F32 else st[bi]["master"]
+            res[bi] = {"main": main, "param": param}
+            for pid, lo, w, k, off in lst:
+                wd = float(cfg["params"][pid].get("wd_mult", 1.0))
+                for o in range(0, k, chunk):
+                    jobs.append((bi, w + o, off + o, min(chunk, k - o), wd))
+
+        def run(j):
+            bi, w, a, k, wd = j
+            buf = self.om.buffers[bi]
+            main = res[bi]["main"][a:a + k]
+            _, bad = oracle.stream_reduce_prepare(keys, buf.grad_dtype, fac, w, k, out=main,
+                                                  inv_scale=inv, n_inst=cfg["n_inst"],
+                                                  average=cfg["average"])
+            if t is None:
+                return bad
+            s = st[bi]
+            out = None if buf.param_dtype == F32 else res[bi]["param"][a:a + k].ctypes.data
+            L.or_adamw_run(main.ctypes.data, k, coef, int(clip), s["master"][a:a + k].ctypes.data,
+                           s["exp_avg"][a:a + k].ctypes.data, s["exp_avg_sq"][a:a + k].ctypes.data,
+                           oracle.ctypes_byref(h), wd, t, out, buf.param_dtype)
+            return bad
+        with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+            bad = sum(ex.map(run, jobs))
+        return res, bad
+
+
+def window_compare(got, want, prev, chunk=1 << 22):
+    """Element-wise parity of a window, in chunks: main grads bit-exact,
+    master / m / v within the state tolerance, 16-bit params within 1 ulp,
+    fp32 params (the master itself) within the state tolerance.  Returns a
+    list of findings (empty when every element passes)."""
+    bad = []
+    for bi in got:
+        g, w, p = got[bi], want[bi], prev[bi]
+        n = g["main"].size
+        for a in range(0, n, chunk):
+            b = min(n, a + chunk)
+            if not amax_equal(g["main"][a:b], w["main"][a:b]):
+                bad.append(f"buffer {bi}: main grad differs in [{a}, {b})")
+            for k in ("master", "exp_avg", "exp_avg_sq"):
+                ok = state_close(g[k][a:b], w[k][a:b], p[k][a:b])
+                if not ok.all():
+                    bad.append(f"buffer {bi}: {k} off at {int((~ok).sum())} elements in [{a}, {b})")
+            if g["param"].dtype == np.uint16:
+                d = ulp16(g["param"][a:b], w["param"][a:b])
+                if d.max(initial=0) > 1:
+                    bad.append(f"buffer {bi}: param off by {int(d.max())} ulp in [{a}, {b})")
+    return bad

@@ -1,13 +1,20 @@
 """Parity at the workloads' full sizes, in the launch configuration the
-benchmark times (same map, layout, rank selection, sizes and entry point).
+benchmark times (same map, layout, rank selection, sizes and entry point),
+over every step the workloads configure.
 
-The oracle cannot hold these inputs, so it checks what it can compute one
-by one: found_inf exactly; the grad norm against its own fp64 sum of squares
-streamed from the generator over every element (rel 1e-5); and thousands of
-sampled elements -- the first and last element of every param piece plus
-random ones -- recomputed from their replica grads (main grad bit-exact,
-master/m/v within 4 ulp or 1e-6 of the operand scale, 16-bit params within
-1 ulp).  A step with an injected inf must leave every sampled state
+The oracle cannot hold these inputs, so each step it checks:
+  - found_inf exactly, and the grad norm against the oracle's own fp64 sum
+    of squares streamed from the generator over every element (rel 1e-5);
+  - a window of whole buckets element by element (at least 64M elements:
+    the first, middle and last bucket of the 16-bit buffer, more buckets
+    from both ends, and every bucket of the fp32 norm-weight buffer), whose
+    main grads the oracle redraws from the generator and whose master, m
+    and v it carries from step to step: main grad bit-exact, master/m/v
+    within 4 ulp or 1e-6 of the operand scale, 16-bit params within 1 ulp;
+  - thousands of sampled elements elsewhere -- the first and last element of
+    every param piece plus random ones -- recomputed from their replica
+    grads at the same tolerances.
+A step with an injected inf must leave every sampled and window element
 bit-identical.
 """
 
@@ -28,6 +35,7 @@ import gpu_harness as H  # noqa: E402
 import oracle  # noqa: E402
 
 INF_BITS = {H.F32: float("inf"), H.BF16: 0x7F80, H.F16: 0x7C00}
+STATE = ("master", "exp_avg", "exp_avg_sq")
 
 
 def _inf_position(fc):
@@ -42,10 +50,15 @@ def _inf_position(fc):
     return best
 
 
-def _run(cfg, steps, n_random=3000):
+def _run(cfg, steps, n_random=3000, window=True):
     fc = H.FullCase(cfg)
     samples = fc.choose_samples(n_random)
     st = fc.initial_sample_state(samples)
+    if window:
+        wp = fc.window_pieces(fc.window_buckets())
+        wst = fc.window_initial_state(wp)
+        assert sum(wst[bi]["master"].size for bi in wst) >= min(64 << 20, sum(
+            len(fc.ranks) * fc.om.shard_numel(bi) for bi in range(len(fc.om.buffers))) // 2)
     t_applied = 0
     L = oracle.lib()
     for t_step in range(1, steps + 1):
@@ -56,43 +69,61 @@ def _run(cfg, steps, n_random=3000):
             assert cfg["layout"] == "full"
             fc.reps[0][spec["replica"]][_inf_position(fc)] = INF_BITS[fc.om.buffers[0].grad_dtype]
         before_dev = fc.device_samples(st)
+        before_win = fc.window_device(wp) if (inject and window) else None
         t = t_applied + 1
         found, norm = fc.step(t)
         if inject:
             assert found and math.isnan(norm)
             after = fc.device_samples(st)
             for bi in after:
-                for k in ("master", "exp_avg", "exp_avg_sq", "param"):
+                for k in STATE + ("param",):
                     assert after[bi][k].tobytes() == before_dev[bi][k].tobytes(), (bi, k)
+            if window:
+                after_win = fc.window_device(wp)
+                for bi in after_win:
+                    for k in STATE + ("param",):
+                        assert after_win[bi][k].tobytes() == before_win[bi][k].tobytes(), (bi, k)
             continue
         sumsq, bad = fc.oracle_sumsq(t_step)
         assert bad == 0 and not found
         o_norm, coef = oracle.ctypes_double(), oracle.ctypes_double()
         clip = L.or_clip_coef(sumsq, cfg["max_norm"], oracle.ctypes_byref(o_norm),
                               oracle.ctypes_byref(coef))
-        assert abs(norm - o_norm.value) <= 1e-5 * o_norm.value, (norm, o_norm.value)
+        assert abs(norm - o_norm.value) <= 1e-5 * o_norm.value, (t_step, norm, o_norm.value)
         prev = {bi: {k: v.copy() for k, v in s.items() if k != "sel"} for bi, s in st.items()}
         mains = fc.oracle_samples(st, t_step, t, coef.value, clip)
         got = fc.device_samples(st)
         for bi, s in st.items():
             g = got[bi]
-            assert np.array_equal(g["main"].view(np.uint32), mains[bi].view(np.uint32)), bi
-            for k in ("master", "exp_avg", "exp_avg_sq"):
+            assert np.array_equal(g["main"].view(np.uint32), mains[bi].view(np.uint32)), (t_step, bi)
+            for k in STATE:
                 ok = H.state_close(g[k], s[k], prev[bi][k])
-                assert ok.all(), (bi, k, int((~ok).sum()))
+                assert ok.all(), (t_step, bi, k, int((~ok).sum()))
             if s["param"].dtype == np.uint16:
-                assert H.ulp16(g["param"], s["param"]).max() <= 1, bi
+                assert H.ulp16(g["param"], s["param"]).max() <= 1, (t_step, bi)
+        if window:
+            wprev = {bi: {k: wst[bi][k].copy() for k in STATE} for bi in wst}
+            res, wbad = fc.window_oracle_step(wp, wst, t_step, t, coef.value, clip)
+            assert wbad == 0
+            want = {bi: dict(wst[bi], main=res[bi]["main"], param=res[bi]["param"]) for bi in wst}
+            findings = H.window_compare(fc.window_device(wp), want, wprev)
+            assert not findings, (t_step, findings[:10])
         t_applied += 1
     del fc
     torch.cuda.empty_cache()
 
 
 def test_bench_workload_llama7b_dp8_rank0():
-    _run(W.config("llama_7b_dp8_rank0"), steps=2)
+    cfg = W.config("llama_7b_dp8_rank0")
+    _run(cfg, steps=cfg["steps"])
 
 
-def test_hierarchical_llama7b_dp16_2x8_1m_buckets():
-    _run(W.config("llama_7b_dp16_2x8_1m"), steps=1)
+@pytest.mark.parametrize("size", ["1m", "10m", "40m", "100m"])
+def test_hierarchical_llama7b_dp16_2x8(size):
+    # 2 instances x 8 ranks, every bucket size of the sweep; the 40M point
+    # (the default bucket size) runs all its configured steps
+    cfg = W.config("llama_7b_dp16_2x8_" + size)
+    _run(cfg, steps=cfg["steps"] if size == "40m" else 3)
 
 
 def test_average_in_collective_llama7b_dp8_rank0():
@@ -105,11 +136,13 @@ def test_dp16_one_instance_general_reduce_kernel():
 
 
 def test_gpt2_small_all_ranks_with_skipped_step():
-    _run(W.config("gpt2_small_dp8"), steps=3)
+    cfg = W.config("gpt2_small_dp8")
+    _run(cfg, steps=cfg["steps"])
 
 
 def test_llama_1p3b_fp16_loss_scaled():
-    _run(W.config("llama_1p3b_fp16_dp8"), steps=1)
+    cfg = W.config("llama_1p3b_fp16_dp8")
+    _run(cfg, steps=cfg["steps"])
 
 
 def test_bf16_replica_grads_fp32_accumulation():
@@ -124,7 +157,7 @@ def test_param_larger_than_2_pow_31_elements():
     cfg = W._cfg(name="huge", params=[dict(name="huge", numel=n, dtype=W.BF16),
                                       dict(name="tail", numel=77, dtype=W.F32)],
                  dp=2, bucket_size=None, layout="shard", ranks=[1], steps=1, seed=21)
-    _run(cfg, steps=1, n_random=2000)
+    _run(cfg, steps=1, n_random=2000, window=False)
 
 
 def test_grad_check_at_full_size_bench_workload():

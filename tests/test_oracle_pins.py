@@ -713,6 +713,12 @@ def test_stream_sumsq_equals_array_path():
         s_arr = float(np.sum(main.astype(np.float64) ** 2))
         s, b = oracle.stream_sumsq(keys, gdt, synth.factor(1e-3), 1234, 5000, 0.5)
         assert bad == b == 0 and abs(s - s_arr) <= 1e-12 * s_arr
+        # the streamed main grads themselves, also with two instances and averaging
+        for n_inst, avg in ((1, False), (2, True)):
+            want, wbad = oracle.reduce_prepare(reps, gdt, 0, 5000, 0.5, n_inst, avg)
+            got, gbad = oracle.stream_reduce_prepare(keys, gdt, synth.factor(1e-3), 1234, 5000,
+                                                     inv_scale=0.5, n_inst=n_inst, average=avg)
+            assert gbad == wbad == 0 and got.tobytes() == want.tobytes()
 
 
 # --------------------------------------------------------------------------
