@@ -607,13 +607,16 @@ int dopt_state_to_model(const dopt_shard_map* map, int32_t buffer, int32_t rank,
 int dopt_state_from_model(const dopt_shard_map* map, int32_t buffer, int32_t rank, int32_t layout,
                           const void* model, void* state, dopt_stream stream);
 
-/* Test hook for the bounded waits of the TMA-staged reduce pass: while set
- * to tile >= 0, CTA 0 of every such launch announces its tile of that
- * (CTA-local) index but never copies it, so its wait runs out after about a
- * second; the step then reports kernel_error, returns DOPT_E_CUDA from
- * dopt_step and is skipped, and the CUDA context stays usable.  -1 turns the
- * hook off (the default).  Not for production use. */
+#if defined(DOPT_BOUNDS_CHECK) && DOPT_BOUNDS_CHECK
+/* Debug builds only (DOPT_BOUNDS_CHECK=1): the release library neither
+ * exports this hook nor tests for it in its kernels.  Test hook for the
+ * bounded waits of the TMA-staged reduce pass: while set to tile >= 0, CTA 0
+ * of every such launch announces its tile of that (CTA-local) index but
+ * never copies it, so its wait runs out after about a second; the step then
+ * reports kernel_error, returns DOPT_E_CUDA from dopt_step and is skipped,
+ * and the CUDA context stays usable.  -1 turns the hook off (the default). */
 int dopt_debug_starve_copy(int32_t tile);
+#endif
 
 /* Debug builds only (compiled with DOPT_BOUNDS_CHECK=1; the default build
  * returns DOPT_E_INVALID).  Every kernel of such a build checks each tile's

@@ -149,13 +149,15 @@ _c = {
     "dopt_loss_scaler_update": _proto("dopt_loss_scaler_update", ctypes.c_int,
                                       ctypes.POINTER(dopt_loss_scaler), _I32),
     "dopt_kernel_launches": _proto("dopt_kernel_launches", ctypes.c_uint64),
-    "dopt_debug_starve_copy": _proto("dopt_debug_starve_copy", ctypes.c_int, _I32),
     "dopt_step_local_stats": _proto("dopt_step_local_stats", ctypes.c_int, ctypes.POINTER(dopt_step_args), _P, _P),
     "dopt_debug_bounds_record": _proto("dopt_debug_bounds_record", ctypes.c_int, ctypes.POINTER(_I64)),
     "dopt_read_step_stats": _proto("dopt_read_step_stats", ctypes.c_int, _P,
                                    ctypes.POINTER(dopt_step_stats), _P),
     "dopt_last_error": _proto("dopt_last_error", ctypes.c_char_p),
 }
+# the debug build's test hook (absent from the release library)
+if hasattr(_lib, "dopt_debug_starve_copy"):
+    _c["dopt_debug_starve_copy"] = _proto("dopt_debug_starve_copy", ctypes.c_int, _I32)
 
 
 class DoptError(RuntimeError):
@@ -483,6 +485,10 @@ def dopt_read_step_stats(workspace, stream=None):
 
 
 def dopt_debug_starve_copy(tile):
+    """The bounded-wait test hook; only the bounds-checked debug build
+    (libdopt_checked.so) has it."""
+    if "dopt_debug_starve_copy" not in _c:
+        raise DoptError(E_INVALID, "dopt_debug_starve_copy: only the bounds-checked debug build has this hook")
     _check(_c["dopt_debug_starve_copy"](tile))
 
 

@@ -107,7 +107,9 @@ namespace {
 using namespace dopt;
 
 thread_local std::vector<char> t_param_scratch;  // kernel-parameter staging
+#if DOPT_BOUNDS_CHECK
 std::atomic<int32_t> g_starve_tile{-1};           // test hook, see dopt_debug_starve_copy
+#endif
 
 // The run table of one launch: runs [first, first + count) of a rank
 // selection, with per-run decay for K3.
@@ -250,7 +252,9 @@ int run_k1_runs(const std::vector<Run>& runs, int region_first, const K1Job& j, 
     kp.average = j.average ? 1 : 0;
     kp.post_scale = j.post_scale;
     kp.error_flag = j.ws ? reinterpret_cast<int32_t*>(static_cast<char*>(j.ws) + kErrorFlagOffset) : nullptr;
+#if DOPT_BOUNDS_CHECK
     kp.starve_tile = g_starve_tile.load(std::memory_order_relaxed);
+#endif
     kp.compact = j.compact && j.stats ? 1 : 0;
     kp.amax = j.amax;
     kp.amax_stride = j.amax_stride;
@@ -651,11 +655,13 @@ int dopt_debug_bounds_record(int64_t* out) {
 #endif
 }
 
+#if DOPT_BOUNDS_CHECK
 int dopt_debug_starve_copy(int32_t tile) {
   if (tile < -1) return fail(DOPT_E_INVALID, "dopt_debug_starve_copy: tile < -1");
   g_starve_tile.store(tile, std::memory_order_relaxed);
   return DOPT_OK;
 }
+#endif
 
 int dopt_read_step_stats(const void* workspace, dopt_step_stats* out, dopt_stream stream) {
   if (!workspace || !out) return dopt::fail(DOPT_E_INVALID, "dopt_read_step_stats: NULL workspace or out");

@@ -693,7 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
     // completes on the arrival alone
     const bool copy_ok = DOPT_RANGE_OK(p, kSiteTmaCopy, r0, n, rep);
     mbar_arrive_expect_tx(&bars[stage], copy_ok ? (unsigned)(nv * sizeof(E)) * DPI : 0u);
-    if (copy_ok && nv > 0 && !(blockIdx.x == 0 && i == p.starve_tile)) {
+#if DOPT_BOUNDS_CHECK
+    const bool starved = blockIdx.x == 0 && i == p.starve_tile;  // test hook of the debug build
+#else
+    constexpr bool starved = false;
+#endif
+    if (copy_ok && nv > 0 && !starved) {
 #pragma unroll
       for (int k = 0; k < DPI; ++k)
         bulk_load(tiles + ((size_t)stage * DPI + k) * kTmaTile, static_cast<const E*>(p.rep[k]) + r0,

@@ -208,7 +208,9 @@ struct K1Params {
   int32_t average;
   float post_scale; // scale_gradients factor on the reduced grad (1 = none)
   int32_t* error_flag;  // set by a kernel that gave up waiting (TMA path)
+#if DOPT_BOUNDS_CHECK
   int32_t starve_tile;  // test hook: CTA 0 never copies its tile of this index (-1: off)
+#endif
   int32_t compact;      // 16-bit grads, statistics pass: store the reduced grads in the
                         // grad dtype instead of the fp32 main grads (see store_main4)
   // grad check (CHECK kernels only): amax[k * amax_stride + bucket] gathers

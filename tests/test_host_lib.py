@@ -21,20 +21,33 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 
-def _header_functions():
+DEBUG_BLOCK = re.compile(r"#if defined\(DOPT_BOUNDS_CHECK\) && DOPT_BOUNDS_CHECK\n(.*?)#endif", re.S)
+
+
+def _header_functions(debug_build):
+    """Functions include/dopt.h declares for the release build, or (debug_build)
+    for the bounds-checked debug build, which adds its test hooks."""
     src = open(os.path.join(ROOT, "include", "dopt.h")).read()
+    if not debug_build:
+        src = DEBUG_BLOCK.sub("", src)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(dopt_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_symbol():
-    names = _header_functions()
+    debug = os.path.basename(dopt.LIB_PATH) == "libdopt_checked.so"
+    names = _header_functions(debug)
     assert len(names) >= 20
     import ctypes
     lib = ctypes.CDLL(dopt.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(dopt.exported_symbols())
+    hooks = set(_header_functions(True)) - set(_header_functions(False))
+    assert hooks == {"dopt_debug_starve_copy"}
+    if not debug:  # the release library carries no test hook
+        for n in hooks:
+            assert not hasattr(lib, n), n
 
 
 def _compare_maps(params, dp, bucket_size, grad_fp32, busbw):
