@@ -70,8 +70,12 @@ typedef enum { DOPT_GROUP_FP32_FROM_FLOAT16 = 0, DOPT_GROUP_FP32 = 1 } dopt_grou
 /* Layout of the emulated replica gradient buffers. */
 typedef enum {
   DOPT_LAYOUT_FULL_BUFFER = 0, /* each replica is a whole grad buffer (numel)   */
-  DOPT_LAYOUT_SHARD_ONLY = 1   /* each replica holds only the selected rank's
+  DOPT_LAYOUT_SHARD_ONLY = 1,  /* each replica holds only the selected rank's
                                   flat shard (shard_numel); one rank only      */
+  DOPT_LAYOUT_BUCKET = 2       /* ZeRO-2 streaming: each replica holds only the
+                                  bucket group being reduced, as laid out in
+                                  the grad buffer from the group's first bucket
+                                  on; dopt_step_reduce_buckets only (see there) */
 } dopt_layout;
 
 #define DOPT_ALL_RANKS (-1)
@@ -436,6 +440,25 @@ int dopt_step_async(const dopt_step_args* args, int32_t* d_found_inf, float* d_n
  * dopt_step_reduce_buckets reduces a group of buckets in as few launches as
  * the kernels' run tables allow (one, for groups of up to 960 runs); with
  * d_step set it issues only launches and memsets, like the fused step.
+ *
+ * ZeRO-2 streaming (DeepSpeed page, ZeRO stage 2: each rank keeps only its
+ * partition of the reduced grads, and the full grads of a bucket are given
+ * up once the bucket's reduce-scatter is done; ZeRO ledger page, section 2:
+ * 2P + 14P/N per card).  With args->layout = DOPT_LAYOUT_BUCKET, replica k
+ * of buffer `buffer` (args->replica_grads[buffer][k]) holds only the grads
+ * of buckets [bucket_first, bucket_first + bucket_count): element i of the
+ * group, i.e. element offset(bucket_first) + i of the grad buffer, at index
+ * i.  The replicas then need only the group's size, not the buffer's, and
+ * may be refilled with another group's grads as soon as this call's work on
+ * args->stream has run (record an event after it); a ring of two such
+ * staging buffers per replica streams every bucket of a step.  The rank's
+ * own grads beyond the group are never held.  The selected rank's
+ * (or every rank's) slice of each bucket is read, as with the whole buffer.
+ * dopt_step_finalize, dopt_step_local_stats and dopt_step_update_buckets
+ * accept this layout and read no replica; every other entry point refuses
+ * it (DOPT_E_INVALID).  For 16-bit grads the main grads between the passes
+ * take 2 bytes per shard element (see the main-grad note above), the
+ * ledger's 2P/N grad term.
  */
 size_t dopt_workspace_bytes_bucketed(const dopt_shard_map* map, int32_t rank);
 int dopt_step_reduce_buckets(const dopt_step_args* args, int32_t buffer, int32_t bucket_first,

@@ -25,7 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 F32, BF16, F16 = 0, 1, 2
 OK, E_INVALID, E_ALIGN, E_SIZE, E_CUDA, E_NOMEM = 0, -1, -2, -3, -4, -5
 GROUP_FP32_FROM_FLOAT16, GROUP_FP32 = 0, 1
-LAYOUT_FULL_BUFFER, LAYOUT_SHARD_ONLY = 0, 1
+LAYOUT_FULL_BUFFER, LAYOUT_SHARD_ONLY, LAYOUT_BUCKET = 0, 1, 2
 ALL_RANKS = -1
 MAX_REPLICAS = 64
 
@@ -371,6 +371,15 @@ class StepArgs:
 
     def set_stream(self, stream):
         self.c.stream = _stream(stream)
+
+    def set_replicas(self, buffer, replicas):
+        """Points buffer `buffer`'s replica grads at other device memory (the
+        same count; e.g. the staging buffers of DOPT_LAYOUT_BUCKET)."""
+        arr = self._reps[buffer]
+        if len(replicas) != len(arr):
+            raise ValueError("replica count differs")
+        for k, r in enumerate(replicas):
+            arr[k] = _ptr(r)
 
     def set_device_step(self, d_step, d_lr=None):
         """Use a device int64 step counter (and optionally a device double

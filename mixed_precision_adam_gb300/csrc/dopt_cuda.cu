@@ -293,7 +293,7 @@ K1Job step_job(const dopt_step_args* a, int32_t b) {
   j.replicas = a->replica_grads[b];
   j.n_rep = m->dp * a->n_instances;
   j.n_inst = a->n_instances;
-  j.full = a->layout == DOPT_LAYOUT_FULL_BUFFER;
+  j.full = a->layout != DOPT_LAYOUT_SHARD_ONLY;  // whole buffers and bucket groups: buffer indices
   j.average = a->average_in_collective;
   j.inv_scale = a->inv_loss_scale;
   j.post_scale = a->grad_scale == 0.0f ? 1.0f : a->grad_scale;  // 0 (unset) means 1
@@ -506,7 +506,7 @@ int check_replicas(const dopt_shard_map* m, int32_t rank, const void* const* rep
   if (n_inst < 1 || n_rep != m->dp * n_inst || n_rep > DOPT_MAX_REPLICAS)
     return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": n_replicas must be DP * n_instances (at most " +
                                           std::to_string(DOPT_MAX_REPLICAS) + ")");
-  if (layout != DOPT_LAYOUT_FULL_BUFFER && layout != DOPT_LAYOUT_SHARD_ONLY)
+  if (layout != DOPT_LAYOUT_FULL_BUFFER && layout != DOPT_LAYOUT_SHARD_ONLY && layout != DOPT_LAYOUT_BUCKET)
     return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": unknown layout");
   if (layout == DOPT_LAYOUT_SHARD_ONLY && rank == DOPT_ALL_RANKS)
     return dopt::fail(DOPT_E_INVALID, std::string(fn) + ": SHARD_ONLY layout needs a single rank");
@@ -540,6 +540,8 @@ int check_step_args(const dopt_step_args* a, bool bucketed, const char* fn) {
   } else if ((st = check_workspace(m, a->rank, a->workspace, a->workspace_bytes, fn))) {
     return st;
   }
+  if (!bucketed && a->layout == DOPT_LAYOUT_BUCKET)
+    return fail(DOPT_E_INVALID, std::string(fn) + ": the bucket layout is for the bucket-staged step only");
   if ((st = check_hparams(&a->hp, fn))) return st;
   if ((a->d_step && (reinterpret_cast<uintptr_t>(a->d_step) & 7)) ||
       (a->d_lr && (reinterpret_cast<uintptr_t>(a->d_lr) & 7)))
@@ -606,13 +608,20 @@ int enqueue_reduce(const dopt_step_args* a, int32_t* d_found_inf, float* d_norm)
                                          a->remote_found_inf, a->max_norm, d_norm, nullptr, d_found_inf, a);
   {
     Range r("reduce_prepare+finalize");
-    for (int32_t b = 0; b < nb; ++b) {
-      K1Job j = step_job(a, b);
-      if (b == nb - 1) {
+    // the largest buffer's launch goes last and carries the finalize, whose
+    // tail then overlaps nothing but that launch's own last CTAs (the
+    // partials' order in the sum is fixed by buffer, not by launch order)
+    std::vector<int32_t> order(nb);
+    for (int32_t b = 0; b < nb; ++b) order[b] = b;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int32_t x, int32_t y) { return shard_numel(m, x) < shard_numel(m, y); });
+    for (int32_t i = 0; i < nb; ++i) {
+      K1Job j = step_job(a, order[i]);
+      if (i == nb - 1) {
         j.fin = &fin;
         j.fin_counter = counter;
       }
-      if ((st = run_k1(m, b, a->rank, j, s))) return st;
+      if ((st = run_k1(m, order[i], a->rank, j, s))) return st;
     }
   }
   if ((st = record_stage(a, 1, s))) return st;
@@ -690,6 +699,8 @@ int dopt_grad_reduce_shard(const dopt_shard_map* map, int32_t buffer, int32_t ra
   if (st) return st;
   dopt_shard_map* m = const_cast<dopt_shard_map*>(map);
   if ((st = check_replicas(m, rank, replicas, n_replicas, n_instances, layout, fn))) return st;
+  if (layout == DOPT_LAYOUT_BUCKET)
+    return dopt::fail(DOPT_E_INVALID, "dopt_grad_reduce_shard: the bucket layout is for the bucket-staged step only");
   if (!main_grad) return dopt::fail(DOPT_E_INVALID, "dopt_grad_reduce_shard: NULL main_grad");
   if (!aligned16(main_grad)) return dopt::fail(DOPT_E_ALIGN, "dopt_grad_reduce_shard: main_grad not aligned");
   (void)workspace;
@@ -801,7 +812,7 @@ int dopt_step_reduce_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
   std::vector<std::vector<Run>> by = runs_by_bucket(m, buffer, a->rank);
   cudaStream_t s = (cudaStream_t)a->stream;
   if ((st = clear_amax(a, bucket_number(m, buffer, bucket_first), bucket_count, s))) return st;
-  const K1Job j = step_job(a, buffer);
+  K1Job j = step_job(a, buffer);
   // the group's runs in as few launches as the run tables allow; their
   // partials fill the group's first regions, and the group's other regions
   // are zeroed so that no partial of an earlier step is left in them
@@ -810,6 +821,16 @@ int dopt_step_reduce_buckets(const dopt_step_args* a, int32_t buffer, int32_t bu
   for (int32_t k = bucket_first; k < bucket_first + bucket_count; ++k) {
     runs.insert(runs.end(), by[k].begin(), by[k].end());
     regions += (int)chunks_of(by[k]).size();
+  }
+  if (a->layout == DOPT_LAYOUT_BUCKET) {
+    // replicas hold the group only: buffer indices from the group's first
+    // bucket on (bucket offsets are multiples of 64 elements, so the runs'
+    // 8-element alignment is kept)
+    const Buffer& buf = m->buffers[buffer];
+    const Bucket& last = buf.buckets[bucket_first + bucket_count - 1];
+    const int64_t base = buf.buckets[bucket_first].offset;
+    for (Run& r : runs) r.world -= base;
+    j.ext_rep = last.offset + last.numel - base;
   }
   const int first = bucketed_region(m, a->rank, buffer, bucket_first);
   if ((st = run_k1_runs(runs, first, j, s))) return st;
@@ -961,6 +982,8 @@ int dopt_step_from_host(const dopt_step_args* a, const void* const* const* host_
   if (st) return st;
   if (a->d_global_sumsq)
     return fail(DOPT_E_INVALID, std::string(fn) + ": d_global_sumsq is for the bucket-staged finalize (dopt_step_finalize)");
+  if (a->layout == DOPT_LAYOUT_BUCKET)
+    return fail(DOPT_E_INVALID, std::string(fn) + ": the bucket layout is for dopt_step_reduce_buckets only");
   dopt_shard_map* m = const_cast<dopt_shard_map*>(a->map);
   const int32_t nb = (int32_t)m->buffers.size();
   const int32_t n_rep = m->dp * a->n_instances;

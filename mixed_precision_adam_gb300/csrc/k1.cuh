@@ -493,6 +493,7 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
     }
     if (STATS) acc.maybe_flush();
   }
+  allow_dependent_launch();
   if constexpr (CHECK) {
     if (cur_bucket >= 0) flush_bucket(cur_bucket);
   }
@@ -630,6 +631,7 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
     }
     if (STATS) acc.maybe_flush();
   }
+  allow_dependent_launch();
   if constexpr (CHECK) {
     if (cur_bucket >= 0) flush_bucket(cur_bucket);
   }
@@ -802,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
     __syncthreads();
     acc.s = __int_as_float(0x7FC00000);  // a NaN partial skips the step
   }
+  allow_dependent_launch();
   if constexpr (CHECK) {
     if (cur_bucket >= 0) flush_bucket(cur_bucket);
   }
@@ -851,7 +854,16 @@ int launch_k1_sel(K1Params& kp, const K1Launch& l, cudaStream_t s) {
   bool all_aligned = true;
   for (int k = 0; k < l.count; ++k) all_aligned &= seg_aligned(l.runs[k].local, l.runs[k].world);
   constexpr bool kTmaKind = DOPT_K1_TMA && STATS && std::is_same<GT, float>::value;
-  const bool tma = kTmaKind && kp.error_flag && special && kp.n_inst == 1 && all_aligned;
+  bool tma = kTmaKind && kp.error_flag && special && kp.n_inst == 1 && all_aligned;
+  if (tma) {
+    // a launch too short to give every CTA several bulk-copied tiles streams
+    // through registers instead: there the copy pipeline's fill and drain
+    // and the uneven last round of tiles cost more than the staging saves
+    fill_table(kp.tab, l.runs, l.count, kTmaTile, l.bucket_base);
+    int sms = 0;
+    if (int st = device_sms(&sms)) return st;
+    tma = kp.tab.n_tiles >= kTmaMinTilesPerSm * sms;
+  }
   const int tile = tma ? kTmaTile : special ? kThreads * kVec * kUnroll1 * GradT<GT>::kUnroll : kTile1;
   fill_table(kp.tab, l.runs, l.count, tile, l.bucket_base);
   if constexpr (kTmaKind) {

@@ -58,6 +58,9 @@
 #ifndef DOPT_K3_MIN_BLOCKS
 #define DOPT_K3_MIN_BLOCKS 4
 #endif
+#ifndef DOPT_K3_BULK_STORE
+#define DOPT_K3_BULK_STORE 0  // 1: the AdamW pass stages its results in shared memory and writes them with bulk copies
+#endif
 #ifndef DOPT_BOUNDS_CHECK
 #define DOPT_BOUNDS_CHECK 0  // 1: debug build; every tile is checked against the extents of its buffers
 #endif
@@ -71,6 +74,7 @@ constexpr int kUnroll3 = DOPT_K3_UNROLL;   // K3 accesses per thread per tile
 constexpr int kTile1 = kThreads * kVec * kUnroll1;  // K1 elements per tile
 constexpr int kTile3 = kThreads * kVec * kUnroll3;  // K3 elements per tile
 constexpr int kTmaTile = DOPT_TMA_TILE;    // elements per tile of the TMA-staged K1
+constexpr int kTmaMinTilesPerSm = 16;      // shorter launches take the register-staged K1
 static_assert(kTmaTile % (kThreads * kVec) == 0, "TMA tile");
 constexpr int kMaxSeg = 960;               // runs per launch (kernel-parameter table)
 constexpr int kMaxGrid = 1024;             // partial slots per launch region (CTAs per launch at most)
@@ -246,6 +250,18 @@ struct K3Params {
 };
 
 static_assert(sizeof(K1Params) <= 32764 && sizeof(K3Params) <= 32764, "kernel parameter limit");
+
+// Programmatic dependent launch.  A reduce kernel lets the kernel after it
+// in the stream start its CTAs once every reduce CTA has finished its tiles
+// (the AdamW pass is launched with programmatic stream serialization), and
+// that kernel waits for the whole reduce grid -- the finalize included --
+// to complete and its writes to be visible before it reads anything.  For a
+// kernel launched without the attribute, or after one that never signals,
+// the wait returns at once.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Advances the run cursor of a CTA to the run holding tile t (tiles visited
 // in increasing order, so the cursor only moves forward).

@@ -448,7 +448,7 @@ def compare_step(hc, dc, ores, found, norm, before, report, compact=True, ws=Non
         got_main = mains[bi]
         if compact:
             got_main = decode_main(got_main, buf.grad_dtype, np.float32(1.0 / hc.cfg["loss_scale"]),
-                                   len(got_main))
+                                   len(st["exp_avg"]))
         if not amax_equal(got_main[mask], om_[mask]):
             report.append(f"buffer {bi}: main grad differs")
             ok = False

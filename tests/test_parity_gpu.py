@@ -215,7 +215,9 @@ def test_bounded_wait_runs_out_and_reports():
     D = H.dopt()
     if "dopt_debug_starve_copy" not in D.exported_symbols():
         pytest.skip("the copy-starving hook is compiled into the bounds-checked debug build only")
-    params = [dict(numel=300_000, dtype=1), dict(numel=4096, dtype=1)]
+    # enough tiles that the reduce pass takes the bulk-copy kernel
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    params = _tma_sized_params(int(1.25 * 16 * 2048 * sms)) + [dict(numel=4096, dtype=1)]
     cfg = _tiny(params, 2, bucket_size=None, steps=2)
     hc = H.HostCase(cfg)
     dc = H.DeviceCase(hc)
@@ -420,3 +422,35 @@ def test_two_hundred_steps_track_the_oracle():
     ok, report = H.run_parity(cfg)
     assert ok, "\n".join(r for r in report if "ok=False" in r or not r.startswith("step"))[:4000]
     assert sum("found_inf=True" in r for r in report) == 1  # the step with the inf, skipped
+
+
+def _tma_sized_params(scale):
+    """Ragged bf16 params (each starts on the 64-element pad, most end off
+    the 4- and 8-element grids) totalling `scale` elements or more."""
+    sizes = [1_000_003, 777_777, 65, 2_500_001, 999_999, 333, 1_234_567, 4_099, 640_000, 31]
+    out, total, i = [], 0, 0
+    while total < scale:
+        n = sizes[i % len(sizes)]
+        out.append(dict(numel=n, dtype=1))
+        total += n
+        i += 1
+    return out
+
+
+@pytest.mark.parametrize("dp,average,check", [(1, False, False), (2, True, False), (4, False, True),
+                                              (8, False, False), (8, True, True)])
+def test_tma_staged_reduce_ragged(dp, average, check):
+    """fp32 replicas in one instance, every run 8-element aligned, and enough
+    tiles (16 x 2048 elements per SM or more) that the reduce pass stages the
+    replica tiles through shared memory with bulk copies: ragged run ends
+    (the last elements of a run after its last multiple of 4), every
+    replica count the staged kernel takes, averaging, and the grad check."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    params = _tma_sized_params(int(1.25 * 16 * 2048 * sms))
+    cfg = _tiny(params, dp, bucket_size=3_000_000, grad_reduce_in_fp32=True, average=average, steps=2,
+                seed=23 + dp)
+    if check:
+        ok, report = H.run_check(cfg, [[(0, 0, 3.0)], [(5, dp - 1, -7.5)]])
+        assert ok, "\n".join(report)
+    else:
+        _check(cfg)
