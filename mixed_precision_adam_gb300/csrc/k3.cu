@@ -337,7 +337,7 @@ int launch_k3_t(K3Params& kp, cudaStream_t s) {
   // pass before it finishes (each waits in wait_for_prior_grids)
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = DOPT_K3_PDL;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);

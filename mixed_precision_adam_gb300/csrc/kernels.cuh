@@ -58,6 +58,9 @@
 #ifndef DOPT_K3_MIN_BLOCKS
 #define DOPT_K3_MIN_BLOCKS 4
 #endif
+#ifndef DOPT_K3_PDL
+#define DOPT_K3_PDL 1  // 1: the AdamW pass is launched as a programmatic dependent of the reduce pass
+#endif
 #ifndef DOPT_K3_BULK_STORE
 #define DOPT_K3_BULK_STORE 0  // 1: the AdamW pass stages its results in shared memory and writes them with bulk copies
 #endif
