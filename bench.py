@@ -410,10 +410,11 @@ def k1_variant(cfg, check_grads):
 
 
 def recorded_traffic(elements_k1, variant):
-    """DRAM traffic of the reduce/prepare pass from the committed ncu summary,
-    scaled to this launch's elements; None when the kernel source changed
-    since the counters were taken, or when this workload runs another
-    variant of the kernel than the one captured."""
+    """DRAM traffic of the reduce/prepare pass from the committed ncu summary
+    (taken on a small case of the same kernel), scaled per element to this
+    launch's elements; None when the kernel source changed since the
+    counters were taken, or when this workload runs another variant of the
+    kernel than the one captured."""
     path = os.path.join(ROOT, "profiles", "ncu_k1_traffic.json")
     try:
         rec = json.load(open(path))
