@@ -53,10 +53,10 @@ k2_finalize(const FinalizeArgs f) {
 // ------------------------------------------- launch helpers (kernels.cuh) --
 
 struct DeviceInfo {
-  int device = -1, sms = 0;
+  int device = -1, sms = 0, l2_bytes = 0;
 };
 
-int device_sms(int* sms) {
+int device_sms(int* sms, int* l2_bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(DOPT_E_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
@@ -66,10 +66,16 @@ int device_sms(int* sms) {
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
       return fail(DOPT_E_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+    int l2 = 0;
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess)
+      return fail(DOPT_E_CUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
     cache.device = dev;
     cache.sms = n;
+    cache.l2_bytes = l2;
   }
   *sms = cache.sms;
+  if (l2_bytes) *l2_bytes = cache.l2_bytes;
   return DOPT_OK;
 }
 
@@ -198,6 +204,7 @@ struct K1Job {
   int64_t amax_stride = 0;   // buckets of all buffers
   int32_t bucket_base = 0;   // number of the buffer's first bucket
   bool compact = false;      // 16-bit grads: keep the reduced grads in the grad dtype
+  bool keep_main = false;    // fp32 main grads stored to stay in L2 for the AdamW pass
   const FinalizeArgs* fin = nullptr;  // finalize in the last launch's last CTA (fused step)
   uint32_t* fin_counter = nullptr;
   int64_t ext_rep = 0, ext_main = 0;  // element extents of each replica and of main_grad
@@ -256,6 +263,7 @@ int run_k1_runs(const std::vector<Run>& runs, int region_first, const K1Job& j, 
     kp.starve_tile = g_starve_tile.load(std::memory_order_relaxed);
 #endif
     kp.compact = j.compact && j.stats ? 1 : 0;
+    kp.keep_main = j.keep_main ? 1 : 0;
     kp.amax = j.amax;
     kp.amax_stride = j.amax_stride;
     const bool last = &c == &chunks.back();
@@ -286,6 +294,19 @@ int32_t bucket_number(const dopt_shard_map* m, int32_t buffer, int32_t bucket) {
   return n + bucket;
 }
 
+// Whether a step's main grads (every buffer of the rank selection) are
+// small enough next to L2 to be stored for the AdamW pass to read back
+// from L2 rather than from DRAM.
+bool keep_main_in_l2(const dopt_shard_map* m, int32_t rank) {
+  if (DOPT_KEEP_MAIN_L2_DIV <= 0) return false;
+  int sms = 0, l2 = 0;
+  if (device_sms(&sms, &l2) != DOPT_OK) return false;
+  size_t bytes = 0;
+  for (int32_t b = 0; b < (int32_t)m->buffers.size(); ++b)
+    bytes += (size_t)shard_extent(m, b, rank) * (m->buffers[b].grad_dtype == DOPT_F32 ? 4 : 2);
+  return bytes <= (size_t)l2 / DOPT_KEEP_MAIN_L2_DIV;
+}
+
 // The K1 job of buffer b of a step.
 K1Job step_job(const dopt_step_args* a, int32_t b) {
   const dopt_shard_map* m = a->map;
@@ -307,6 +328,7 @@ K1Job step_job(const dopt_step_args* a, int32_t b) {
   j.compact = j.gdt != DOPT_F32;
   j.ext_rep = replica_extent(m, b, a->rank, j.full);
   j.ext_main = shard_extent(m, b, a->rank);
+  j.keep_main = keep_main_in_l2(m, a->rank);
   return j;
 }
 

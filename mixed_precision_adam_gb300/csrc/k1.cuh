@@ -266,7 +266,10 @@ __device__ __forceinline__ void finish_store4(const K1Params& p, int64_t i, floa
   }
 #pragma unroll
   for (int j = 0; j < kVec; ++j) v[j] = __fmul_rn(v[j], p.inv_scale);
-  __stcs(reinterpret_cast<float4*>(p.main_grad + i), make_float4(v[0], v[1], v[2], v[3]));
+  if (p.keep_main)  // a short step: the AdamW pass will find the main grads in L2
+    __stcg(reinterpret_cast<float4*>(p.main_grad + i), make_float4(v[0], v[1], v[2], v[3]));
+  else
+    __stcs(reinterpret_cast<float4*>(p.main_grad + i), make_float4(v[0], v[1], v[2], v[3]));
 }
 template <typename GT, bool STATS>
 __device__ __forceinline__ float finish_store1(const K1Params& p, int64_t i, float r) {
@@ -512,8 +515,15 @@ k1_reduce_prepare(const __grid_constant__ K1Params p) {
 // CHECK every thread keeps a running maximum per replica in registers and
 // each warp merges it into the global table when its tiles move to another
 // bucket.
+// Up to four fp32 replicas of one instance fit in 64 registers, so four
+// CTAs share an SM: twice the loads in flight of the two-CTA bound.
+template <typename GT, int DPI, int NINST>
+constexpr int k1n_min_blocks() {
+  return (sizeof(GT) == 4 && DPI <= 4 && NINST == 1) ? DOPT_K1N_FP32_MIN_BLOCKS : DOPT_K1_MIN_BLOCKS;
+}
+
 template <typename GT, bool FULL, bool STATS, bool CHECK, bool AVG, int DPI, int NINST>
-__global__ void __launch_bounds__(kThreads, DOPT_K1_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, (k1n_min_blocks<GT, DPI, NINST>()))
 k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
   constexpr int U = kUnroll1 * GradT<GT>::kUnroll;  // accesses per thread per tile
   constexpr int TILE = kThreads * kVec * U;

@@ -55,6 +55,12 @@
 #ifndef DOPT_K1_MIN_BLOCKS
 #define DOPT_K1_MIN_BLOCKS 2
 #endif
+#ifndef DOPT_K1N_FP32_MIN_BLOCKS
+#define DOPT_K1N_FP32_MIN_BLOCKS 4  // register-staged K1, up to 4 fp32 replicas of one instance
+#endif
+#ifndef DOPT_KEEP_MAIN_L2_DIV
+#define DOPT_KEEP_MAIN_L2_DIV 4  // fp32 main grads of a step at most L2 / this are kept in L2 (0: never)
+#endif
 #ifndef DOPT_K3_MIN_BLOCKS
 #define DOPT_K3_MIN_BLOCKS 4
 #endif
@@ -220,6 +226,8 @@ struct K1Params {
 #endif
   int32_t compact;      // 16-bit grads, statistics pass: store the reduced grads in the
                         // grad dtype instead of the fp32 main grads (see store_main4)
+  int32_t keep_main;    // fp32 main grads stored without the evict-first hint, to be
+                        // read back from L2 (steps whose main grads fit L2 easily)
   // grad check (CHECK kernels only): amax[k * amax_stride + bucket] gathers
   // the fp32 bits of replica k's largest |g| in that bucket (atomic max)
   uint32_t* amax;
@@ -398,8 +406,9 @@ __device__ __forceinline__ void finalize_if_last(const K1Params& p) {
 
 // ------------------------------------------------------- host-side launch --
 
-// SM count of the current device (cached per thread and device).
-int device_sms(int* sms);
+// SM count (and, when l2_bytes is given, the L2 size in bytes) of the
+// current device, cached per thread and device.
+int device_sms(int* sms, int* l2_bytes = nullptr);
 // Counts a launch and turns a launch error into a status.
 int check_launch(const char* what);
 
