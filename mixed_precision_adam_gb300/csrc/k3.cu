@@ -12,6 +12,19 @@
 
 namespace dopt {
 
+// The AdamW pass's result stores: streaming (evict-first) by default;
+// DOPT_K3_STORE_HINT 1 caches them in L2 only, 2 uses plain write-back stores.
+template <typename T>
+__device__ __forceinline__ void st_out(T* p, const T& v) {
+#if DOPT_K3_STORE_HINT == 1
+  __stcg(p, v);
+#elif DOPT_K3_STORE_HINT == 2
+  *p = v;
+#else
+  __stcs(p, v);
+#endif
+}
+
 template <typename PT>
 struct ParamT;
 template <>
@@ -24,7 +37,7 @@ struct ParamT<__nv_bfloat16> {
     return make_uint2((unsigned)h[0] | ((unsigned)h[1] << 16), (unsigned)h[2] | ((unsigned)h[3] << 16));
   }
   static __device__ __forceinline__ void store4(void* p, int64_t i, const float* x) {
-    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i), pack4(x));
+    st_out(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i), pack4(x));
   }
   static __device__ __forceinline__ void store1(void* p, int64_t i, float x) {
     static_cast<unsigned short*>(p)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
@@ -40,7 +53,7 @@ struct ParamT<__half> {
     return make_uint2((unsigned)h[0] | ((unsigned)h[1] << 16), (unsigned)h[2] | ((unsigned)h[3] << 16));
   }
   static __device__ __forceinline__ void store4(void* p, int64_t i, const float* x) {
-    __stcs(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i), pack4(x));
+    st_out(reinterpret_cast<uint2*>(static_cast<unsigned short*>(p) + i), pack4(x));
   }
   static __device__ __forceinline__ void store1(void* p, int64_t i, float x) {
     static_cast<unsigned short*>(p)[i] = __half_as_ushort(__float2half_rn(x));
@@ -215,9 +228,9 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
         float v[kVec] = {cur.v[u].x, cur.v[u].y, cur.v[u].z, cur.v[u].w};
 #pragma unroll
         for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[j], c), cur.decay, p, ss, w[j], m[j], v[j]);
-        __stcs(reinterpret_cast<float4*>(wbase + cur.m0 + e), make_float4(w[0], w[1], w[2], w[3]));
-        __stcs(reinterpret_cast<float4*>(p.exp_avg + cur.l0 + e), make_float4(m[0], m[1], m[2], m[3]));
-        __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + cur.l0 + e), make_float4(v[0], v[1], v[2], v[3]));
+        st_out(reinterpret_cast<float4*>(wbase + cur.m0 + e), make_float4(w[0], w[1], w[2], w[3]));
+        st_out(reinterpret_cast<float4*>(p.exp_avg + cur.l0 + e), make_float4(m[0], m[1], m[2], m[3]));
+        st_out(reinterpret_cast<float4*>(p.exp_avg_sq + cur.l0 + e), make_float4(v[0], v[1], v[2], v[3]));
         ParamT<PT>::store4(p.param, cur.w0 + e, w);
       } else if (e < cur.n) {
         const int cnt = min(kVec, cur.n - e);

@@ -67,6 +67,9 @@
 #ifndef DOPT_K3_PDL
 #define DOPT_K3_PDL 1  // 1: the AdamW pass is launched as a programmatic dependent of the reduce pass
 #endif
+#ifndef DOPT_K3_STORE_HINT
+#define DOPT_K3_STORE_HINT 0  // the AdamW pass's stores: 0 streaming, 1 L2 only, 2 write-back
+#endif
 #ifndef DOPT_K3_BULK_STORE
 #define DOPT_K3_BULK_STORE 0  // 1: the AdamW pass stages its results in shared memory and writes them with bulk copies
 #endif
