@@ -293,3 +293,32 @@ def test_rank_buffer_sizes_equal_the_ledger(dp):
     zero2 = 2 * P + 2 * S + state           # params + grad shard
     assert dopt.dopt_memory_ledger(P, dp, 1)[0] == zero1
     assert dopt.dopt_memory_ledger(P, dp, 2)[0] == zero2
+
+
+def test_bucket_layout_only_for_the_bucket_staged_reduce():
+    """DOPT_LAYOUT_BUCKET (replicas that hold one bucket group) is refused,
+    before any device work, by every entry point but the bucket-staged
+    ones: the fused step, the host-fed step and the separate reduce."""
+    m = dopt.dopt_build_shard_map([dict(numel=1000, dtype=1), dict(numel=64, dtype=1, new_bucket=True)],
+                                  2, -1, True, False)
+    fake = [[16, 32], [48, 64]]  # aligned, never dereferenced
+    per_buf = [16, 16]
+    ws_fused = dopt.dopt_workspace_bytes(m, 0)
+    args = dopt.StepArgs(m, 0, fake, per_buf, per_buf, per_buf, per_buf, per_buf, W.HP, 1, 256, ws_fused,
+                         layout=dopt.LAYOUT_BUCKET)
+    for call in (lambda: dopt.dopt_step(args), lambda: dopt.dopt_step_async(args, None, None)):
+        with pytest.raises(dopt.DoptError) as e:
+            call()
+        assert e.value.status == dopt.E_INVALID and "bucket" in str(e.value)
+    args.c.workspace_bytes = dopt.dopt_workspace_bytes_bucketed(m, 0)
+    with pytest.raises(dopt.DoptError) as e:
+        dopt.dopt_step_from_host(args, [[np.zeros(4, np.float32)] * 2] * 2)
+    assert e.value.status == dopt.E_INVALID and "bucket" in str(e.value)
+    with pytest.raises(dopt.DoptError) as e:
+        dopt.dopt_grad_reduce_shard(m, 0, 0, [16, 32], 1, dopt.LAYOUT_BUCKET, False, 16, 16,
+                                    dopt.dopt_workspace_bytes(m, 0))
+    assert e.value.status == dopt.E_INVALID and "bucket" in str(e.value)
+    args.c.layout = 7
+    with pytest.raises(dopt.DoptError) as e:
+        dopt.dopt_step(args)
+    assert e.value.status == dopt.E_INVALID
