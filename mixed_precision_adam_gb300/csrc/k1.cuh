@@ -651,6 +651,100 @@ k1_reduce_prepare_n(const __grid_constant__ K1Params p) {
   }
 }
 
+// ------------------------------------------------- K1 for short launches --
+//
+// fp32 replicas of one instance in a launch too short for the bulk-copy
+// pipeline: one access of kVec elements per thread per tile (kShortTile
+// elements), with the loads of a CTA's next tile issued before the current
+// tile's arithmetic (software pipelining across tiles, as in the AdamW
+// pass), so every CTA keeps two tiles of replica reads in flight and the
+// last round of tiles is short.  Same arithmetic, in the same order, as
+// the other kernels.
+
+template <int DPI>
+struct ShortTile {
+  float4 x[DPI];
+  int64_t l0, r0;
+  int n;
+  bool aligned;
+};
+
+template <bool FULL, int DPI>
+__device__ __forceinline__ void short_load(const K1Params& p, int& si, int t, ShortTile<DPI>& T) {
+  si = seek(p.tab, si, t);
+  const Seg& sg = p.tab.seg[si];
+  const int64_t off = (int64_t)(t - sg.tile0) * kShortTile;
+  T.n = (int)min((int64_t)kShortTile, (int64_t)sg.len - off);
+  T.l0 = sg.local + off;
+  T.r0 = FULL ? sg.world + off : T.l0;
+  T.aligned = seg_aligned(sg.local, sg.world);
+  if (!(DOPT_RANGE_OK(p, kSiteK1Rep, T.r0, T.n, rep) && DOPT_RANGE_OK(p, kSiteK1Main, T.l0, T.n, main)))
+    T.n = 0;  // debug builds only: a tile outside its buffers is skipped
+  const int e = threadIdx.x * kVec;
+  if (T.aligned && e + kVec <= T.n) {
+#pragma unroll
+    for (int k = 0; k < DPI; ++k) T.x[k] = GradT<float>::load4(p.rep[k], T.r0 + e);
+  }
+}
+
+template <int DPI>
+constexpr int k1s_min_blocks() {
+  return DPI <= 4 ? 4 : 2;
+}
+
+template <bool FULL, bool STATS, bool AVG, int DPI>
+__global__ void __launch_bounds__(kThreads, (k1s_min_blocks<DPI>()))
+k1_reduce_prepare_short(const __grid_constant__ K1Params p) {
+  SumSq acc;
+  const float pre = p.pre;
+  int si = 0;
+  int t = blockIdx.x;
+  if (t < p.tab.n_tiles) {
+    ShortTile<DPI> cur;
+    short_load<FULL, DPI>(p, si, t, cur);
+    for (; t < p.tab.n_tiles; t += gridDim.x) {
+      const bool more = t + (int)gridDim.x < p.tab.n_tiles;
+      ShortTile<DPI> nxt;
+      if (more) short_load<FULL, DPI>(p, si, t + gridDim.x, nxt);
+      const int e = threadIdx.x * kVec;
+      if (cur.aligned && e + kVec <= cur.n) {
+        float m[kVec];
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          float sum = term_of<AVG>(GradT<float>::at(cur.x[0], q), pre);
+#pragma unroll
+          for (int k = 1; k < DPI; ++k) sum = __fadd_rn(sum, term_of<AVG>(GradT<float>::at(cur.x[k], q), pre));
+          m[q] = post_scaled<float>(instance_value<float, AVG>(sum, p.inv_dpi), p.post_scale);
+        }
+        finish_store4<float, STATS>(p, cur.l0 + e, m);
+        if (STATS) acc.add4(m);
+      } else if (e < cur.n) {
+        // the ragged end of a run, or a run whose starts are not 8-element aligned
+        const int cnt = min(kVec, cur.n - e);
+        for (int q = 0; q < cnt; ++q) {
+          float sum = 0.f;
+#pragma unroll
+          for (int k = 0; k < DPI; ++k) {
+            const float term = term_of<AVG>(GradT<float>::widen1(p.rep[k], cur.r0 + e + q), pre);
+            sum = k == 0 ? term : __fadd_rn(sum, term);
+          }
+          const float m = finish_store1<float, STATS>(p, cur.l0 + e + q,
+                                                      post_scaled<float>(instance_value<float, AVG>(sum, p.inv_dpi),
+                                                                         p.post_scale));
+          if (STATS) acc.add1(m);
+        }
+      }
+      if (STATS) acc.maybe_flush();
+      if (more) cur = nxt;
+    }
+  }
+  allow_dependent_launch();
+  if (STATS) {
+    write_partial(acc, p.partials);
+    finalize_if_last(p);
+  }
+}
+
 // ---------------------------------------------------------- K1 with TMA --
 //
 // The single-instance reduction with every replica tile staged through
@@ -864,15 +958,30 @@ int launch_k1_sel(K1Params& kp, const K1Launch& l, cudaStream_t s) {
   bool all_aligned = true;
   for (int k = 0; k < l.count; ++k) all_aligned &= seg_aligned(l.runs[k].local, l.runs[k].world);
   constexpr bool kTmaKind = DOPT_K1_TMA && STATS && std::is_same<GT, float>::value;
-  bool tma = kTmaKind && kp.error_flag && special && kp.n_inst == 1 && all_aligned;
-  if (tma) {
-    // a launch too short to give every CTA several bulk-copied tiles streams
-    // through registers instead: there the copy pipeline's fill and drain
-    // and the uneven last round of tiles cost more than the staging saves
+  // fp32 replicas of one instance in a launch too short to give every CTA
+  // several bulk-copied tiles stream through registers instead: there the
+  // copy pipeline's fill and drain and the uneven last round of tiles cost
+  // more than the staging saves
+  constexpr bool kF32 = std::is_same<GT, float>::value;
+  bool shrt = false;
+  if (kF32 && special && kp.n_inst == 1) {
     fill_table(kp.tab, l.runs, l.count, kTmaTile, l.bucket_base);
     int sms = 0;
     if (int st = device_sms(&sms)) return st;
-    tma = kp.tab.n_tiles >= kTmaMinTilesPerSm * sms;
+    shrt = kp.tab.n_tiles < kTmaMinTilesPerSm * sms;
+  }
+  const bool tma = kTmaKind && kp.error_flag && special && kp.n_inst == 1 && all_aligned && !shrt;
+  if constexpr (kF32 && !CHECK) {
+    if (shrt && DOPT_K1_SHORT_PIPE) {
+      fill_table(kp.tab, l.runs, l.count, kShortTile, l.bucket_base);
+      const char* w = "k1_reduce_prepare_short launch";
+      switch (dpi) {
+        case 1: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 1>, kp, s, w);
+        case 2: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 2>, kp, s, w);
+        case 4: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 4>, kp, s, w);
+        default: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 8>, kp, s, w);
+      }
+    }
   }
   const int tile = tma ? kTmaTile : special ? kThreads * kVec * kUnroll1 * GradT<GT>::kUnroll : kTile1;
   fill_table(kp.tab, l.runs, l.count, tile, l.bucket_base);

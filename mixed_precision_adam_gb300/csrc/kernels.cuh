@@ -55,6 +55,9 @@
 #ifndef DOPT_K1_MIN_BLOCKS
 #define DOPT_K1_MIN_BLOCKS 2
 #endif
+#ifndef DOPT_K1_SHORT_PIPE
+#define DOPT_K1_SHORT_PIPE 1  // 1: short fp32 single-instance reduces take the pipelined register kernel
+#endif
 #ifndef DOPT_K1N_FP32_MIN_BLOCKS
 #define DOPT_K1N_FP32_MIN_BLOCKS 4  // register-staged K1, up to 4 fp32 replicas of one instance
 #endif
@@ -87,6 +90,7 @@ constexpr int kTile1 = kThreads * kVec * kUnroll1;  // K1 elements per tile
 constexpr int kTile3 = kThreads * kVec * kUnroll3;  // K3 elements per tile
 constexpr int kTmaTile = DOPT_TMA_TILE;    // elements per tile of the TMA-staged K1
 constexpr int kTmaMinTilesPerSm = 16;      // shorter launches take the register-staged K1
+constexpr int kShortTile = kThreads * kVec;  // elements per tile of K1 for short fp32 launches
 static_assert(kTmaTile % (kThreads * kVec) == 0, "TMA tile");
 constexpr int kMaxSeg = 960;               // runs per launch (kernel-parameter table)
 constexpr int kMaxGrid = 1024;             // partial slots per launch region (CTAs per launch at most)
@@ -303,9 +307,11 @@ __host__ __device__ __forceinline__ double pow_int(double b, int64_t t) {
 // read past L1 (they may have been written by other SMs moments before).
 template <int NT>
 __device__ __forceinline__ void finalize_block(const FinalizeArgs& f) {
-  __shared__ double s_sum[NT];
-  __shared__ int s_bad[NT];
-  __shared__ long long s_zero[NT];
+  static_assert(NT % 32 == 0 && NT <= 1024, "whole warps");
+  constexpr int NW = NT / 32;
+  __shared__ double s_sum[NW];
+  __shared__ int s_bad[NW];
+  __shared__ long long s_zero[NW];
   double v[4] = {0.0, 0.0, 0.0, 0.0};
   int b = 0;
   long long z = 0;
@@ -320,22 +326,38 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f) {
     b |= (int)(fz & 0xFFFFFFFFll);
     z += (int)(fz >> 32);
   };
-  for (; i + 7 * NT < f.n_slots; i += 8 * NT) {
+  // the error flag, read with the slots rather than after the sum
+  const int err_early = (threadIdx.x == 0 && !f.local_sumsq) ? __ldcg(f.err_flag) : 0;
+  // every slot's load issued before any is summed (up to eight per thread
+  // per round; a short tail predicated rather than looped)
+  for (; i < f.n_slots; i += 8 * NT) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) take(i + q * NT, q & 3);
-  }
-  for (; i < f.n_slots; i += NT) take(i, 0);
-  s_sum[threadIdx.x] = (v[0] + v[1]) + (v[2] + v[3]);
-  s_bad[threadIdx.x] = b;
-  s_zero[threadIdx.x] = z;
-  __syncthreads();
-  for (int w = NT / 2; w > 0; w >>= 1) {
-    if ((int)threadIdx.x < w) {
-      s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
-      s_bad[threadIdx.x] |= s_bad[threadIdx.x + w];
-      s_zero[threadIdx.x] += s_zero[threadIdx.x + w];
+    for (int q = 0; q < 8; ++q) {
+      const int j = i + q * NT;
+      if (j < f.n_slots) take(j, q & 3);
     }
-    __syncthreads();
+  }
+  // a fixed tree: lanes by xor shuffles within each warp, then the warps'
+  // totals in warp order by thread 0 (one barrier instead of one per level)
+  double sum = (v[0] + v[1]) + (v[2] + v[3]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    b |= __shfl_xor_sync(0xFFFFFFFFu, b, o);
+    z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+  }
+  if (threadIdx.x % 32 == 0) {
+    s_sum[threadIdx.x / 32] = sum;
+    s_bad[threadIdx.x / 32] = b;
+    s_zero[threadIdx.x / 32] = z;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < NW; ++w) {
+      s_sum[0] += s_sum[w];
+      s_bad[0] |= s_bad[w];
+      s_zero[0] += s_zero[w];
+    }
   }
   if (f.local_sumsq) {  // local statistics only; the finalize comes later
     if (threadIdx.x == 0) {
@@ -345,7 +367,7 @@ __device__ __forceinline__ void finalize_block(const FinalizeArgs& f) {
     return;
   }
   if (threadIdx.x == 0) {
-    const int kernel_error = __ldcg(f.err_flag) == kErrorMagic ? 1 : 0;
+    const int kernel_error = err_early == kErrorMagic ? 1 : 0;
     *f.err_flag = 0;
     const double sumsq = f.d_global_sumsq ? __ldcg(f.d_global_sumsq) : s_sum[0] + f.remote_sumsq;
     const int remote_bad = f.d_global_sumsq ? (__ldcg(f.d_global_found) != 0) : (f.remote_found != 0);
