@@ -6,7 +6,7 @@ replica grads from the generator and stepping per param piece
 next to oracle.step on the whole shard, over several steps: every window
 element's main grad, master, m, v and param must be bit-identical, so the
 window's indexing (rank slots, bucket bases, buffer offsets, weight-decay
-groups) is right before it judges the GPU.  No GPU is involved.
+groups) is right before it is used to check the GPU.  No GPU is involved.
 """
 
 import numpy as np
