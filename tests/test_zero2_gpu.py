@@ -52,8 +52,9 @@ class Zero2Rank:
     def staging_bytes(self):
         return sum(t.numel() * t.element_size() for s in self.slots for ring in s for t in ring)
 
-    def step(self, grads, t):
-        """grads: the oracle's whole-buffer replica arrays.  Returns
+    def step(self, grads, t, grad_amax=None):
+        """grads: the oracle's whole-buffer replica arrays; grad_amax: a
+        device table for the pre-reduction grad check, or None.  Returns
         (found_inf, norm) of the step."""
         D = H.dopt()
         hc, dc = self.hc, self.dc
@@ -61,6 +62,8 @@ class Zero2Rank:
                  for r in reps] for reps in grads]
         args = dc.step_args([ring for ring in (s[0] for s in self.slots)], t)
         args.c.layout = D.LAYOUT_BUCKET
+        if grad_amax is not None:
+            args.set_grad_check(grad_amax)
         args.c.workspace, args.c.workspace_bytes = self.ws.data_ptr(), self.ws_bytes
         main = torch.cuda.current_stream()
         self.producer.wait_stream(main)
@@ -170,3 +173,35 @@ def test_zero2_rank_memory_equals_the_ledger(dp):
         torch.cuda.synchronize()
         free.append(torch.cuda.mem_get_info()[0])
     assert free[1] == free[2]  # after the first step (pinned copies, events) nothing more is held
+
+
+@pytest.mark.parametrize("name", ["llama_7b_dp8_rank0", "gpt2_small_dp8"])
+def test_zero2_streaming_grad_check(name):
+    """The pre-reduction grad check through the ZeRO-2 flow: each bucket's
+    staging buffers are checked as they are reduced, and the table (largest
+    |g| per replica and bucket among the elements the step reads) equals
+    the oracle's for whole buffers, with a large value and a NaN planted."""
+    cfg = dict(_cfg(name), inf_at=None)
+    hc = H.HostCase(cfg)
+    rank = Zero2Rank(hc)
+    D = H.dopt()
+    total = D.dopt_total_buckets(hc.pm)
+    sites = H.plant_sites(hc)
+    report = []
+    for step, plants in ((1, [(0, 1, 1.0e3)]), (2, [(len(sites) // 2, hc.n_rep - 1, float("nan"))])):
+        grads = hc.grads(step)
+        for site, k, value in plants:
+            bi, w = sites[site]
+            H.plant(hc, grads, bi, k, w, value)
+        t = hc.t_applied + 1
+        before = H.snapshot(hc)
+        ores = H.oracle.step(hc.om, hc.ranks, grads, hc.state, hc.params, cfg["hp"], t,
+                             inv_scale=float(np.float32(1.0 / cfg["loss_scale"])), max_norm=cfg["max_norm"],
+                             layout="full", n_inst=cfg["n_inst"], average=cfg["average"], check_grads=True)
+        amax = torch.full((hc.n_rep, total), 12345.0, dtype=torch.float32, device="cuda")
+        found, norm = rank.step(grads, t, grad_amax=amax)
+        assert H.amax_equal(amax.cpu().numpy(), ores["grad_amax"]), (step, amax.cpu().numpy(), ores["grad_amax"])
+        assert H.compare_step(hc, rank.dc, ores, found, norm, before, report, ws=rank.ws), "\n".join(report)
+        assert found == (step == 2)
+        if not found:
+            hc.t_applied += 1
