@@ -5,12 +5,15 @@ over every step the workloads configure.
 The oracle cannot hold these inputs, so each step it checks:
   - found_inf exactly, and the grad norm against the oracle's own fp64 sum
     of squares streamed from the generator over every element (rel 1e-5);
-  - a window of whole buckets element by element (at least 64M elements:
-    the first, middle and last bucket of the 16-bit buffer, more buckets
-    from both ends, and every bucket of the fp32 norm-weight buffer), whose
-    main grads the oracle redraws from the generator and whose master, m
-    and v it carries from step to step: main grad bit-exact, master/m/v
-    within 4 ulp or 1e-6 of the operand scale, 16-bit params within 1 ulp;
+  - every element of the shard for the bench workload (Llama-7B DP=8) and
+    Llama-1.3B fp16 (and for two steps of the 2 x 8 hierarchy at its 40M
+    bucket size), and elsewhere a window of whole buckets (at least 64M
+    elements: the first, middle and last bucket of the 16-bit buffer, more
+    buckets from both ends, and every bucket of the fp32 norm-weight
+    buffer), element by element: the oracle redraws the main grads from the
+    generator and carries master, m and v from step to step; main grad
+    bit-exact, master/m/v within 4 ulp or 1e-6 of the operand scale, 16-bit
+    params within 1 ulp;
   - thousands of sampled elements elsewhere -- the first and last element of
     every param piece plus random ones -- recomputed from their replica
     grads at the same tolerances.
@@ -55,17 +58,25 @@ def _inf_position(fc):
     return best
 
 
-def _run(cfg, steps, n_random=3000, window=True):
+def _run(cfg, steps, n_random=3000, window=True, every=False):
+    """Steps a workload at full size.  window: compare a window of whole
+    buckets element by element (every: the window is the whole shard);
+    always: found_inf, the streamed norm and sampled elements."""
     if STEP_CAP is not None:
         steps = min(steps, STEP_CAP)
     fc = H.FullCase(cfg)
     samples = fc.choose_samples(n_random)
     st = fc.initial_sample_state(samples)
     if window:
-        wp = fc.window_pieces(fc.window_buckets())
+        if every:
+            buckets = [(bi, b) for bi, buf in enumerate(fc.om.buffers) for b in range(len(buf.buckets))]
+        else:
+            buckets = fc.window_buckets()
+        wp = fc.window_pieces(buckets)
         wst = fc.window_initial_state(wp)
-        assert sum(wst[bi]["master"].size for bi in wst) >= min(64 << 20, sum(
-            len(fc.ranks) * fc.om.shard_numel(bi) for bi in range(len(fc.om.buffers))) // 2)
+        n_win = sum(wst[bi]["master"].size for bi in wst)
+        n_pieces = sum(n for *_, n in fc.pieces())
+        assert n_win == n_pieces if every else n_win >= min(64 << 20, n_pieces // 2)
     t_applied = 0
     L = oracle.lib()
     for t_step in range(1, steps + 1):
@@ -76,7 +87,8 @@ def _run(cfg, steps, n_random=3000, window=True):
             assert cfg["layout"] == "full"
             fc.reps[0][spec["replica"]][_inf_position(fc)] = INF_BITS[fc.om.buffers[0].grad_dtype]
         before_dev = fc.device_samples(st)
-        before_win = fc.window_device(wp) if (inject and window) else None
+        before_win = [fc.window_device(sub) for sub, _ in H.window_chunks(wp, wst, 64 << 20)] \
+            if (inject and window) else None
         t = t_applied + 1
         found, norm = fc.step(t)
         if inject:
@@ -86,10 +98,11 @@ def _run(cfg, steps, n_random=3000, window=True):
                 for k in STATE + ("param",):
                     assert after[bi][k].tobytes() == before_dev[bi][k].tobytes(), (bi, k)
             if window:
-                after_win = fc.window_device(wp)
-                for bi in after_win:
-                    for k in STATE + ("param",):
-                        assert after_win[bi][k].tobytes() == before_win[bi][k].tobytes(), (bi, k)
+                for (sub, _), bw in zip(H.window_chunks(wp, wst, 64 << 20), before_win):
+                    aw = fc.window_device(sub)
+                    for bi in aw:
+                        for k in STATE + ("param",):
+                            assert aw[bi][k].tobytes() == bw[bi][k].tobytes(), (bi, k)
             continue
         sumsq, bad = fc.oracle_sumsq(t_step)
         assert bad == 0 and not found
@@ -109,20 +122,24 @@ def _run(cfg, steps, n_random=3000, window=True):
             if s["param"].dtype == np.uint16:
                 assert H.ulp16(g["param"], s["param"]).max() <= 1, (t_step, bi)
         if window:
-            wprev = {bi: {k: wst[bi][k].copy() for k in STATE} for bi in wst}
-            res, wbad = fc.window_oracle_step(wp, wst, t_step, t, coef.value, clip)
-            assert wbad == 0
-            want = {bi: dict(wst[bi], main=res[bi]["main"], param=res[bi]["param"]) for bi in wst}
-            findings = H.window_compare(fc.window_device(wp), want, wprev)
-            assert not findings, (t_step, findings[:10])
+            # a group of whole param pieces at a time: oracle, device, compare
+            for sub, views in H.window_chunks(wp, wst, 64 << 20):
+                wprev = {bi: {k: views[bi][k].copy() for k in STATE} for bi in views}
+                res, wbad = fc.window_oracle_step(sub, views, t_step, t, coef.value, clip)
+                assert wbad == 0
+                want = {bi: dict(views[bi], main=res[bi]["main"], param=res[bi]["param"]) for bi in views}
+                findings = H.window_compare(fc.window_device(sub), want, wprev)
+                assert not findings, (t_step, findings[:10])
         t_applied += 1
     del fc
     torch.cuda.empty_cache()
 
 
 def test_bench_workload_llama7b_dp8_rank0():
+    # every element of the shard (842,301,952), every configured step; the
+    # oracle carries master, m and v of all of them (about 10 GB of host memory)
     cfg = W.config("llama_7b_dp8_rank0")
-    _run(cfg, steps=cfg["steps"])
+    _run(cfg, steps=cfg["steps"], every=True)
 
 
 @pytest.mark.parametrize("size", ["1m", "10m", "40m", "100m"])
@@ -130,6 +147,8 @@ def test_hierarchical_llama7b_dp16_2x8(size):
     # 2 instances x 8 ranks, every bucket size of the sweep, all steps
     cfg = W.config("llama_7b_dp16_2x8_" + size)
     _run(cfg, steps=cfg["steps"])
+    if size == "40m":  # and the whole shard for two steps
+        _run(cfg, steps=2, n_random=0, every=True)
 
 
 def test_average_in_collective_llama7b_dp8_rank0():
@@ -147,8 +166,9 @@ def test_gpt2_small_all_ranks_with_skipped_step():
 
 
 def test_llama_1p3b_fp16_loss_scaled():
+    # every element of all 8 ranks' shards (1,345,423,360), every step
     cfg = W.config("llama_1p3b_fp16_dp8")
-    _run(cfg, steps=cfg["steps"])
+    _run(cfg, steps=cfg["steps"], every=True)
 
 
 def test_bf16_replica_grads_fp32_accumulation():
