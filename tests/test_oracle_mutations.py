@@ -65,6 +65,11 @@ MUTANTS = [
      "static int or_is_finite(float x) { return x == x; }", "infinity counted finite"),
     (PY, "zeros += int(np.count_nonzero(main[local:local + n] == 0))",
      "zeros += int(np.count_nonzero(main[local:local + n]))", "count_zeros counts nonzeros"),
+    # the generator-streamed form of A2 + A3 (full-size checks)
+    (C, "                                    grad_scale, gdt) * inv_scale;\n      main_out[j] = mg;",
+     "                                    grad_scale, gdt);\n      main_out[j] = mg;", "streamed main grads not unscaled"),
+    (C, "      main_out[j] = mg;\n      if (!or_is_finite(mg)) ++bad;", "      main_out[j] = mg;",
+     "streamed form counts no non-finite main grad"),
     # casts and widening
     (C, "if (rem > 0x8000u || (rem == 0x8000u && (kept & 1u))) kept += 1u;", "if (rem >= 0x8000u) kept += 1u;",
      "bf16 ties away from zero"),

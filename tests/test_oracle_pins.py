@@ -719,6 +719,14 @@ def test_stream_sumsq_equals_array_path():
             got, gbad = oracle.stream_reduce_prepare(keys, gdt, synth.factor(1e-3), 1234, 5000,
                                                      inv_scale=0.5, n_inst=n_inst, average=avg)
             assert gbad == wbad == 0 and got.tobytes() == want.tobytes()
+    # and their count of non-finite main grads: two unit-variance fp32
+    # replicas averaged, unscaled by 3e38, overflow wherever the reduced
+    # grad exceeds about 1.13 in magnitude
+    reps = [synth.normal(5000, k, 77, 1.0) for k in keys[:2]]
+    want, wbad = oracle.reduce_prepare(reps, F32, 0, 5000, 3e38)
+    got, gbad = oracle.stream_reduce_prepare(keys[:2], F32, synth.factor(1.0), 77, 5000, inv_scale=3e38)
+    assert gbad == wbad == int(np.count_nonzero(~np.isfinite(want))) > 0
+    assert np.array_equal(np.isfinite(got), np.isfinite(want))
 
 
 # --------------------------------------------------------------------------
