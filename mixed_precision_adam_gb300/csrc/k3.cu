@@ -8,7 +8,6 @@
 // check each tile against the extents of the main grad, master/m/v and the
 // param buffer and skip a tile outside them.
 #include "kernels.cuh"
-#include "tma.cuh"
 
 namespace dopt {
 
@@ -249,100 +248,10 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
   }
 }
 
-#if DOPT_K3_BULK_STORE
-// The same pass with the results of each tile staged in shared memory and
-// written by bulk copies (one per array, issued by thread 0), so the stores
-// leave the SM as a few long contiguous writes instead of one 16-byte store
-// per thread and array.  Two stages: a stage is rewritten only after the
-// bulk copies of the tile before last have finished reading it.  The part of
-// a tile past its last multiple of 8 elements, and runs that are not
-// 8-element aligned, are stored by the threads as in k3_adamw_pipe.
-template <typename PT>
-struct K3Stage {
-  float w[kTile3], m[kTile3], v[kTile3];
-  unsigned short p[ParamT<PT>::kInPlace ? 8 : kTile3];  // 16-bit params (none in place)
-};
-
-template <typename PT, typename MG>
-__global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_bulk(const __grid_constant__ K3Params p) {
-  wait_for_prior_grids();    // the reduce pass and its finalize are done
-  if (*p.found_inf) return;  // skipped step: nothing is written
-  __shared__ __align__(128) K3Stage<PT> stage[2];
-  const float c = *p.coef;
-  const StepScalars ss = step_scalars(p);
-  float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
-  int si = 0, decay_si = -1;
-  float decay = 1.f;
-  int t = blockIdx.x;
-  if (t >= p.tab.n_tiles) return;
-  K3Tile<MG> cur;
-  k3_load<PT, MG>(p, wbase, t, si, cur, decay_si, decay, ss.lr_wd);
-  for (int it = 0; t < p.tab.n_tiles; t += gridDim.x, ++it) {
-    K3Tile<MG> nxt;
-    const bool more = t + (int)gridDim.x < p.tab.n_tiles;
-    if (more) k3_load<PT, MG>(p, wbase, t + gridDim.x, si, nxt, decay_si, decay, ss.lr_wd);
-    K3Stage<PT>& sb = stage[it & 1];
-    const int nv = cur.aligned ? (cur.n & ~7) : 0;  // elements the bulk copies write
-    if (threadIdx.x == 0) bulk_wait_read<1>();  // this stage's copies of two tiles ago are done
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kUnroll3; ++u) {
-      const int e = (u * kThreads + threadIdx.x) * kVec;
-      if (cur.aligned && e + kVec <= cur.n) {
-        float g[kVec];
-        MainT<MG>::widen4(cur.g[u], p.inv_scale, g);
-        float w[kVec] = {cur.w[u].x, cur.w[u].y, cur.w[u].z, cur.w[u].w};
-        float m[kVec] = {cur.m[u].x, cur.m[u].y, cur.m[u].z, cur.m[u].w};
-        float v[kVec] = {cur.v[u].x, cur.v[u].y, cur.v[u].z, cur.v[u].w};
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) adamw1(__fmul_rn(g[j], c), cur.decay, p, ss, w[j], m[j], v[j]);
-        if (e + kVec <= nv) {
-          *reinterpret_cast<float4*>(sb.w + e) = make_float4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<float4*>(sb.m + e) = make_float4(m[0], m[1], m[2], m[3]);
-          *reinterpret_cast<float4*>(sb.v + e) = make_float4(v[0], v[1], v[2], v[3]);
-          if (!ParamT<PT>::kInPlace) *reinterpret_cast<uint2*>(sb.p + e) = ParamT<PT>::pack4(w);
-        } else {
-          __stcs(reinterpret_cast<float4*>(wbase + cur.m0 + e), make_float4(w[0], w[1], w[2], w[3]));
-          __stcs(reinterpret_cast<float4*>(p.exp_avg + cur.l0 + e), make_float4(m[0], m[1], m[2], m[3]));
-          __stcs(reinterpret_cast<float4*>(p.exp_avg_sq + cur.l0 + e), make_float4(v[0], v[1], v[2], v[3]));
-          ParamT<PT>::store4(p.param, cur.w0 + e, w);
-        }
-      } else if (e < cur.n) {
-        const int cnt = min(kVec, cur.n - e);
-        for (int j = 0; j < cnt; ++j) {
-          float ww = wbase[cur.m0 + e + j], mm = p.exp_avg[cur.l0 + e + j], vv = p.exp_avg_sq[cur.l0 + e + j];
-          adamw1(__fmul_rn(MainT<MG>::load1(p.main_grad, cur.l0 + e + j, p.inv_scale), c), cur.decay, p, ss,
-                 ww, mm, vv);
-          wbase[cur.m0 + e + j] = ww;
-          p.exp_avg[cur.l0 + e + j] = mm;
-          p.exp_avg_sq[cur.l0 + e + j] = vv;
-          ParamT<PT>::store1(p.param, cur.w0 + e + j, ww);
-        }
-      }
-    }
-    fence_proxy_async();  // this thread's stage writes, before the bulk copies read them
-    __syncthreads();
-    if (threadIdx.x == 0 && nv > 0) {
-      bulk_store(wbase + cur.m0, sb.w, (unsigned)nv * 4u);
-      bulk_store(p.exp_avg + cur.l0, sb.m, (unsigned)nv * 4u);
-      bulk_store(p.exp_avg_sq + cur.l0, sb.v, (unsigned)nv * 4u);
-      if (!ParamT<PT>::kInPlace)
-        bulk_store(static_cast<unsigned short*>(p.param) + cur.w0, sb.p, (unsigned)nv * 2u);
-      bulk_commit();
-    }
-    if (more) cur = nxt;
-  }
-  if (threadIdx.x == 0) bulk_wait<0>();  // the stages stay valid until the last copies are done
-}
-#endif
 
 template <typename PT, typename MG>
 int launch_k3_t(K3Params& kp, cudaStream_t s) {
-#if DOPT_K3_BULK_STORE
-  auto kern = k3_adamw_bulk<PT, MG>;
-#else
   auto kern = k3_adamw_pipe<PT, MG>;
-#endif
   int grid = 0;
   int st = grid_for(kern, kp.tab.n_tiles, &grid);
   if (st) return st;

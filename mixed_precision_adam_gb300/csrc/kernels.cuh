@@ -73,9 +73,6 @@
 #ifndef DOPT_K3_STORE_HINT
 #define DOPT_K3_STORE_HINT 0  // the AdamW pass's stores: 0 streaming, 1 L2 only, 2 write-back
 #endif
-#ifndef DOPT_K3_BULK_STORE
-#define DOPT_K3_BULK_STORE 0  // 1: the AdamW pass stages its results in shared memory and writes them with bulk copies
-#endif
 #ifndef DOPT_BOUNDS_CHECK
 #define DOPT_BOUNDS_CHECK 0  // 1: debug build; every tile is checked against the extents of its buffers
 #endif
@@ -232,7 +229,7 @@ struct K1Params {
   int32_t starve_tile;  // test hook: CTA 0 never copies its tile of this index (-1: off)
 #endif
   int32_t compact;      // 16-bit grads, statistics pass: store the reduced grads in the
-                        // grad dtype instead of the fp32 main grads (see store_main4)
+                        // grad dtype instead of the fp32 main grads (see finish_store4)
   int32_t keep_main;    // fp32 main grads stored without the evict-first hint, to be
                         // read back from L2 (steps whose main grads fit L2 easily)
   // grad check (CHECK kernels only): amax[k * amax_stride + bucket] gathers

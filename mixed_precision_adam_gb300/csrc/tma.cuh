@@ -65,29 +65,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
   }
 }
 
-// 1-D bulk copy from shared to global memory (16-byte aligned addresses, a
-// multiple of 16 bytes), in the issuing thread's current bulk group.  The
-// writes to shared memory it reads must be ordered before it by
-// fence_proxy_async() in every writing thread and a barrier.
-__device__ __forceinline__ void bulk_store(void* dst, const void* src, unsigned bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                   (unsigned long long)__cvta_generic_to_global(dst)),
-               "r"(smem_addr(src)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until at most N of the thread's bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Waits until at most N of the thread's bulk groups are incomplete.
-template <int N>
-__device__ __forceinline__ void bulk_wait() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
 // Raises a kernel's dynamic shared-memory limit once per device (a later
 // call, e.g. inside a stream capture, then issues nothing but the launch);
 // `done` is one bit per device, owned by the caller per kernel.
