@@ -6,8 +6,8 @@ The oracle cannot hold these inputs, so each step it checks:
   - found_inf exactly, and the grad norm against the oracle's own fp64 sum
     of squares streamed from the generator over every element (rel 1e-5);
   - every element of the shard for the bench workload (Llama-7B DP=8) and
-    Llama-1.3B fp16 (and for two steps of the 2 x 8 hierarchy at its 40M
-    bucket size), and elsewhere a window of whole buckets (at least 64M
+    Llama-1.3B fp16 (and for two steps of the 2 x 8 hierarchy at each bucket
+    size), and elsewhere a window of whole buckets (at least 64M
     elements: the first, middle and last bucket of the 16-bit buffer, more
     buckets from both ends, and every bucket of the fp32 norm-weight
     buffer), element by element: the oracle redraws the main grads from the
@@ -147,8 +147,7 @@ def test_hierarchical_llama7b_dp16_2x8(size):
     # 2 instances x 8 ranks, every bucket size of the sweep, all steps
     cfg = W.config("llama_7b_dp16_2x8_" + size)
     _run(cfg, steps=cfg["steps"])
-    if size == "40m":  # and the whole shard for two steps
-        _run(cfg, steps=2, n_random=0, every=True)
+    _run(cfg, steps=2, n_random=0, every=True)  # and the whole shard for two steps
 
 
 def test_average_in_collective_llama7b_dp8_rank0():
