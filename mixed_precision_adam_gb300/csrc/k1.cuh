@@ -173,7 +173,7 @@ struct GradT<__half> {
 // amax[k * stride + bucket] (fp32 bits of |g|; an atomic max, so the
 // result does not depend on the order of the CTAs).  Called by whole warps.
 template <typename GT>
-__device__ __forceinline__ void amax_flush(uint32_t bits, const K1Params& p, int k, int bucket) {
+__device__ __forceinline__ void amax_flush(uint32_t bits, const K1Head& p, int k, int bucket) {
   const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, GradT<GT>::f32_bits(bits));
   if ((threadIdx.x & 31) == 0 && v != 0u) atomicMax(p.amax + (size_t)k * p.amax_stride + bucket, v);
 }
@@ -201,7 +201,7 @@ __device__ __forceinline__ ReplicaPos replica_pos(int k, int dpi) {
 
 template <typename GT>
 __device__ __forceinline__ void reduce_term(ReduceState& st, float x, ReplicaPos rp,
-                                            const K1Params& p) {
+                                            const K1Head& p) {
   float term = p.average ? x : __fmul_rn(x, p.pre);
   st.s = rp.opens ? term : __fadd_rn(st.s, term);
   if (rp.closes) {
@@ -241,7 +241,7 @@ __device__ __forceinline__ float across_instances(float t, float inv_ninst) {
 // The reduced grad of an element in the grad dtype, after scale_gradients
 // (before the unscale that makes it the fp32 main grad).
 template <typename GT>
-__device__ __forceinline__ float reduce_value(const ReduceState& st, const K1Params& p) {
+__device__ __forceinline__ float reduce_value(const ReduceState& st, const K1Head& p) {
   float total = st.total;
   if (p.n_inst > 1) {
     if (p.average) total = __fmul_rn(total, p.inv_ninst);
@@ -255,7 +255,7 @@ __device__ __forceinline__ float reduce_value(const ReduceState& st, const K1Par
 // compact form, stores the reduced grads themselves in the grad dtype first
 // (half the bytes; the AdamW pass forms the same main grads from them).
 template <typename GT, bool STATS>
-__device__ __forceinline__ void finish_store4(const K1Params& p, int64_t i, float* v) {
+__device__ __forceinline__ void finish_store4(const K1Head& p, int64_t i, float* v) {
   if constexpr (STATS && GradT<GT>::kCompact) {
     if (p.compact) {
       GradT<GT>::store4c(p.main_grad, i, v);
@@ -272,7 +272,7 @@ __device__ __forceinline__ void finish_store4(const K1Params& p, int64_t i, floa
     __stcs(reinterpret_cast<float4*>(p.main_grad + i), make_float4(v[0], v[1], v[2], v[3]));
 }
 template <typename GT, bool STATS>
-__device__ __forceinline__ float finish_store1(const K1Params& p, int64_t i, float r) {
+__device__ __forceinline__ float finish_store1(const K1Head& p, int64_t i, float r) {
   const float m = __fmul_rn(r, p.inv_scale);
   if constexpr (STATS && GradT<GT>::kCompact) {
     if (p.compact) {
@@ -669,8 +669,8 @@ struct ShortTile {
   bool aligned;
 };
 
-template <bool FULL, int DPI>
-__device__ __forceinline__ void short_load(const K1Params& p, int& si, int t, ShortTile<DPI>& T) {
+template <bool FULL, int DPI, typename P>
+__device__ __forceinline__ void short_load(const P& p, int& si, int t, ShortTile<DPI>& T) {
   si = seek(p.tab, si, t);
   const Seg& sg = p.tab.seg[si];
   const int64_t off = (int64_t)(t - sg.tile0) * kShortTile;
@@ -692,9 +692,9 @@ constexpr int k1s_min_blocks() {
   return DPI <= 4 ? 4 : 2;
 }
 
-template <bool FULL, bool STATS, bool AVG, int DPI>
+template <bool FULL, bool STATS, bool AVG, int DPI, int CAP = kMaxSeg>
 __global__ void __launch_bounds__(kThreads, (k1s_min_blocks<DPI>()))
-k1_reduce_prepare_short(const __grid_constant__ K1Params p) {
+k1_reduce_prepare_short(const __grid_constant__ K1ParamsT<CAP> p) {
   SumSq acc;
   const float pre = p.pre;
   int si = 0;
@@ -920,8 +920,8 @@ __global__ void __launch_bounds__(kThreads, 1) k1_reduce_prepare_tma(const __gri
 
 // ------------------------------------------------------------ launchers --
 
-template <typename K>
-int launch_plain(K kern, const K1Params& kp, cudaStream_t s, const char* what) {
+template <typename K, typename P>
+int launch_plain(K kern, const P& kp, cudaStream_t s, const char* what) {
   int grid = 0;
   int st = grid_for(kern, kp.tab.n_tiles, &grid);
   if (st) return st;
@@ -975,6 +975,17 @@ int launch_k1_sel(K1Params& kp, const K1Launch& l, cudaStream_t s) {
     if (shrt && DOPT_K1_SHORT_PIPE) {
       fill_table(kp.tab, l.runs, l.count, kShortTile, l.bucket_base);
       const char* w = "k1_reduce_prepare_short launch";
+      if constexpr (STATS) {  // the steps' statistics pass: the compact parameter block when it fits
+        if (kp.tab.n_seg <= kSmallSeg) {
+          const K1ParamsT<kSmallSeg> sp = with_table_of<kSmallSeg, K1Head>(kp);
+          switch (dpi) {
+            case 1: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 1, kSmallSeg>, sp, s, w);
+            case 2: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 2, kSmallSeg>, sp, s, w);
+            case 4: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 4, kSmallSeg>, sp, s, w);
+            default: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 8, kSmallSeg>, sp, s, w);
+          }
+        }
+      }
       switch (dpi) {
         case 1: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 1>, kp, s, w);
         case 2: return launch_plain(k1_reduce_prepare_short<FULL, STATS, AVG, 2>, kp, s, w);

@@ -132,7 +132,7 @@ struct StepScalars {
   double lr_wd;
 };
 
-__device__ __forceinline__ StepScalars step_scalars(const K3Params& p) {
+__device__ __forceinline__ StepScalars step_scalars(const K3Head& p) {
   if (p.dev) return StepScalars{p.dev->step_size, p.dev->bc2_sqrt, p.dev->lr_wd};
   return StepScalars{p.step_size, p.bc2_sqrt, p.lr_wd};
 }
@@ -140,7 +140,7 @@ __device__ __forceinline__ StepScalars step_scalars(const K3Params& p) {
 // One element of AdamW (torch semantics: decay the weight, update m and v,
 // divide the bias-corrected sqrt(v) + eps into m, step), each operation
 // rounded once in fp32.
-__device__ __forceinline__ void adamw1(float g, float decay, const K3Params& p, const StepScalars& ss,
+__device__ __forceinline__ void adamw1(float g, float decay, const K3Head& p, const StepScalars& ss,
                                        float& w, float& m, float& v) {
   float pp = __fmul_rn(w, decay);
   float mm = __fadd_rn(__fmul_rn(p.b1, m), __fmul_rn(p.omb1, g));
@@ -165,8 +165,8 @@ struct K3Tile {
   bool aligned;
 };
 
-template <typename PT, typename MG>
-__device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, int& si, K3Tile<MG>& T,
+template <typename PT, typename MG, typename P>
+__device__ __forceinline__ void k3_load(const P& p, float* wbase, int t, int& si, K3Tile<MG>& T,
                                         int& decay_si, float& decay, double lr_wd) {
   si = seek(p.tab, si, t);
   const Seg& sg = p.tab.seg[si];
@@ -199,8 +199,8 @@ __device__ __forceinline__ void k3_load(const K3Params& p, float* wbase, int t, 
   }
 }
 
-template <typename PT, typename MG>
-__global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(const __grid_constant__ K3Params p) {
+template <typename PT, typename MG, int CAP>
+__global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(const __grid_constant__ K3ParamsT<CAP> p) {
   wait_for_prior_grids();    // the reduce pass and its finalize are done
   if (*p.found_inf) return;  // skipped step: nothing is written
   const float c = *p.coef;
@@ -249,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(co
 }
 
 
-template <typename PT, typename MG>
-int launch_k3_t(K3Params& kp, cudaStream_t s) {
-  auto kern = k3_adamw_pipe<PT, MG>;
+template <typename PT, typename MG, int CAP>
+int launch_k3_cap(const K3ParamsT<CAP>& kp, cudaStream_t s) {
+  auto kern = k3_adamw_pipe<PT, MG, CAP>;
   int grid = 0;
   int st = grid_for(kern, kp.tab.n_tiles, &grid);
   if (st) return st;
@@ -273,6 +273,13 @@ int launch_k3_t(K3Params& kp, cudaStream_t s) {
     return fail(DOPT_E_CUDA, std::string("k3_adamw launch: ") + cudaGetErrorString(e));
   }
   return check_launch("k3_adamw launch");
+}
+
+// With the compact parameter block when the launch's runs fit in it.
+template <typename PT, typename MG>
+int launch_k3_t(const K3Params& kp, cudaStream_t s) {
+  if (kp.tab.n_seg <= kSmallSeg) return launch_k3_cap<PT, MG, kSmallSeg>(with_table_of<kSmallSeg, K3Head>(kp), s);
+  return launch_k3_cap<PT, MG, kMaxSeg>(kp, s);
 }
 
 // Param and grad dtypes pair up as the buffers allow: a 16-bit param buffer

@@ -112,11 +112,19 @@ struct Seg {
 };
 static_assert(sizeof(Seg) == 32, "Seg layout");
 
-struct SegTable {
+// A launch's run table, held in the kernel's parameter block.  The GPU
+// copies the whole block at every launch, so a launch whose runs fit in
+// kSmallSeg entries takes a kernel compiled for that table (about 2 KB of
+// parameters instead of about 31 KB): about a microsecond less per launch,
+// which short steps notice.
+template <int CAP>
+struct SegTableT {
   int32_t n_seg;
   int32_t n_tiles;
-  Seg seg[kMaxSeg];
+  Seg seg[CAP];
 };
+using SegTable = SegTableT<kMaxSeg>;
+constexpr int kSmallSeg = 32;
 
 struct Partial {
   double sumsq;
@@ -213,7 +221,8 @@ __device__ __forceinline__ bool range_ok(const Extents& x, int site, int64_t lo,
 #define DOPT_RANGE_OK(params, site, lo, n, field) true
 #endif
 
-struct K1Params {
+// A reduce launch's parameters: K1Head, then its run table.
+struct K1Head {
   const void* rep[DOPT_MAX_REPLICAS];
   float* main_grad;
   Partial* partials;  // this launch's region of kMaxGrid slots (STATS only)
@@ -243,10 +252,15 @@ struct K1Params {
 #if DOPT_BOUNDS_CHECK
   Extents ext;
 #endif
-  SegTable tab;
 };
+template <int CAP>
+struct K1ParamsT : K1Head {
+  SegTableT<CAP> tab;
+};
+using K1Params = K1ParamsT<kMaxSeg>;
 
-struct K3Params {
+// An AdamW launch's parameters: K3Head, then its run table.
+struct K3Head {
   const float* main_grad;
   float* master;      // flat shard, or NULL when the param buffer is the master
   float* exp_avg;
@@ -261,10 +275,27 @@ struct K3Params {
 #if DOPT_BOUNDS_CHECK
   Extents ext;
 #endif
-  SegTable tab;
 };
+template <int CAP>
+struct K3ParamsT : K3Head {
+  SegTableT<CAP> tab;
+};
+using K3Params = K3ParamsT<kMaxSeg>;
 
 static_assert(sizeof(K1Params) <= 32764 && sizeof(K3Params) <= 32764, "kernel parameter limit");
+static_assert(sizeof(K1ParamsT<kSmallSeg>) <= 4096 && sizeof(K3ParamsT<kSmallSeg>) <= 4096, "compact parameters");
+
+// The same launch parameters with a run table of CAP entries; the table's
+// runs must fit (n_seg <= CAP).
+template <int CAP, typename Head, template <int> class ParamsT>
+ParamsT<CAP> with_table_of(const ParamsT<kMaxSeg>& big) {
+  ParamsT<CAP> out{};
+  static_cast<Head&>(out) = static_cast<const Head&>(big);
+  out.tab.n_seg = big.tab.n_seg;
+  out.tab.n_tiles = big.tab.n_tiles;
+  for (int i = 0; i < big.tab.n_seg; ++i) out.tab.seg[i] = big.tab.seg[i];
+  return out;
+}
 
 // Programmatic dependent launch.  A reduce kernel lets the kernel after it
 // in the stream start its CTAs once every reduce CTA has finished its tiles
@@ -280,7 +311,8 @@ __device__ __forceinline__ void wait_for_prior_grids() { asm volatile("griddepco
 
 // Advances the run cursor of a CTA to the run holding tile t (tiles visited
 // in increasing order, so the cursor only moves forward).
-__device__ __forceinline__ int seek(const SegTable& tab, int si, int t) {
+template <typename Tab>
+__device__ __forceinline__ int seek(const Tab& tab, int si, int t) {
   while (si + 1 < tab.n_seg && tab.seg[si + 1].tile0 <= t) ++si;
   return si;
 }
@@ -412,7 +444,7 @@ static __device__ __noinline__ void finalize_call(const FinalizeArgs& f) { final
 // is written (by thread 0): with a ticket counter set, the last CTA to take
 // a ticket runs the finalize and returns the counter to zero for the next
 // step.  No CTA waits for another.
-__device__ __forceinline__ void finalize_if_last(const K1Params& p) {
+__device__ __forceinline__ void finalize_if_last(const K1Head& p) {
   if (!p.fin_counter) return;
   __shared__ int s_last;
   if (threadIdx.x == 0) {
