@@ -77,6 +77,17 @@ def test_many_runs_chunked_launches():
     _check(_tiny(params, 1, bucket_size=None, steps=2))
 
 
+@pytest.mark.parametrize("n_runs", [31, 32, 33])
+@pytest.mark.parametrize("grad_fp32", [True, False])
+def test_run_table_capacity_boundary(n_runs, grad_fp32):
+    # a launch of at most 32 runs takes the kernels built for a 32-entry
+    # parameter table (the short-launch reduce with fp32 grads, the AdamW
+    # pass), a longer one the full table: one rank and one bucket, with
+    # alternating wd_mult so that every param is a run of its own
+    params = [dict(numel=1000 + 37 * i, dtype=1, wd_mult=float(i % 2)) for i in range(n_runs)]
+    _check(_tiny(params, 1, bucket_size=None, grad_reduce_in_fp32=grad_fp32, grad_sigma=1e-2))
+
+
 def test_average_in_collective_and_hierarchy():
     params = W.llama(1, 128, 344, 257)
     _check(_tiny(params, 4, bucket_size=20000, average=True, steps=2))
