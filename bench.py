@@ -641,10 +641,10 @@ def run_ours(args):
     # write a buffer of twice the L2 size between the timed steps and time
     # each step from its own first to last stage event, so the flushes stay
     # outside the timed work.  The step is timed as a caller runs it, with
-    # events before and after it only: an event recorded between the reduce
-    # pass and the AdamW pass waits for the reduce grid to drain and stops
-    # the AdamW CTAs from starting early (about 7 us a step on the toy MLP,
-    # within the noise of the larger steps).  The per-pass durations come
+    # events before and after it only: a timing event recorded between the
+    # reduce pass and the AdamW pass waits for the reduce grid to drain and
+    # stops the AdamW CTAs from starting early (about 6 us a step on the toy
+    # MLP, within the noise of the larger steps).  The per-pass durations come
     # from a second region of the same steps with all four stage events.
     l2_bytes = torch.cuda.get_device_properties(local_rank).L2_cache_size
     rep_bytes = sum(r.numel() * r.element_size() for reps in wl.reps for r in reps)

@@ -425,6 +425,9 @@ struct K3Job {
   const float* d_coef = nullptr;
   const int32_t* d_found = nullptr;
   const DevStep* dev = nullptr;   // device step scalars, or NULL: from hp
+  // the launch before this pass is a kernel of the same step that writes
+  // none of its master, m and v (K3Head::early_state)
+  bool early_state = false;
   int64_t ext_main = 0, ext_state = 0, ext_param = 0;  // element extents (debug builds check them)
 };
 
@@ -450,6 +453,7 @@ int run_k3_runs(const std::vector<Run>& runs, const K3Job& j, cudaStream_t s) {
     kp.step_size = (float)(hp->lr / (1.0 - pow_int(hp->beta1, hp->step)));
     kp.bc2_sqrt = (float)std::sqrt(1.0 - pow_int(hp->beta2, hp->step));
     kp.inv_scale = j.inv_scale;
+    kp.early_state = j.early_state ? 1 : 0;
 #if DOPT_BOUNDS_CHECK
     kp.ext = Extents{0, j.ext_main, j.ext_state, j.ext_param, 0, nullptr};
     if (int st = bounds_record(&kp.ext.record)) return st;
@@ -655,7 +659,11 @@ int enqueue_update(const dopt_step_args* a) {
   cudaStream_t s = (cudaStream_t)a->stream;
   Range r("adamw");
   for (int32_t b = 0; b < (int32_t)m->buffers.size(); ++b) {
-    int st = run_k3_runs(runs_for(m, b, a->rank), step_job3(a, b), s);
+    // queued right behind the step's reduce pass or the previous buffer's
+    // AdamW pass, all in this call
+    K3Job j = step_job3(a, b);
+    j.early_state = true;
+    int st = run_k3_runs(runs_for(m, b, a->rank), j, s);
     if (st) return st;
   }
   return record_stage(a, 3, s);

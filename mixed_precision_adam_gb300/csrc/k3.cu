@@ -165,15 +165,13 @@ struct K3Tile {
   bool aligned;
 };
 
+// Where tile t lies: its run, its element count and its first element in
+// the flat shard (l0), in the param buffer (w0) and in the master array (m0:
+// the param buffer itself for fp32 params).  No loads.
 template <typename PT, typename MG, typename P>
-__device__ __forceinline__ void k3_load(const P& p, float* wbase, int t, int& si, K3Tile<MG>& T,
-                                        int& decay_si, float& decay, double lr_wd) {
+__device__ __forceinline__ void k3_place(const P& p, int t, int& si, K3Tile<MG>& T) {
   si = seek(p.tab, si, t);
   const Seg& sg = p.tab.seg[si];
-  if (si != decay_si) {
-    decay = decay_of(lr_wd, sg.wd_mult);
-    decay_si = si;
-  }
   const int64_t off = (int64_t)(t - sg.tile0) * kTile3;
   T.n = (int)min((int64_t)kTile3, (int64_t)sg.len - off);
   T.l0 = sg.local + off;
@@ -186,12 +184,27 @@ __device__ __forceinline__ void k3_load(const P& p, float* wbase, int t, int& si
                                     DOPT_RANGE_OK(p, kSiteK3Param, T.w0, T.n, param))))
     T.n = 0;
   T.aligned = seg_aligned(sg.local, sg.world);
+}
+
+// The weight-decay factor of the tile's run (recomputed only when the run
+// changes).
+template <typename MG, typename P>
+__device__ __forceinline__ void k3_decay(const P& p, int si, K3Tile<MG>& T, int& decay_si, float& decay,
+                                         double lr_wd) {
+  if (si != decay_si) {
+    decay = decay_of(lr_wd, p.tab.seg[si].wd_mult);
+    decay_si = si;
+  }
   T.decay = decay;
+}
+
+// The tile's master weights (or fp32 params), m and v.
+template <typename MG>
+__device__ __forceinline__ void k3_load_state(const K3Head& p, const float* wbase, K3Tile<MG>& T) {
 #pragma unroll
   for (int u = 0; u < kUnroll3; ++u) {
     const int e = (u * kThreads + threadIdx.x) * kVec;
     if (T.aligned && e + kVec <= T.n) {
-      T.g[u] = MainT<MG>::load4(p.main_grad, T.l0 + e);
       T.w[u] = __ldcs(reinterpret_cast<const float4*>(wbase + T.m0 + e));
       T.m[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg + T.l0 + e));
       T.v[u] = __ldcs(reinterpret_cast<const float4*>(p.exp_avg_sq + T.l0 + e));
@@ -199,19 +212,51 @@ __device__ __forceinline__ void k3_load(const P& p, float* wbase, int t, int& si
   }
 }
 
+// The tile's main grads.
+template <typename MG>
+__device__ __forceinline__ void k3_load_grad(const K3Head& p, K3Tile<MG>& T) {
+#pragma unroll
+  for (int u = 0; u < kUnroll3; ++u) {
+    const int e = (u * kThreads + threadIdx.x) * kVec;
+    if (T.aligned && e + kVec <= T.n) T.g[u] = MainT<MG>::load4(p.main_grad, T.l0 + e);
+  }
+}
+
+template <typename PT, typename MG, typename P>
+__device__ __forceinline__ void k3_load(const P& p, const float* wbase, int t, int& si, K3Tile<MG>& T,
+                                        int& decay_si, float& decay, double lr_wd) {
+  k3_place<PT, MG>(p, t, si, T);
+  k3_decay<MG>(p, si, T, decay_si, decay, lr_wd);
+  k3_load_grad<MG>(p, T);
+  k3_load_state<MG>(p, wbase, T);
+}
+
 template <typename PT, typename MG, int CAP>
 __global__ void __launch_bounds__(kThreads, DOPT_K3_MIN_BLOCKS) k3_adamw_pipe(const __grid_constant__ K3ParamsT<CAP> p) {
+  float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
+  int si = 0;
+  int t = blockIdx.x;
+  K3Tile<MG> cur;
+  // the first tile's master, m and v, which the launch before this one does
+  // not write, are loaded while that launch ends (its last CTA finalizes)
+  const bool early = p.early_state && t < p.tab.n_tiles;
+  if (early) {
+    k3_place<PT, MG>(p, t, si, cur);
+    k3_load_state<MG>(p, wbase, cur);
+  }
   wait_for_prior_grids();    // the reduce pass and its finalize are done
   if (*p.found_inf) return;  // skipped step: nothing is written
   const float c = *p.coef;
   const StepScalars ss = step_scalars(p);
-  float* const wbase = ParamT<PT>::kInPlace ? static_cast<float*>(p.param) : p.master;
-  int si = 0, decay_si = -1;
+  int decay_si = -1;
   float decay = 1.f;
-  int t = blockIdx.x;
   if (t >= p.tab.n_tiles) return;
-  K3Tile<MG> cur;
-  k3_load<PT, MG>(p, wbase, t, si, cur, decay_si, decay, ss.lr_wd);
+  if (early) {
+    k3_decay<MG>(p, si, cur, decay_si, decay, ss.lr_wd);
+    k3_load_grad<MG>(p, cur);
+  } else {
+    k3_load<PT, MG>(p, wbase, t, si, cur, decay_si, decay, ss.lr_wd);
+  }
   for (; t < p.tab.n_tiles; t += gridDim.x) {
     K3Tile<MG> nxt;
     const bool more = t + (int)gridDim.x < p.tab.n_tiles;

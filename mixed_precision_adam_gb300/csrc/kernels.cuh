@@ -272,6 +272,11 @@ struct K3Head {
   double lr_wd;        // lr * weight_decay (host step)
   float b1, b2, omb1, omb2, eps, step_size, bc2_sqrt;
   float inv_scale;     // compact main grads: main = widen(stored) * inv_scale
+  // 1: the launch before this one in the stream is a kernel of the same
+  // step that writes none of master, m and v here (the step's reduce pass,
+  // its finalize, or the AdamW pass of another buffer or bucket), so a CTA
+  // may load its first tile's master, m and v before waiting for it
+  int32_t early_state;
 #if DOPT_BOUNDS_CHECK
   Extents ext;
 #endif
