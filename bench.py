@@ -639,8 +639,8 @@ def run_ours(args):
 
     # device-resident timed region.  Inputs smaller than L2 (the toy MLP):
     # write a buffer of twice the L2 size between the timed steps and time
-    # each step from its own first to last stage event, so the flushes stay
-    # outside the timed work.  The step is timed as a caller runs it, with
+    # each step from the event before it to the event after it, so the
+    # flushes stay outside the timed work.  The step is timed as a caller runs it, with
     # events before and after it only: a timing event recorded between the
     # reduce pass and the AdamW pass waits for the reduce grid to drain and
     # stops the AdamW CTAs from starting early (about 6 us a step on the toy
