@@ -88,6 +88,44 @@ def test_run_table_capacity_boundary(n_runs, grad_fp32):
     _check(_tiny(params, 1, bucket_size=None, grad_reduce_in_fp32=grad_fp32, grad_sigma=1e-2))
 
 
+@pytest.mark.parametrize("name", ["llama_7b_dp8_rank0", "toy_mlp_dp4"])
+def test_state_rewritten_just_before_a_fused_step(name):
+    # a kernel that rewrites master (or the fp32 params), m and v is queued
+    # right before each fused step on the same stream, with no host
+    # synchronisation, and the step must read the new values: the AdamW
+    # pass loads its first tile's state ahead of its wait for the reduce
+    # pass, which stream order makes safe (the rewriting kernel ends before
+    # the reduce pass starts)
+    D = H.dopt()
+    cfg = W.mini(name)
+    hc = H.HostCase(cfg)
+    dc = H.DeviceCase(hc)
+    report = []
+    for t_step in (1, 2, 3):
+        grads = hc.grads(t_step)
+        t = hc.t_applied + 1
+        reps = [[dc._up(r) for r in g] for g in grads]
+        torch.cuda.synchronize()
+        if t_step > 1:  # exact rewrites: halving, quartering, negation
+            for b, st in enumerate(hc.state):
+                st["exp_avg"] *= np.float32(0.5)
+                dc.exp_avg[b].mul_(0.5)
+                st["exp_avg_sq"] *= np.float32(0.25)
+                dc.exp_avg_sq[b].mul_(0.25)
+                if "master" in st:
+                    st["master"] *= np.float32(-1.0)
+                    dc.master[b].mul_(-1.0)
+                else:
+                    hc.params[b] *= np.float32(-1.0)
+                    dc.params[b].mul_(-1.0)
+        before = H.snapshot(hc)
+        ores = hc.oracle_step(grads, t)
+        found, norm = D.dopt_step(dc.step_args(reps, t))
+        assert H.compare_step(hc, dc, ores, found, norm, before, report), "\n".join(report)
+        assert not found
+        hc.t_applied += 1
+
+
 def test_average_in_collective_and_hierarchy():
     params = W.llama(1, 128, 344, 257)
     _check(_tiny(params, 4, bucket_size=20000, average=True, steps=2))
