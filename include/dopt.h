@@ -296,7 +296,11 @@ typedef struct {
    * the norm finalize and after the AdamW pass, so a caller can time each
    * stage of the step with cudaEventElapsedTime.  In the fused step the
    * finalize runs inside the last reduce launch, so the second and third
-   * events are recorded back to back. */
+   * events are recorded back to back.  Any entry may be NULL (not
+   * recorded).  A timing event between the passes makes the AdamW pass
+   * wait for the reduce grid to drain before it launches (about 5 us per
+   * step, which only short steps notice); events 0 and 3 alone time the
+   * whole step without that cost. */
   void* const* stage_events;
   /* scale_gradients factor (per-token loss normalization, 1/num_tokens):
    * multiplies the reduced grads in the grad dtype (one rounding) before
