@@ -38,6 +38,9 @@ if ROOT not in sys.path:
 METRIC = "sharded Adam step params/s and HBM GB/s (% of GB300 peak), 1 GPU"
 UNIT = "params/s"
 DEFAULT_WORKLOAD = "llama_7b_dp8_rank0"
+# the other configurations of the method's workloads: the toy MLP, GPT-2
+# small, Llama-1.3B fp16, and the Llama-7B 2 x 8 hierarchy at 40M buckets
+OTHER_CONFIGS = "toy_mlp_dp4,gpt2_small_dp8,llama_1p3b_fp16_dp8,llama_7b_dp16_2x8_40m"
 CPU_SAMPLE_ELEMENTS = 32 * 2**20
 F32, BF16, F16 = 0, 1, 2
 ELEM_BYTES = {F32: 4, BF16: 2, F16: 2}
@@ -63,6 +66,9 @@ def parse_args(argv=None):
                    help="turn on the pre-reduction grad check (largest |g| per replica and bucket)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--other-configs", default=OTHER_CONFIGS,
+                   help="comma-separated workloads also timed (N=1 only) after the main one, "
+                        "each reported under other_configs; empty: none")
     p.add_argument("--graph", action="store_true",
                    help="time the step replayed from a CUDA graph (device step counter) "
                         "against dopt_step calls")
@@ -618,6 +624,104 @@ def barrier(world):
         dist.barrier()
 
 
+def timed_region(wl, sargs, steps, traced, local_rank, world):
+    """One device-resident timed region of `steps` steps of workload wl:
+    (elapsed ms, per-step events, kernel launches, clocks).  Untraced, each
+    step records only the events before and after it; traced, all four
+    stage events.  Inputs smaller than twice L2 get an L2 flush (a write,
+    then a read of another buffer as large) between the steps, outside the
+    timed work."""
+    import torch
+    D = wl.D
+    l2_bytes = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    rep_bytes = sum(r.numel() * r.element_size() for reps in wl.reps for r in reps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e4 in ev:  # torch creates the CUDA event on its first record
+        for e in e4:
+            e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if rep_bytes < 2 * l2_bytes else None
+    # after the write, a read of another buffer as large: L2 is left
+    # holding clean lines, so the step does not pay the write-back of
+    # the flush's own dirty lines
+    clean = torch.zeros(2 * l2_bytes // 8, dtype=torch.int64, device="cuda") if flush is not None else None
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = D.dopt_kernel_launches()
+    start.record()
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+            clean.sum()
+        wl.step(sargs, ev[i] if traced else [ev[i][0], None, None, ev[i][3]])
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = D.dopt_kernel_launches() - launches0
+    clocks.stop()
+    if flush is None:
+        elapsed = start.elapsed_time(end)
+    else:
+        elapsed = sum(e[0].elapsed_time(e[3]) for e in ev)
+    return elapsed, ev, launches, clocks.summary()
+
+
+def measured(wl, sargs, steps, traced, local_rank, world, rank):
+    """timed_region, taken once more when its clocks show a hardware or
+    thermal slowdown, or SM clocks held well below their maximum with no
+    reason given (a clock lock left behind); every rank decides alike.
+    Returns (the region, the first attempt's clocks or None)."""
+    out = timed_region(wl, sargs, steps, traced, local_rank, world)
+    if any_rank(clocks_rejected(out[3]), world):
+        log(f"[bench] rank {rank}: timed region taken again (clocks {out[3]})")
+        return timed_region(wl, sargs, steps, traced, local_rank, world), out[3]
+    return out, None
+
+
+def other_config(name, args, local_rank):
+    """One more workload timed like the main line's (device-resident step,
+    an untraced and a traced region of the same steps, L2 flushed between
+    steps when its inputs are smaller than twice L2), for the line's
+    `other_configs`.  Never raises: a failure is reported in the entry."""
+    import torch
+    out = {"workload": name}
+    try:
+        cfg = workload_config(name)
+        wl = Workload(cfg)
+        sargs = wl.args()
+        for _ in range(max(3, args.warmup)):
+            wl.step(sargs)
+        torch.cuda.synchronize()
+        steps = max(5, min(args.steps, 50))
+        (elapsed, _, launches, clk), first = measured(wl, sargs, steps, False, local_rank, 1, 0)
+        (_, sev, _, sclk), _ = measured(wl, sargs, steps, True, local_rank, 1, 0)
+        peak, _ = measured_peak_hbm()
+        ms = elapsed / steps
+        k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in sev)
+        k3 = statistics.mean(e[2].elapsed_time(e[3]) for e in sev)
+        l2_bytes = torch.cuda.get_device_properties(local_rank).L2_cache_size
+        rep_bytes = sum(r.numel() * r.element_size() for reps in wl.reps for r in reps)
+        out.update({
+            "config": line_config(cfg, wl.elements, rep_bytes, l2_bytes, False),
+            "value": wl.elements / (ms * 1e-3), "unit": UNIT, "steps": steps,
+            "ms_per_step": ms,
+            "hbm_frac": (wl.k1_bytes + wl.k3_bytes) / (ms * 1e-3) / 1e9 / peak,
+            "reduce_prepare_ms": k1, "reduce_prepare_frac": wl.k1_bytes / (k1 * 1e-3) / 1e9 / peak,
+            "adamw_ms": k3, "adamw_frac": wl.k3_bytes / (k3 * 1e-3) / 1e9 / peak,
+            "traced_ms_per_step": statistics.mean(e[0].elapsed_time(e[3]) for e in sev),
+            "gpu_launches": launches, "clocks": clk, "stage_clocks": sclk})
+        if first is not None:
+            out["remeasured"] = {"first_clocks": first}
+        del wl, sargs
+    except Exception as e:  # reported, so the main line still prints
+        out["error"] = f"{type(e).__name__}: {e}"[:300]
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -649,51 +753,8 @@ def run_ours(args):
     l2_bytes = torch.cuda.get_device_properties(local_rank).L2_cache_size
     rep_bytes = sum(r.numel() * r.element_size() for reps in wl.reps for r in reps)
 
-    def timed_region(traced):
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        for e4 in ev:  # torch creates the CUDA event on its first record
-            for e in e4:
-                e.record()
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if rep_bytes < 2 * l2_bytes else None
-        # after the write, a read of another buffer as large: L2 is left
-        # holding clean lines, so the step does not pay the write-back of
-        # the flush's own dirty lines
-        clean = torch.zeros(2 * l2_bytes // 8, dtype=torch.int64, device="cuda") if flush is not None else None
-        clocks = ClockSampler(local_rank)
-        time.sleep(0.3)
-        barrier(world)
-        torch.cuda.synchronize()
-        launches0 = D.dopt_kernel_launches()
-        start.record()
-        for i in range(args.steps):
-            if flush is not None:
-                flush.fill_(i & 0xFF)
-                clean.sum()
-            wl.step(sargs, ev[i] if traced else [ev[i][0], None, None, ev[i][3]])
-        end.record()
-        torch.cuda.synchronize()
-        barrier(world)
-        launches = D.dopt_kernel_launches() - launches0
-        clocks.stop()
-        if flush is None:
-            elapsed = start.elapsed_time(end)
-        else:
-            elapsed = sum(e[0].elapsed_time(e[3]) for e in ev)
-        return elapsed, ev, launches, clocks.summary()
-
-    # a run whose clocks show a hardware or thermal slowdown, or SM clocks
-    # held well below their maximum with no reason given (a clock lock left
-    # behind), is taken once more; every rank decides alike
-    def measured(traced):
-        out = timed_region(traced)
-        if any_rank(clocks_rejected(out[3]), world):
-            log(f"[bench] rank {rank}: timed region taken again (clocks {out[3]})")
-            return timed_region(traced), out[3]
-        return out, None
-
-    (elapsed, ev, launches, clk), first_clocks = measured(False)
-    (_, sev, _, sclk), first_sclocks = measured(True)
+    (elapsed, ev, launches, clk), first_clocks = measured(wl, sargs, args.steps, False, local_rank, world, rank)
+    (_, sev, _, sclk), first_sclocks = measured(wl, sargs, args.steps, True, local_rank, world, rank)
     k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in sev)
     k2 = statistics.mean(e[1].elapsed_time(e[2]) for e in sev)
     k3 = statistics.mean(e[2].elapsed_time(e[3]) for e in sev)
@@ -709,6 +770,7 @@ def run_ours(args):
     # host memory every step, then the C-ABI step, which reads back found_inf
     # and the norm
     e2e = None
+    eargs = None
     if not args.no_e2e:
         # distinct pinned host copies of every replica, unless all ranks' copies
         # would take more than half of the host's available memory: then each
@@ -809,6 +871,13 @@ def run_ours(args):
     }
     if first_clocks is not None or first_sclocks is not None:
         line["remeasured"] = {"first_clocks": first_clocks, "first_stage_clocks": first_sclocks}
+    names = [n for n in args.other_configs.split(",") if n] if world == 1 else []
+    if names:
+        # the other workloads, each in turn on its own, after the main one is freed
+        del sargs, wl, eargs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["other_configs"] = [other_config(n, args, local_rank) for n in names]
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -30,7 +30,7 @@ def _bench(*argv):
 
 def test_main_line_on_a_small_case():
     d = _bench("--layers", "2", "--steps", "5", "--warmup", "3", "--e2e-steps", "2",
-               "--no-cpu-baseline")
+               "--no-cpu-baseline", "--other-configs", "toy_mlp_dp4")
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "e2e", "gpu_launches", "clocks", "read_once_ideal"):
@@ -44,6 +44,13 @@ def test_main_line_on_a_small_case():
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert e["value"] < d["value"]  # the host copies are inside the end-to-end time
+    # one more workload, timed the same way after the main one
+    (o,) = d["other_configs"]
+    assert "error" not in o, o
+    assert o["workload"] == "toy_mlp_dp4" and o["value"] > 0 and o["ms_per_step"] > 0
+    assert 0 < o["hbm_frac"] and 0 < o["reduce_prepare_frac"] and 0 < o["adamw_frac"]
+    assert o["gpu_launches"] == 2 * o["steps"]  # one reduce and one AdamW launch a step
+    assert o["config"]["workload"].startswith("toy_mlp_dp4:")
 
 
 def test_graph_replay_line():
