@@ -717,8 +717,11 @@ def other_config(name, args, local_rank):
         del wl, sargs
     except Exception as e:  # reported, so the main line still prints
         out["error"] = f"{type(e).__name__}: {e}"[:300]
-    torch.cuda.synchronize()
-    torch.cuda.empty_cache()
+    try:
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    except Exception as e:
+        out.setdefault("error", f"{type(e).__name__}: {e}"[:300])
     return out
 
 

@@ -97,3 +97,18 @@ def test_read_once_ideal_is_4n_plus_26_bytes():
         assert bench.read_once_bytes(D, pm, dp, list(range(dp))) == want * (1 << 16)
     pm = D.dopt_build_shard_map([dict(numel=4096, dtype=D.F32)], 4, 0, True, False)
     assert bench.read_once_bytes(D, pm, 4, [1]) == (4 * 4 + 24) * 1024
+
+
+def test_other_configs_default_and_failure_entry():
+    """The default line times the four other workloads; a workload that
+    cannot be timed gives an entry with its error instead of raising, so the
+    main line still prints."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth import workloads as W
+    names = bench.parse_args([]).other_configs.split(",")
+    assert len(names) == 4 and bench.DEFAULT_WORKLOAD not in names
+    assert all(n in W.NAMES for n in names)
+    assert bench.parse_args(["--other-configs", ""]).other_configs == ""
+    out = bench.other_config("no_such_workload", bench.parse_args([]), 0)
+    assert out["workload"] == "no_such_workload" and "KeyError" in out["error"]
